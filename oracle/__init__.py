@@ -1,0 +1,149 @@
+"""Float64 CPU oracle for causal grouped-query attention (TEST INFRASTRUCTURE).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may import this package.  The CUDA
+library never calls it and shares no code with it.
+
+The arithmetic lives in ``gqa_oracle.c`` (plain C, float64, OpenMP); this
+module only compiles it with gcc on first use and marshals numpy arrays.
+What it computes is stated in the C file's header: the definition printed in
+"nx_f32_gqa_gate.nx source" (scores, causal mask, softmax, attn.V, the GQA
+head map of test T2, the softmax backward of test T4) plus the window/sink
+mask and the backward named in "SnapKitty Transformer 8B".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gqa_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libgqa_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH, defines=()) -> str:
+    """Compile the oracle with gcc (-O2, no fast-math, OpenMP).  Returns the .so path."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-fno-fast-math",
+           *[f"-D{d}" for d in defines], src, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _declare(lib):
+    dp = ctypes.POINTER(ctypes.c_double)
+    lp = ctypes.POINTER(ctypes.c_long)
+    i, d = ctypes.c_int, ctypes.c_double
+    lib.oracle_visible.argtypes = [ctypes.c_long, ctypes.c_long, i, i, i]
+    lib.oracle_visible.restype = i
+    lib.oracle_attn_fwd.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, i, i, i, d]
+    lib.oracle_attn_fwd.restype = None
+    lib.oracle_attn_fwd_rows.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, i, i, i, d, lp, i]
+    lib.oracle_attn_fwd_rows.restype = None
+    lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, i, i, i, i, i, i, i, i, d]
+    lib.oracle_attn_bwd.restype = None
+    lib.oracle_attn_bwd_group.argtypes = [dp, dp, dp, dp, dp, dp, dp,
+                                          i, i, i, i, i, i, i, i, d, i, i]
+    lib.oracle_attn_bwd_group.restype = None
+    return lib
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) the oracle library; a custom path loads a variant."""
+    global _lib
+    if path is not None:
+        return _declare(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            _lib = _declare(ctypes.CDLL(build()))
+    return _lib
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _shape(q, k):
+    B, H, S, d = q.shape
+    Bk, G, Sk, dk = k.shape
+    assert (B, S, d) == (Bk, Sk, dk) and H % G == 0, "q [B,H,S,d] / k,v [B,G,S,d] with H % G == 0"
+    return B, H, G, S, d
+
+
+def attn_fwd(q, k, v, *, causal=True, window=0, n_sink=0, scale=None, lib=None):
+    """Full forward.  q [B,H,S,d], k/v [B,G,S,d] -> (o [B,H,S,d], lse [B,H,S]) in float64."""
+    lib = lib or load()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, G, S, d = _shape(q, k)
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    o = np.zeros((B, H, S, d))
+    lse = np.zeros((B, H, S))
+    lib.oracle_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                        B, H, G, S, d, int(causal), int(window), int(n_sink), scale)
+    return o, lse
+
+
+def attn_fwd_rows(q, k, v, rows, *, causal=True, window=0, n_sink=0, scale=None, lib=None):
+    """Forward on sampled rows (b, h, i) only -> (o_rows [n,d], lse_rows [n])."""
+    lib = lib or load()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, G, S, d = _shape(q, k)
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+    n = rows.shape[0]
+    o = np.zeros((n, d))
+    lse = np.zeros(n)
+    lib.oracle_attn_fwd_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                             B, H, G, S, d, int(causal), int(window), int(n_sink), scale,
+                             rows.ctypes.data_as(ctypes.POINTER(ctypes.c_long)), n)
+    return o, lse
+
+
+def attn_bwd(q, k, v, dO, *, causal=True, window=0, n_sink=0, scale=None, lib=None):
+    """Full backward (exact P recomputed by the oracle) -> (dq, dk, dv) in float64."""
+    lib = lib or load()
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    B, H, G, S, d = _shape(q, k)
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    dq = np.zeros((B, H, S, d))
+    dk = np.zeros((B, G, S, d))
+    dv = np.zeros((B, G, S, d))
+    lib.oracle_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv),
+                        B, H, G, S, d, int(causal), int(window), int(n_sink), scale)
+    return dq, dk, dv
+
+
+def attn_bwd_group(q, k, v, dO, b, g, *, causal=True, window=0, n_sink=0, scale=None, lib=None):
+    """Backward of one kv group -> (dq of its R heads [R,S,d], dk [S,d], dv [S,d])."""
+    lib = lib or load()
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    B, H, G, S, d = _shape(q, k)
+    R = H // G
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    dq = np.zeros((R, S, d))
+    dk = np.zeros((S, d))
+    dv = np.zeros((S, d))
+    lib.oracle_attn_bwd_group(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv),
+                              B, H, G, S, d, int(causal), int(window), int(n_sink), scale,
+                              int(b), int(g))
+    return dq, dk, dv
+
+
+def visible(i: int, j: int, *, causal=True, window=0, n_sink=0, lib=None) -> bool:
+    lib = lib or load()
+    return bool(lib.oracle_visible(int(i), int(j), int(causal), int(window), int(n_sink)))
