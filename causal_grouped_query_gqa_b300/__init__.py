@@ -1,0 +1,31 @@
+"""libgqa_attn Python binding: causal grouped-query attention on one B300.
+
+The compute path is the C-ABI library ``libgqa_attn.so`` (hand-written CUDA for
+sm_103a, declared in ``include/gqa_attn.h``).  This module only marshals
+arguments: torch provides device memory and the current stream, and every step
+of the attention runs in the library's kernels.  There is no fallback: if the
+library is missing or cannot be loaded, every call raises.
+
+Low-level calls (same names and argument order as the C header):
+    gqa_attn_fwd(q, k, v, o, lse, B, H, G, S, d, causal, window, n_sink, scale, stream)
+    gqa_attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, G, S, d, causal, window,
+                 n_sink, scale, workspace, workspace_bytes, stream)
+    gqa_attn_bwd_workspace_size(B, H, G, S, d)
+    gqa_attn_strerror(status), gqa_attn_last_device_status(stream)
+Tensor helpers: ``fwd(q, k, v, ...)`` and ``bwd(q, k, v, o, dout, lse, ...)``.
+"""
+from __future__ import annotations
+
+from ._lib import (GQA_ERR_ALIGN, GQA_ERR_CUDA, GQA_ERR_DEVICE_TIMEOUT, GQA_ERR_HEADDIM,
+                   GQA_ERR_MASK, GQA_ERR_NULL, GQA_ERR_SCALE, GQA_ERR_SHAPE,
+                   GQA_ERR_WORKSPACE, GQA_OK, GqaError, bwd, fwd, gqa_attn_bwd,
+                   gqa_attn_bwd_workspace_size, gqa_attn_fwd, gqa_attn_last_device_status,
+                   gqa_attn_strerror, lib_path, load_library)
+
+__all__ = [
+    "fwd", "bwd", "gqa_attn_fwd", "gqa_attn_bwd", "gqa_attn_bwd_workspace_size",
+    "gqa_attn_strerror", "gqa_attn_last_device_status", "load_library", "lib_path", "GqaError",
+    "GQA_OK", "GQA_ERR_NULL", "GQA_ERR_SHAPE", "GQA_ERR_HEADDIM", "GQA_ERR_ALIGN",
+    "GQA_ERR_MASK", "GQA_ERR_SCALE", "GQA_ERR_WORKSPACE", "GQA_ERR_CUDA",
+    "GQA_ERR_DEVICE_TIMEOUT",
+]

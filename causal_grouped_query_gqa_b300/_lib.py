@@ -1,0 +1,159 @@
+"""ctypes marshalling for libgqa_attn.so (see include/gqa_attn.h for the contract)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libgqa_attn.so")
+_lock = threading.Lock()
+_lib = None
+
+GQA_OK = 0
+GQA_ERR_NULL = -1
+GQA_ERR_SHAPE = -2
+GQA_ERR_HEADDIM = -3
+GQA_ERR_ALIGN = -4
+GQA_ERR_MASK = -5
+GQA_ERR_SCALE = -6
+GQA_ERR_WORKSPACE = -7
+GQA_ERR_CUDA = -8
+GQA_ERR_DEVICE_TIMEOUT = -9
+
+
+class GqaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {gqa_attn_strerror(status)} (status {status})")
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Loads the in-tree CUDA library; raises if it is absent (no fallback exists)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is missing: build it with "
+                "`python -m causal_grouped_query_gqa_b300.build` (nvcc, sm_103a)")
+        lib = ctypes.CDLL(_LIB_PATH)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.gqa_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp]
+        lib.gqa_attn_fwd.restype = i
+        lib.gqa_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                     i, i, i, i, i, i, i, i, f, vp, sz, vp]
+        lib.gqa_attn_bwd.restype = i
+        lib.gqa_attn_bwd_workspace_size.argtypes = [i, i, i, i, i]
+        lib.gqa_attn_bwd_workspace_size.restype = sz
+        lib.gqa_attn_strerror.argtypes = [i]
+        lib.gqa_attn_strerror.restype = ctypes.c_char_p
+        lib.gqa_attn_last_device_status.argtypes = [vp]
+        lib.gqa_attn_last_device_status.restype = i
+        _lib = lib
+        return lib
+
+
+def _p(x):
+    """Device address of a tensor (or an int address / None)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ----------------------------------------------------------- C-ABI mirrors ---
+
+def gqa_attn_fwd(q, k, v, o, lse, B, H, G, S, d, causal, window, n_sink, scale, stream=None):
+    return load_library().gqa_attn_fwd(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, G, S, d,
+                                       int(causal), int(window), int(n_sink), float(scale),
+                                       _stream(stream))
+
+
+def gqa_attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, G, S, d, causal, window, n_sink,
+                 scale, workspace, workspace_bytes, stream=None):
+    return load_library().gqa_attn_bwd(_p(q), _p(k), _p(v), _p(o), _p(dout), _p(lse), _p(dq),
+                                       _p(dk), _p(dv), B, H, G, S, d, int(causal), int(window),
+                                       int(n_sink), float(scale), _p(workspace),
+                                       int(workspace_bytes), _stream(stream))
+
+
+def gqa_attn_bwd_workspace_size(B, H, G, S, d):
+    return load_library().gqa_attn_bwd_workspace_size(B, H, G, S, d)
+
+
+def gqa_attn_strerror(status: int) -> str:
+    return load_library().gqa_attn_strerror(int(status)).decode()
+
+
+def gqa_attn_last_device_status(stream=None) -> int:
+    return load_library().gqa_attn_last_device_status(_stream(stream))
+
+
+# --------------------------------------------------------- tensor helpers ---
+
+def _check(t, shape, dtype, name):
+    import torch
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name}: expected contiguous CUDA {dtype} {tuple(shape)}, "
+                         f"got {t.dtype} {tuple(t.shape)} on {t.device}")
+    return torch
+
+
+def fwd(q, k, v, *, causal=True, window=0, n_sink=0, scale=None, out=None, lse=None,
+        stream=None):
+    """o, lse = fwd(q [B,H,S,64] bf16, k/v [B,G,S,64] bf16) on the current CUDA stream."""
+    import torch
+    B, H, S, d = q.shape
+    G = k.shape[1]
+    _check(q, (B, H, S, d), torch.bfloat16, "q")
+    _check(k, (B, G, S, d), torch.bfloat16, "k")
+    _check(v, (B, G, S, d), torch.bfloat16, "v")
+    scale = 1.0 / d ** 0.5 if scale is None else scale
+    o = torch.empty_like(q) if out is None else out
+    l = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if lse is None else lse
+    rc = gqa_attn_fwd(q, k, v, o, l, B, H, G, S, d, causal, window, n_sink, scale, stream)
+    if rc != GQA_OK:
+        raise GqaError(rc, "gqa_attn_fwd")
+    return o, l
+
+
+def bwd(q, k, v, o, dout, lse, *, causal=True, window=0, n_sink=0, scale=None,
+        workspace=None, stream=None):
+    """dq, dk, dv = bwd(q, k, v, o, dout, lse) (o and lse from fwd)."""
+    import torch
+    B, H, S, d = q.shape
+    G = k.shape[1]
+    _check(q, (B, H, S, d), torch.bfloat16, "q")
+    _check(k, (B, G, S, d), torch.bfloat16, "k")
+    _check(v, (B, G, S, d), torch.bfloat16, "v")
+    _check(o, (B, H, S, d), torch.bfloat16, "o")
+    _check(dout, (B, H, S, d), torch.bfloat16, "dout")
+    _check(lse, (B, H, S), torch.float32, "lse")
+    scale = 1.0 / d ** 0.5 if scale is None else scale
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    need = gqa_attn_bwd_workspace_size(B, H, G, S, d)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    rc = gqa_attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, G, S, d, causal, window, n_sink,
+                      scale, workspace, workspace.numel() * workspace.element_size(), stream)
+    if rc != GQA_OK:
+        raise GqaError(rc, "gqa_attn_bwd")
+    return dq, dk, dv

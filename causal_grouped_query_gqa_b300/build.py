@@ -1,0 +1,57 @@
+"""Builds libgqa_attn.so in-tree with nvcc for sm_103a.
+
+    python -m causal_grouped_query_gqa_b300.build [--force]
+
+The library is plain CUDA C++ with an extern "C" interface (include/gqa_attn.h);
+the CUDA runtime is linked statically, and the driver's tensor-map encoder is
+fetched at run time, so the .so loads on a machine without a GPU.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import os
+import subprocess
+import sys
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+LIB = os.path.join(PKG, "libgqa_attn.so")
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def nvcc_cmd(out: str = LIB, extra=()):
+    return ["nvcc", *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
+            "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr",
+            "-I", os.path.join(ROOT, "include"), *extra,
+            os.path.join(CSRC, "gqa_attn_api.cu"), "-o", out, "-cudart", "static"]
+
+
+def sources():
+    return glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cuh")) + \
+        glob.glob(os.path.join(ROOT, "include", "*.h")) + [os.path.abspath(__file__)]
+
+
+def build(force: bool = False, verbose: bool = False, out: str = LIB, extra=()) -> str:
+    if not force and os.path.exists(out):
+        newest = max(os.path.getmtime(s) for s in sources())
+        if os.path.getmtime(out) >= newest:
+            return out
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = nvcc_cmd(tmp, extra)
+    if verbose:
+        cmd.insert(1, "-Xptxas=-v")
+        print(" ".join(cmd), flush=True)
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+if __name__ == "__main__":
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--force", action="store_true")
+    ap.add_argument("--verbose", action="store_true")
+    a = ap.parse_args()
+    print(build(force=a.force, verbose=a.verbose))
+    sys.exit(0)

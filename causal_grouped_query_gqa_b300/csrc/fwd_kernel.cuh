@@ -1,0 +1,463 @@
+// fwd_kernel.cuh -- forward of causal grouped-query attention on sm_103a.
+//
+// Computes, for each query row i of head h (kv head g = h / (H/G)):
+//   o_i = softmax_j(scale * q_i . k_j, visible j) . V,   lse_i = ln sum_j exp(scale * q_i . k_j)
+// ("nx_f32_gqa_gate.nx source": scores, causal mask, softmax, attn.V and the
+// head map of test T2; "SnapKitty Transformer 8B": online softmax over K/V
+// tiles, sliding window and attention sinks.)
+//
+// One CTA = one work unit = (batch b, kv head g, 128-row query block qb) x two
+// query heads of g.  Both heads read every K/V tile the CTA loads, so each tile
+// crosses HBM/L2 once per pair of heads.  Only key tiles with at least one
+// visible key are visited (sink tiles, then the window / causal range), and the
+// elementwise mask runs only on tiles that straddle a mask boundary.
+//
+// Roles (384 threads):
+//   warp 0        TMA producer: Q tiles once, then K and V tiles through an
+//                 NSTAGE-deep shared-memory ring (full/empty mbarriers).
+//   warp 1        MMA issuer (one thread): S_t = Q_t K^T into TMEM, then
+//                 O_t += P_t V with P_t read from TMEM (or shared memory).
+//   warp 2        allocates / frees the 512 TMEM columns.
+//   warps 4..7    softmax + O correction + epilogue of head 0 (one row per thread)
+//   warps 8..11   the same for head 1
+// TMEM columns: S0 [0,128) S1 [128,256) O0 [256,320) O1 [320,384); P_t (bf16
+// pairs) overwrites the first 64 columns of S_t once S_t has been read.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "sm100_ptx.cuh"
+
+namespace gqa {
+namespace fwd {
+
+constexpr int BM = 128;  // query rows per tile
+constexpr int BN = 128;  // keys per tile
+constexpr int HD = 64;   // head dimension
+constexpr int NSTAGE = 3;
+constexpr int TILE_BYTES = BM * HD * 2;  // 16 KB, 128-byte rows
+constexpr int NTHREADS = 384;
+constexpr uint32_t TMEM_COLS = 512;
+__device__ __forceinline__ uint32_t col_s(int t) { return static_cast<uint32_t>(t) * 128u; }
+__device__ __forceinline__ uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(t) * 64u; }
+
+constexpr int SM_Q = 0;
+constexpr int SM_K = SM_Q + 2 * TILE_BYTES;
+constexpr int SM_V = SM_K + NSTAGE * TILE_BYTES;
+constexpr int SM_P = SM_V + NSTAGE * TILE_BYTES;  // P tiles when P goes through smem
+
+template <bool P_TMEM>
+constexpr int bars_offset() {
+  return P_TMEM ? SM_P : SM_P + 2 * 2 * TILE_BYTES;
+}
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t k_full[NSTAGE];
+  uint64_t k_empty[NSTAGE];
+  uint64_t v_full[NSTAGE];
+  uint64_t v_empty[NSTAGE];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_full;
+  uint32_t tmem_base;
+  AbortState abort;
+};
+
+template <bool P_TMEM>
+constexpr int smem_bytes() {
+  return 1024 /* alignment slack */ + bars_offset<P_TMEM>() + static_cast<int>(sizeof(Bars));
+}
+
+struct Params {
+  int B, H, G, S, R;
+  int causal, window, n_sink;
+  float scale_log2;  // scale * log2(e): scores are kept in the base-2 domain
+  int n_qblocks;
+  int n_pairs;  // ceil(R / 2) head pairs per kv head
+  __nv_bfloat16 *o;
+  float *lse;
+  int *status;
+};
+
+enum : int { kTimeoutCode = -9 };
+
+// Key tiles a query block visits: [0, n_sink_tiles) then [wlo, hi].
+struct KvRange {
+  int n_sink_tiles;
+  int wlo;
+  int count;
+  __device__ __forceinline__ int tile(int idx) const {
+    return idx < n_sink_tiles ? idx : wlo + (idx - n_sink_tiles);
+  }
+};
+
+__device__ __forceinline__ KvRange kv_range(int qb, const Params &p) {
+  const int nkb = (p.S + BN - 1) / BN;
+  KvRange r;
+  r.n_sink_tiles = 0;
+  r.wlo = 0;
+  if (!p.causal) {
+    r.count = nkb;
+    return r;
+  }
+  const int i0 = qb * BM;
+  const int hi = min((i0 + BM - 1) / BN, nkb - 1);
+  if (p.window <= 0) {
+    r.count = hi + 1;
+    return r;
+  }
+  const int lo_key = i0 - p.window + 1;  // oldest key any row of the block sees in-window
+  const int wlo = lo_key <= 0 ? 0 : lo_key / BN;
+  const int nst = min((p.n_sink + BN - 1) / BN, wlo);
+  r.n_sink_tiles = nst;
+  r.wlo = wlo;
+  r.count = nst + hi - wlo + 1;
+  return r;
+}
+
+// True when some (row, key) pair of the tile is masked, so the elementwise
+// mask must run.
+__device__ __forceinline__ bool tile_needs_mask(int qb, int kb, const Params &p) {
+  const int i0 = qb * BM, j0 = kb * BN, j1 = j0 + BN - 1;
+  if (j1 >= p.S) return true;
+  if (!p.causal) return false;
+  if (j1 > i0) return true;
+  if (p.window > 0) {
+    const bool all_in_window = j0 > i0 + BM - 1 - p.window;
+    const bool all_sinks = j1 < p.n_sink;
+    if (!all_in_window && !all_sinks) return true;
+  }
+  return false;
+}
+
+template <bool P_TMEM>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    gqa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                   const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  Bars *bars = reinterpret_cast<Bars *>(smem + bars_offset<P_TMEM>());
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work unit: heaviest (latest) query blocks first
+  const int per_qb = p.B * p.G * p.n_pairs;
+  const int u = blockIdx.x;
+  const int qb = p.n_qblocks - 1 - u / per_qb;
+  const int rem = u % per_qb;
+  const int b = rem / (p.G * p.n_pairs);
+  const int g = (rem / p.n_pairs) % p.G;
+  const int pair = rem % p.n_pairs;
+  const int h0 = g * p.R + 2 * pair;
+  const bool two = (2 * pair + 1) < p.R;
+  const KvRange kr = kv_range(qb, p);
+  const int n = kr.count;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_full[t], 128);
+    }
+    mbar_init(&bars->o_full, 1);
+    bars->abort.flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(&bars->tmem_base, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tbase = bars->tmem_base;
+  AbortState *ab = &bars->abort;
+
+  if (warp == 0) {
+    // ================================================================ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      const int qrow = qb * BM;
+      mbar_arrive_expect_tx(&bars->q_full, (two ? 2 : 1) * TILE_BYTES);
+      tma_load_3d(smem + SM_Q, &tm_q, &bars->q_full, 0, qrow, b * p.H + h0);
+      if (two) tma_load_3d(smem + SM_Q + TILE_BYTES, &tm_q, &bars->q_full, 0, qrow, b * p.H + h0 + 1);
+      const int kvz = b * p.G + g;
+      int issued = 0;
+      for (int it = 0; it < n; ++it) {
+        const int st = it % NSTAGE;
+        const uint32_t ph = (it / NSTAGE) & 1;
+        const int kb = kr.tile(it);
+        if (!mbar_wait(&bars->k_empty[st], ph ^ 1, ab, p.status, kTimeoutCode)) break;
+        mbar_arrive_expect_tx(&bars->k_full[st], TILE_BYTES);
+        tma_load_3d(smem + SM_K + st * TILE_BYTES, &tm_k, &bars->k_full[st], 0, kb * BN, kvz);
+        if (!mbar_wait(&bars->v_empty[st], ph ^ 1, ab, p.status, kTimeoutCode)) {
+          issued = it + 1;  // K of this tile is in flight, V is not
+          mbar_wait_drain(&bars->k_full[st], ph);
+          issued = it;  // drained
+          break;
+        }
+        mbar_arrive_expect_tx(&bars->v_full[st], TILE_BYTES);
+        tma_load_3d(smem + SM_V + st * TILE_BYTES, &tm_v, &bars->v_full[st], 0, kb * BN, kvz);
+        issued = it + 1;
+      }
+      // Exit drain: every copy this CTA issued must have landed before the CTA
+      // leaves (no-op on the normal path, where the consumers already saw them).
+      mbar_wait_drain(&bars->q_full, 0);
+      for (int it = max(0, issued - NSTAGE); it < issued; ++it) {
+        const int st = it % NSTAGE;
+        const uint32_t ph = (it / NSTAGE) & 1;
+        mbar_wait_drain(&bars->k_full[st], ph);
+        mbar_wait_drain(&bars->v_full[st], ph);
+      }
+    }
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false, false);
+      const uint32_t idesc_pv = idesc_bf16_f32(BM, HD, false, true);
+      const uint32_t q_addr0 = smem_u32(smem + SM_Q);
+      const uint32_t k_addr0 = smem_u32(smem + SM_K);
+      const uint32_t v_addr0 = smem_u32(smem + SM_V);
+      const uint32_t p_addr0 = smem_u32(smem + SM_P);
+
+      auto issue_qk = [&](int t, int st) {
+        const uint64_t ad = sdesc_sw128(q_addr0 + t * TILE_BYTES, 16, 1024);
+        const uint64_t bd = sdesc_sw128(k_addr0 + st * TILE_BYTES, 16, 1024);
+#pragma unroll
+        for (int ks = 0; ks < HD / 16; ++ks)  // K step 16 bf16 = 32 B inside the 128-B row
+          mma_bf16_ss(tbase + col_s(t), ad + 2 * ks, bd + 2 * ks, idesc_qk, ks > 0);
+        mma_commit(&bars->s_full[t]);
+      };
+      auto issue_pv = [&](int t, int st, bool acc) {
+        const uint64_t bd = sdesc_sw128(v_addr0 + st * TILE_BYTES, TILE_BYTES, 1024);
+#pragma unroll
+        for (int ks = 0; ks < BN / 16; ++ks) {  // 16 keys = two 8-row groups = 2048 B
+          const uint32_t acc_k = (acc || ks > 0) ? 1u : 0u;
+          if constexpr (P_TMEM) {
+            mma_bf16_ts(tbase + col_o(t), tbase + col_s(t) + ks * 8, bd + (ks * 2048 >> 4),
+                        idesc_pv, acc_k);
+          } else {
+            const uint32_t pa = p_addr0 + t * 2 * TILE_BYTES + (ks / 4) * TILE_BYTES + (ks % 4) * 32;
+            mma_bf16_ss(tbase + col_o(t), sdesc_sw128(pa, 16, 1024), bd + (ks * 2048 >> 4),
+                        idesc_pv, acc_k);
+          }
+        }
+      };
+
+      bool ok = mbar_wait(&bars->q_full, 0, ab, p.status, kTimeoutCode);
+      ok = ok && mbar_wait(&bars->k_full[0], 0, ab, p.status, kTimeoutCode);
+      if (ok) {
+        tc_fence_after_sync();
+        issue_qk(0, 0);
+        if (two) issue_qk(1, 0);
+        mma_commit(&bars->k_empty[0]);
+        for (int it = 0; it < n; ++it) {
+          const int st = it % NSTAGE;
+          const uint32_t ph = (it / NSTAGE) & 1;
+          const uint32_t pp = it & 1;
+          const bool more = it + 1 < n;
+          const int st2 = (it + 1) % NSTAGE;
+          const uint32_t ph2 = ((it + 1) / NSTAGE) & 1;
+          if (!mbar_wait(&bars->v_full[st], ph, ab, p.status, kTimeoutCode)) { ok = false; break; }
+          if (!mbar_wait(&bars->p_full[0], pp, ab, p.status, kTimeoutCode)) { ok = false; break; }
+          tc_fence_after_sync();
+          issue_pv(0, st, it > 0);
+          if (more) {
+            if (!mbar_wait(&bars->k_full[st2], ph2, ab, p.status, kTimeoutCode)) { ok = false; break; }
+            tc_fence_after_sync();
+            issue_qk(0, st2);
+          }
+          if (two) {
+            if (!mbar_wait(&bars->p_full[1], pp, ab, p.status, kTimeoutCode)) { ok = false; break; }
+            tc_fence_after_sync();
+            issue_pv(1, st, it > 0);
+          }
+          mma_commit(&bars->v_empty[st]);
+          if (more) {
+            if (two) issue_qk(1, st2);
+            mma_commit(&bars->k_empty[st2]);
+          }
+        }
+      }
+      // Final commit: on the normal path it releases the epilogue; on the abort
+      // path it lets this thread wait until the tensor pipe is idle before TMEM
+      // is freed.
+      mma_commit(&bars->o_full);
+      if (!ok) mbar_wait_drain(&bars->o_full, 0);
+    }
+  } else if (warp >= 4) {
+    // ================================================================ softmax
+    const int t = (warp - 4) >> 2;
+    if (t == 0 || two) {
+      const int lane_base = 32 * (warp & 3);
+      const int r = lane_base + lane;  // row of the tile this thread owns
+      const int i = qb * BM + r;       // query index
+      const float sl2 = p.scale_log2;
+      // mask bounds: key j visible iff j <= hi && (j > lo || j < ns)
+      const int hi = p.causal ? min(i, p.S - 1) : p.S - 1;
+      const bool win = p.causal && p.window > 0;
+      const int lo = win ? i - p.window : -1;
+      const int ns = win ? p.n_sink : 0;
+      const uint32_t t_s = tbase + (static_cast<uint32_t>(lane_base) << 16) + col_s(t);
+      const uint32_t t_o = tbase + (static_cast<uint32_t>(lane_base) << 16) + col_o(t);
+      uint8_t *p_smem = smem + SM_P + t * 2 * TILE_BYTES;
+
+      float m_run = -CUDART_INF_F;  // running max of scaled scores, base-2 units
+      float l_run = 0.f;            // running sum of 2^(s - m_run)
+      bool ok = true;
+      for (int it = 0; it < n; ++it) {
+        const int kb = kr.tile(it);
+        if (!mbar_wait(&bars->s_full[t], it & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        tc_fence_after_sync();
+        float s[BN];
+        {
+          uint32_t r0[32], r1[32], r2[32], r3[32];
+          tmem_ld_32x32b_x32(t_s + 0, r0);
+          tmem_ld_32x32b_x32(t_s + 32, r1);
+          tmem_ld_32x32b_x32(t_s + 64, r2);
+          tmem_ld_32x32b_x32(t_s + 96, r3);
+          tmem_wait_ld();
+          reg_fence(r0);
+          reg_fence(r1);
+          reg_fence(r2);
+          reg_fence(r3);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            s[c] = __uint_as_float(r0[c]);
+            s[32 + c] = __uint_as_float(r1[c]);
+            s[64 + c] = __uint_as_float(r2[c]);
+            s[96 + c] = __uint_as_float(r3[c]);
+          }
+        }
+        if (tile_needs_mask(qb, kb, p)) {
+          const int j0 = kb * BN;
+#pragma unroll
+          for (int c = 0; c < BN; ++c) {
+            const int j = j0 + c;
+            const bool vis = (j <= hi) && (j > lo || j < ns);
+            s[c] = vis ? s[c] : -CUDART_INF_F;
+          }
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int c = 1; c < BN; ++c) mx = fmaxf(mx, s[c]);
+        const float m_new = fmaxf(m_run, mx * sl2);
+        const float m_use = (m_new == -CUDART_INF_F) ? 0.f : m_new;
+        const float alpha = ex2_approx(m_run - m_use);
+        float sum = 0.f;
+#pragma unroll
+        for (int c = 0; c < BN; ++c) {
+          s[c] = ex2_approx(fmaf(s[c], sl2, -m_use));
+          sum += s[c];
+        }
+        // P (bf16) for the P.V product
+        if constexpr (P_TMEM) {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(s[half * 64 + 2 * c], s[half * 64 + 2 * c + 1]);
+            tmem_st_32x32b_x32(t_s + half * 32, pk);
+          }
+        } else {
+          // 128-byte-swizzled K-major tile: row r, 16-byte chunk c of the
+          // 64-key sub-tile lands at chunk (c ^ (r & 7)).
+#pragma unroll
+          for (int ch = 0; ch < 16; ++ch) {
+            const int sub = ch >> 3, cc = ch & 7;
+            uint4 w;
+            w.x = pack_bf16x2(s[ch * 8 + 0], s[ch * 8 + 1]);
+            w.y = pack_bf16x2(s[ch * 8 + 2], s[ch * 8 + 3]);
+            w.z = pack_bf16x2(s[ch * 8 + 4], s[ch * 8 + 5]);
+            w.w = pack_bf16x2(s[ch * 8 + 6], s[ch * 8 + 7]);
+            *reinterpret_cast<uint4 *>(p_smem + sub * TILE_BYTES + r * 128 + ((cc ^ (r & 7)) << 4)) = w;
+          }
+        }
+        // O correction: rescale the accumulator when the row max grew.  S_t of
+        // this tile was committed after P.V of the previous tile, so O_t is final
+        // for the previous tile here.
+        if (it > 0) {
+          const bool need = alpha != 1.f;
+          if (__any_sync(0xffffffffu, need)) {
+            uint32_t o0[32], o1[32];
+            tmem_ld_32x32b_x32(t_o + 0, o0);
+            tmem_ld_32x32b_x32(t_o + 32, o1);
+            tmem_wait_ld();
+            reg_fence(o0);
+            reg_fence(o1);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              o0[c] = __float_as_uint(__uint_as_float(o0[c]) * alpha);
+              o1[c] = __float_as_uint(__uint_as_float(o1[c]) * alpha);
+            }
+            tmem_st_32x32b_x32(t_o + 0, o0);
+            tmem_st_32x32b_x32(t_o + 32, o1);
+          }
+        }
+        tmem_wait_st();
+        if constexpr (!P_TMEM) fence_proxy_async_smem();
+        tc_fence_before_sync();
+        mbar_arrive(&bars->p_full[t]);
+        l_run = l_run * alpha + sum;
+        m_run = m_new;
+      }
+      if (ok && mbar_wait(&bars->o_full, 0, ab, p.status, kTimeoutCode)) {
+        tc_fence_after_sync();
+        uint32_t o0[32], o1[32];
+        tmem_ld_32x32b_x32(t_o + 0, o0);
+        tmem_ld_32x32b_x32(t_o + 32, o1);
+        tmem_wait_ld();
+        reg_fence(o0);
+        reg_fence(o1);
+        if (i < p.S) {
+          const int h = h0 + t;
+          const float inv_l = 1.f / l_run;
+          const size_t row = (static_cast<size_t>(b) * p.H + h) * p.S + i;
+          uint4 *dst = reinterpret_cast<uint4 *>(p.o + row * HD);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(o0[8 * c + 0]) * inv_l, __uint_as_float(o0[8 * c + 1]) * inv_l);
+            w.y = pack_bf16x2(__uint_as_float(o0[8 * c + 2]) * inv_l, __uint_as_float(o0[8 * c + 3]) * inv_l);
+            w.z = pack_bf16x2(__uint_as_float(o0[8 * c + 4]) * inv_l, __uint_as_float(o0[8 * c + 5]) * inv_l);
+            w.w = pack_bf16x2(__uint_as_float(o0[8 * c + 6]) * inv_l, __uint_as_float(o0[8 * c + 7]) * inv_l);
+            dst[c] = w;
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(o1[8 * c + 0]) * inv_l, __uint_as_float(o1[8 * c + 1]) * inv_l);
+            w.y = pack_bf16x2(__uint_as_float(o1[8 * c + 2]) * inv_l, __uint_as_float(o1[8 * c + 3]) * inv_l);
+            w.z = pack_bf16x2(__uint_as_float(o1[8 * c + 4]) * inv_l, __uint_as_float(o1[8 * c + 5]) * inv_l);
+            w.w = pack_bf16x2(__uint_as_float(o1[8 * c + 6]) * inv_l, __uint_as_float(o1[8 * c + 7]) * inv_l);
+            dst[4 + c] = w;
+          }
+          // natural-log LSE of the scaled scores: (m + log2 l) * ln 2
+          p.lse[row] = (m_run + __log2f(l_run)) * 0.69314718055994530942f;
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after_sync();
+    tmem_dealloc(tbase, TMEM_COLS);
+  }
+}
+
+}  // namespace fwd
+}  // namespace gqa

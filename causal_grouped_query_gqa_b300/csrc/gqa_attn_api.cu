@@ -1,0 +1,223 @@
+// gqa_attn_api.cu -- the C ABI of libgqa_attn (declared in include/gqa_attn.h):
+// argument checks, TMA tensor-map encoding and kernel launches.  No torch types
+// and no allocation on the forward path; every step of the computation runs in
+// the kernels of fwd_kernel.cuh and bwd_kernels.cuh.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/gqa_attn.h"
+#include "bwd_kernels.cuh"
+#include "fwd_kernel.cuh"
+
+namespace {
+
+// Device status word: kernels set it (first error wins) when a bounded wait
+// expires; gqa_attn_last_device_status() reads and clears it.
+__device__ int g_device_status;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  int sm_count = 0;
+  int *status = nullptr;  // device address of g_device_status
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int device_state(DeviceState **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GQA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState &st = g_dev[dev];
+  if (!st.ready) {
+    if (!g_encode) {
+      void *fn = nullptr;
+      cudaDriverEntryPointQueryResult q{};
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return GQA_ERR_CUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    if (cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return GQA_ERR_CUDA;
+    if (cudaGetSymbolAddress(reinterpret_cast<void **>(&st.status), g_device_status) != cudaSuccess)
+      return GQA_ERR_CUDA;
+#ifdef GQA_FWD_P_IN_SMEM
+    constexpr bool kPTmem = false;
+#else
+    constexpr bool kPTmem = true;
+#endif
+    if (cudaFuncSetAttribute(gqa::fwd::gqa_fwd_kernel<kPTmem>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             gqa::fwd::smem_bytes<kPTmem>()) != cudaSuccess)
+      return GQA_ERR_CUDA;
+    int rc = gqa::bwd::configure_kernels();
+    if (rc != 0) return GQA_ERR_CUDA;
+    st.ready = true;
+  }
+  *out = &st;
+  return GQA_OK;
+}
+
+// 3-D bf16 tensor map over [outer][rows][64] with a box of [1][box_rows][64],
+// 128-byte swizzle; rows past `rows` read as zeros.
+int make_tmap_bf16(CUtensorMap *map, const void *base, uint64_t outer, uint64_t rows,
+                   uint32_t box_rows) {
+  cuuint64_t dims[3] = {64, rows, outer};
+  cuuint64_t strides[2] = {64 * 2, rows * 64 * 2};
+  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GQA_OK : GQA_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_common(int B, int H, int G, int S, int d, int causal, int window, int n_sink,
+                 float scale) {
+  if (B <= 0 || H <= 0 || G <= 0 || S <= 0) return GQA_ERR_SHAPE;
+  if (H % G != 0) return GQA_ERR_SHAPE;
+  // element counts must fit the kernels' int64 offsets and TMA's 32-bit dims
+  const uint64_t rows_q = static_cast<uint64_t>(B) * H;
+  if (rows_q > 0x7fffffffull || static_cast<uint64_t>(S) * 64ull * 2ull * rows_q > (1ull << 46))
+    return GQA_ERR_SHAPE;
+  if (d != 64) return GQA_ERR_HEADDIM;
+  if (n_sink < 0) return GQA_ERR_MASK;
+  if (!causal && window > 0) return GQA_ERR_MASK;
+  if (!(std::isfinite(scale) && scale > 0.f)) return GQA_ERR_SCALE;
+  return GQA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *gqa_attn_strerror(int status) {
+  switch (status) {
+    case GQA_OK: return "ok";
+    case GQA_ERR_NULL: return "a required pointer is NULL";
+    case GQA_ERR_SHAPE: return "invalid sizes (B, H, G, S must be positive, H % G == 0)";
+    case GQA_ERR_HEADDIM: return "unsupported head dimension (only d = 64)";
+    case GQA_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case GQA_ERR_MASK: return "invalid mask (window > 0 needs causal; n_sink >= 0)";
+    case GQA_ERR_SCALE: return "scale must be finite and positive";
+    case GQA_ERR_WORKSPACE: return "workspace too small";
+    case GQA_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case GQA_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait";
+    default: return "unknown status";
+  }
+}
+
+int gqa_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                 int G, int S, int d, int causal, int window, int n_sink, float scale,
+                 void *stream) {
+  int rc = check_common(B, H, G, S, d, causal, window, n_sink, scale);
+  if (rc != GQA_OK) return rc;
+  if (!q || !k || !v || !o || !lse) return GQA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return GQA_ERR_ALIGN;
+  DeviceState *ds = nullptr;
+  if ((rc = device_state(&ds)) != GQA_OK) return rc;
+
+  using namespace gqa::fwd;
+  CUtensorMap tq, tk, tv;
+  if (make_tmap_bf16(&tq, q, static_cast<uint64_t>(B) * H, S, BM) != GQA_OK ||
+      make_tmap_bf16(&tk, k, static_cast<uint64_t>(B) * G, S, BN) != GQA_OK ||
+      make_tmap_bf16(&tv, v, static_cast<uint64_t>(B) * G, S, BN) != GQA_OK)
+    return GQA_ERR_CUDA;
+
+  Params p{};
+  p.B = B;
+  p.H = H;
+  p.G = G;
+  p.S = S;
+  p.R = H / G;
+  p.causal = causal ? 1 : 0;
+  p.window = (causal && window > 0) ? window : 0;
+  p.n_sink = p.window > 0 ? n_sink : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.n_qblocks = (S + BM - 1) / BM;
+  p.n_pairs = (p.R + 1) / 2;
+  p.o = static_cast<__nv_bfloat16 *>(o);
+  p.lse = lse;
+  p.status = ds->status;
+  const long long units = static_cast<long long>(p.n_qblocks) * B * G * p.n_pairs;
+  if (units > 0x7fffffffLL) return GQA_ERR_SHAPE;
+
+#ifdef GQA_FWD_P_IN_SMEM
+  constexpr bool kPTmem = false;
+#else
+  constexpr bool kPTmem = true;
+#endif
+  gqa_fwd_kernel<kPTmem><<<static_cast<unsigned>(units), NTHREADS, smem_bytes<kPTmem>(),
+                           static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, p);
+  return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+size_t gqa_attn_bwd_workspace_size(int B, int H, int G, int S, int d) {
+  if (check_common(B, H, G, S, d, 1, 0, 0, 1.f) != GQA_OK) return 0;
+  return gqa::bwd::workspace_bytes(B, H, S);
+}
+
+int gqa_attn_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                 const float *lse, void *dq, void *dk, void *dv, int B, int H, int G, int S, int d,
+                 int causal, int window, int n_sink, float scale, void *workspace,
+                 size_t workspace_bytes, void *stream) {
+  int rc = check_common(B, H, G, S, d, causal, window, n_sink, scale);
+  if (rc != GQA_OK) return rc;
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return GQA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      (workspace && !aligned16(workspace)))
+    return GQA_ERR_ALIGN;
+  const size_t need = gqa::bwd::workspace_bytes(B, H, S);
+  if (workspace && workspace_bytes < need) return GQA_ERR_WORKSPACE;
+  DeviceState *ds = nullptr;
+  if ((rc = device_state(&ds)) != GQA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void *ws = workspace;
+  if (!ws) {
+    if (cudaMallocAsync(&ws, need, st) != cudaSuccess) return GQA_ERR_CUDA;
+  }
+  gqa::bwd::Problem pr{};
+  pr.B = B;
+  pr.H = H;
+  pr.G = G;
+  pr.S = S;
+  pr.causal = causal ? 1 : 0;
+  pr.window = (causal && window > 0) ? window : 0;
+  pr.n_sink = pr.window > 0 ? n_sink : 0;
+  pr.scale = scale;
+  rc = gqa::bwd::launch(pr, q, k, v, o, dout, lse, dq, dk, dv, ws, ds->status, g_encode, st);
+  if (!workspace) {
+    if (cudaFreeAsync(ws, st) != cudaSuccess && rc == GQA_OK) rc = GQA_ERR_CUDA;
+  }
+  return rc;
+}
+
+int gqa_attn_last_device_status(void *stream) {
+  DeviceState *ds = nullptr;
+  if (device_state(&ds) != GQA_OK) return GQA_ERR_CUDA;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GQA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, ds->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpy(ds->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  return v;
+}
+
+}  // extern "C"

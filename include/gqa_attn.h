@@ -1,0 +1,121 @@
+/*
+ * gqa_attn.h -- C ABI of libgqa_attn: exact causal scaled-dot-product attention
+ * with grouped-query K/V sharing, an optional sliding window plus always-visible
+ * leading sink tokens, and its backward pass, on one NVIDIA B300 (sm_103a).
+ *
+ * The operation (from "nx_f32_gqa_gate.nx source", header comment and tests T0-T5,
+ * and "SnapKitty Transformer 8B", sections "FlashAttention Inference" and
+ * "Protected Inventions"):
+ *
+ *   for batch b, query head h (kv head g = h / (H/G)), query row i:
+ *     s_ij  = scale * q[b,h,i,:] . k[b,g,j,:]            for every visible j
+ *     P_ij  = exp(s_ij - max_j s_ij) / sum_j exp(s_ij - max_j s_ij)
+ *     o[b,h,i,:] = sum_j P_ij v[b,g,j,:]
+ *     lse[b,h,i] = ln sum_j exp(s_ij)                    (natural log)
+ *
+ *   visible(i, j) = (!causal || j <= i) &&
+ *                   (window <= 0 || j > i - window || j < n_sink)
+ *
+ *   so with causal and window = W > 0 a query sees the W most recent keys
+ *   (itself included) plus the keys j < n_sink that are not in its future.
+ *   window <= 0 disables the window; n_sink is then ignored.  A window
+ *   without causal masking is rejected (GQA_ERR_MASK).
+ *
+ * Conventions shared by every call:
+ *   - Tensors are DEVICE pointers owned by the caller, dense and row-major:
+ *       q, o, dout, dq : [B][H][S][d] bf16      k, v, dk, dv : [B][G][S][d] bf16
+ *       lse            : [B][H][S]    fp32
+ *     each aligned to 16 bytes.  Only d = 64 is implemented.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call
+ *     is asynchronous on that stream; the return value covers argument checks
+ *     and launch errors only.  A kernel that gives up a bounded wait records
+ *     GQA_ERR_DEVICE_TIMEOUT in a device status word read by
+ *     gqa_attn_last_device_status().
+ *   - Calls are C: no exceptions, 0 on success, a negative gqa_status on error.
+ *     Nothing is launched when an argument check fails.
+ *   - The calls use the GPU that is current on the calling thread.
+ */
+#ifndef GQA_ATTN_H_
+#define GQA_ATTN_H_
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define GQA_API __attribute__((visibility("default")))
+#else
+#define GQA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GQA_OK = 0,
+    GQA_ERR_NULL = -1,           /* a required pointer is NULL */
+    GQA_ERR_SHAPE = -2,          /* B, H, G or S not positive, H % G != 0, or a size overflows */
+    GQA_ERR_HEADDIM = -3,        /* d != 64 */
+    GQA_ERR_ALIGN = -4,          /* a pointer is not 16-byte aligned */
+    GQA_ERR_MASK = -5,           /* window > 0 without causal, or n_sink < 0 */
+    GQA_ERR_SCALE = -6,          /* scale not finite or not positive */
+    GQA_ERR_WORKSPACE = -7,      /* workspace smaller than gqa_attn_bwd_workspace_size() */
+    GQA_ERR_CUDA = -8,           /* a CUDA runtime/driver call or a launch failed */
+    GQA_ERR_DEVICE_TIMEOUT = -9  /* a kernel gave up a bounded wait (device status) */
+} gqa_status;
+
+/*
+ * Forward.  Writes o [B][H][S][d] bf16 and lse [B][H][S] fp32 (natural log of the
+ * softmax denominator of the scaled scores; it is what gqa_attn_bwd needs).
+ * Inputs q [B][H][S][d], k and v [B][G][S][d] are bf16; products accumulate in
+ * fp32.  Page: "SnapKitty Transformer 8B", section "FlashAttention Inference"
+ * (flash_attention_fwd(Q, K, V, causal, sliding_window, num_sinks) on
+ * [batch, heads, seq_len, head_dim] tensors), with the GQA head map of
+ * "nx_f32_gqa_gate.nx source", test T2.
+ */
+GQA_API int gqa_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                 int B, int H, int G, int S, int d,
+                 int causal, int window, int n_sink, float scale, void *stream);
+
+/*
+ * Bytes of scratch that gqa_attn_bwd needs for these sizes: an fp32 dq
+ * accumulator [B][H][S][d] and the fp32 row term D = rowsum(dout * o) [B][H][S].
+ * Returns 0 for invalid sizes.
+ */
+GQA_API size_t gqa_attn_bwd_workspace_size(int B, int H, int G, int S, int d);
+
+/*
+ * Backward.  Given q, k, v, the forward's o and lse, and dout = dL/do, writes
+ * dq [B][H][S][d], dk and dv [B][G][S][d] (bf16; fp32 accumulation).  dk and dv
+ * are summed over the H/G query heads that share each kv head.
+ * Page: "SnapKitty Transformer 8B", section "Protected Inventions" (backward with
+ * P recomputed from the saved row statistics, dP = dO.V^T, dS = P * (dP - D),
+ * D = rowsum(dO * O), dQ reduced across query tiles), and the softmax backward
+ * of "nx_f32_gqa_gate.nx source", test T4.
+ * workspace: device memory of at least gqa_attn_bwd_workspace_size() bytes,
+ * 16-byte aligned, owned by the caller and not used by any other call running at
+ * the same time.  When workspace is NULL the call takes it with cudaMallocAsync
+ * on `stream` and frees it with cudaFreeAsync before returning.
+ * The call has no other effect on o, lse, q, k, v or dout.
+ */
+GQA_API int gqa_attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                 const void *dout, const float *lse,
+                 void *dq, void *dk, void *dv,
+                 int B, int H, int G, int S, int d,
+                 int causal, int window, int n_sink, float scale,
+                 void *workspace, size_t workspace_bytes, void *stream);
+
+/* Static text for a gqa_status value (never NULL). */
+GQA_API const char *gqa_attn_strerror(int status);
+
+/*
+ * Synchronises `stream`, then returns and clears the device status word that
+ * kernels set when a bounded wait expires: GQA_OK or GQA_ERR_DEVICE_TIMEOUT
+ * (GQA_ERR_CUDA if the synchronisation itself failed).
+ */
+GQA_API int gqa_attn_last_device_status(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_ATTN_H_ */

@@ -1,0 +1,115 @@
+"""Host-side checks of the C ABI: the library loads without a GPU, exports every
+symbol include/gqa_attn.h declares, and rejects bad arguments before touching
+the device (so these calls are safe on a machine with no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import causal_grouped_query_gqa_b300 as gq
+from causal_grouped_query_gqa_b300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return gq.load_library()
+
+
+def _declared_symbols():
+    names = set()
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            names |= set(re.findall(r"GQA_API\s+[\w\s\*]*?\b(gqa_\w+)\s*\(", text))
+    return names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared_symbols()
+    assert {"gqa_attn_fwd", "gqa_attn_bwd", "gqa_attn_bwd_workspace_size",
+            "gqa_attn_strerror", "gqa_attn_last_device_status"} <= names
+    raw = ctypes.CDLL(gq.lib_path())
+    for n in sorted(names):
+        assert hasattr(raw, n), f"{n} declared but not exported"
+
+
+def test_strerror(lib):
+    for code in range(0, -10, -1):
+        s = gq.gqa_attn_strerror(code)
+        assert isinstance(s, str) and s and s != "unknown status"
+    assert gq.gqa_attn_strerror(12345) == "unknown status"
+
+
+def test_workspace_size(lib):
+    B, H, G, S = 4, 32, 8, 4096
+    assert gq.gqa_attn_bwd_workspace_size(B, H, G, S, 64) == B * H * S * 64 * 4 + B * H * S * 4
+    assert gq.gqa_attn_bwd_workspace_size(B, H, G, S, 128) == 0
+    assert gq.gqa_attn_bwd_workspace_size(1, 3, 2, 10, 64) == 0
+    assert gq.gqa_attn_bwd_workspace_size(0, 4, 2, 10, 64) == 0
+
+
+FAKE = 0x10000  # a 16-byte-aligned non-null address that is never dereferenced
+
+
+def _fwd(**kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=4, G=2, S=128, d=64,
+             causal=1, window=0, n_sink=0, scale=0.125, stream=0)
+    a.update(kw)
+    return gq.gqa_attn_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["G"],
+                           a["S"], a["d"], a["causal"], a["window"], a["n_sink"], a["scale"],
+                           a["stream"])
+
+
+def _bwd(**kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, dout=FAKE, lse=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
+             B=1, H=4, G=2, S=128, d=64, causal=1, window=0, n_sink=0, scale=0.125,
+             ws=FAKE, wsb=1 << 30, stream=0)
+    a.update(kw)
+    return gq.gqa_attn_bwd(a["q"], a["k"], a["v"], a["o"], a["dout"], a["lse"], a["dq"], a["dk"],
+                           a["dv"], a["B"], a["H"], a["G"], a["S"], a["d"], a["causal"],
+                           a["window"], a["n_sink"], a["scale"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("call", [_fwd, _bwd])
+def test_argument_errors(lib, call):
+    assert call(B=0) == gq.GQA_ERR_SHAPE
+    assert call(S=0) == gq.GQA_ERR_SHAPE
+    assert call(S=-5) == gq.GQA_ERR_SHAPE
+    assert call(H=5, G=2) == gq.GQA_ERR_SHAPE
+    assert call(G=0) == gq.GQA_ERR_SHAPE
+    assert call(d=128) == gq.GQA_ERR_HEADDIM
+    assert call(d=32) == gq.GQA_ERR_HEADDIM
+    assert call(causal=0, window=16) == gq.GQA_ERR_MASK
+    assert call(n_sink=-1, window=16) == gq.GQA_ERR_MASK
+    assert call(scale=0.0) == gq.GQA_ERR_SCALE
+    assert call(scale=-1.0) == gq.GQA_ERR_SCALE
+    assert call(scale=float("inf")) == gq.GQA_ERR_SCALE
+    assert call(scale=float("nan")) == gq.GQA_ERR_SCALE
+    assert call(q=None) == gq.GQA_ERR_NULL
+    assert call(k=FAKE + 8) == gq.GQA_ERR_ALIGN
+    assert call(v=FAKE + 2) == gq.GQA_ERR_ALIGN
+
+
+def test_fwd_specific_errors(lib):
+    assert _fwd(lse=None) == gq.GQA_ERR_NULL
+    assert _fwd(o=FAKE + 4) == gq.GQA_ERR_ALIGN
+
+
+def test_bwd_specific_errors(lib):
+    assert _bwd(dq=None) == gq.GQA_ERR_NULL
+    assert _bwd(dout=None) == gq.GQA_ERR_NULL
+    assert _bwd(dv=FAKE + 8) == gq.GQA_ERR_ALIGN
+    assert _bwd(wsb=16) == gq.GQA_ERR_WORKSPACE
+    assert _bwd(ws=FAKE + 4) == gq.GQA_ERR_ALIGN
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    import causal_grouped_query_gqa_b300._lib as L
+    monkeypatch.setattr(L, "_lib", None)
+    monkeypatch.setattr(L, "_LIB_PATH", str(tmp_path / "libgqa_attn.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        L.load_library()

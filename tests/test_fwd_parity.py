@@ -1,0 +1,118 @@
+"""GPU forward vs the float64 oracle, element by element, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import causal_grouped_query_gqa_b300 as gq
+from causal_grouped_query_gqa_b300.inputs import WORKLOADS, make_inputs
+from parity_util import LSE_ABS, check_close, sample_rows, to64
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_full(B, H, G, S, causal=True, window=0, n_sink=0, seed=0, scale=None):
+    q, k, v = make_inputs(B, H, G, S, seed=seed)
+    o, lse = gq.fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, window=window, n_sink=n_sink,
+                    scale=scale)
+    torch.cuda.synchronize()
+    assert gq.gqa_attn_last_device_status() == gq.GQA_OK
+    ro, rl = oracle.attn_fwd(to64(q), to64(k), to64(v), causal=causal, window=window,
+                             n_sink=n_sink, scale=scale)
+    check_close("O", to64(o), ro)
+    check_close("LSE", to64(lse), rl, max_abs=LSE_ABS, mean_abs=None, bf16_out=False)
+
+
+@pytest.mark.parametrize("B,H,G,S", [
+    (1, 4, 2, 128),      # the tiny workload
+    (1, 4, 2, 1),        # one token
+    (1, 2, 1, 127),      # one partial tile
+    (1, 2, 1, 129),      # a full tile and a 1-row tail
+    (2, 4, 2, 300),      # several tiles and a ragged tail
+    (1, 3, 1, 256),      # odd heads per kv head: the last pair has one head
+    (1, 6, 2, 200),      # R = 3
+    (1, 2, 2, 384),      # H == G (plain multi-head)
+    (1, 8, 1, 520),      # R = 8, multi-query
+])
+def test_causal(B, H, G, S):
+    _run_full(B, H, G, S)
+
+
+@pytest.mark.parametrize("S", [64, 200, 513])
+def test_full_attention(S):
+    _run_full(1, 4, 2, S, causal=False)
+
+
+@pytest.mark.parametrize("S,window,n_sink", [
+    (700, 256, 64),     # sink tile + window tiles
+    (900, 100, 130),    # more sinks than the window, window inside a tile
+    (640, 1, 0),        # each row sees only itself
+    (640, 200, 0),      # pure window
+    (500, 600, 5),      # window longer than the sequence: plain causal
+    (1000, 128, 128),   # tile-aligned window and sinks
+    (777, 129, 300),    # sinks spanning three tiles
+])
+def test_window_sinks(S, window, n_sink):
+    _run_full(1, 4, 2, S, window=window, n_sink=n_sink)
+
+
+def test_scale_not_default():
+    _run_full(1, 4, 2, 300, scale=0.37)
+
+
+def test_gqa_workload_full():
+    w = WORKLOADS["gqa_b2_h32_g8_s2048"]
+    _run_full(w.B, w.H, w.G, w.S)
+
+
+def _run_sampled(w, n_rows=48):
+    """Full-size launch (the benchmark's), checked on sampled rows plus
+    properties that hold at any size."""
+    q, k, v = make_inputs(w.B, w.H, w.G, w.S, seed=0)
+    o, lse = gq.fwd(q.cuda(), k.cuda(), v.cuda(), causal=w.causal, window=w.window,
+                    n_sink=w.n_sink, scale=w.scale)
+    torch.cuda.synchronize()
+    assert gq.gqa_attn_last_device_status() == gq.GQA_OK
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    # T1 at full size: row 0 of every head is exactly v[g, 0]
+    R = w.H // w.G
+    v_rep = v.cuda().repeat_interleave(R, dim=1)
+    assert torch.equal(o[:, :, 0], v_rep[:, :, 0])
+    rows = sample_rows(w.B, w.H, w.S, n_rows, extra=[(0, w.H - 1, w.S - 1)])
+    got_o = np.stack([to64(o[b, h, i]) for b, h, i in rows])
+    got_l = np.array([float(lse[b, h, i]) for b, h, i in rows])
+    ref_o = np.zeros_like(got_o)
+    ref_l = np.zeros_like(got_l)
+    by_head = {}
+    for t, (b, h, i) in enumerate(rows):
+        by_head.setdefault((b, h), []).append((t, i))
+    for (b, h), items in by_head.items():
+        g = h // R
+        qs = to64(q[b:b + 1, h:h + 1])
+        ks = to64(k[b:b + 1, g:g + 1])
+        vs = to64(v[b:b + 1, g:g + 1])
+        ro, rl = oracle.attn_fwd_rows(qs, ks, vs, [(0, 0, i) for _, i in items],
+                                      causal=w.causal, window=w.window, n_sink=w.n_sink,
+                                      scale=w.scale)
+        for (t, _), a, c in zip(items, ro, rl):
+            ref_o[t] = a
+            ref_l[t] = c
+    check_close("O(sampled)", got_o, ref_o)
+    check_close("LSE(sampled)", got_l, ref_l, max_abs=LSE_ABS, mean_abs=None, bf16_out=False)
+
+
+def test_wide_workload_sampled():
+    _run_sampled(WORKLOADS["wide_b1_h128_g16_s8192"])
+
+
+def test_window_workload_sampled():
+    _run_sampled(WORKLOADS["window_b1_h128_g16_s32768_w4096_sink128"])
+
+
+def test_repeat_is_deterministic():
+    q, k, v = make_inputs(1, 8, 2, 1000, seed=3)
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    o1, l1 = gq.fwd(q, k, v, window=300, n_sink=17)
+    o2, l2 = gq.fwd(q, k, v, window=300, n_sink=17)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
