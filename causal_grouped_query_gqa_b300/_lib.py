@@ -55,6 +55,10 @@ def load_library():
         lib.gqa_attn_strerror.restype = ctypes.c_char_p
         lib.gqa_attn_last_device_status.argtypes = [vp]
         lib.gqa_attn_last_device_status.restype = i
+        lib.gqa_attn_timing_enable.argtypes = [i]
+        lib.gqa_attn_timing_enable.restype = i
+        lib.gqa_attn_timing_collect.argtypes = [ctypes.POINTER(ctypes.c_float), i]
+        lib.gqa_attn_timing_collect.restype = i
         _lib = lib
         return lib
 
@@ -103,6 +107,27 @@ def gqa_attn_strerror(status: int) -> str:
 
 def gqa_attn_last_device_status(stream=None) -> int:
     return load_library().gqa_attn_last_device_status(_stream(stream))
+
+
+GQA_KERNEL_COUNT = 4  # fwd, bwd prep, bwd main, bwd dq convert
+
+
+def gqa_attn_timing_enable(on: bool) -> int:
+    return load_library().gqa_attn_timing_enable(int(bool(on)))
+
+
+def timing_buffer():
+    return (ctypes.c_float * GQA_KERNEL_COUNT)()
+
+
+def gqa_attn_timing_collect(buf=None):
+    """Durations (ms) of the last launch of each kernel since the previous collect
+    (-1 where a kernel did not run); fills and returns `buf`."""
+    buf = timing_buffer() if buf is None else buf
+    rc = load_library().gqa_attn_timing_collect(buf, len(buf))
+    if rc != GQA_OK:
+        raise GqaError(rc, "gqa_attn_timing_collect")
+    return buf
 
 
 # --------------------------------------------------------- tensor helpers ---

@@ -1,14 +1,83 @@
-// bwd_kernels.cuh -- backward of causal grouped-query attention (in progress).
+// bwd_kernels.cuh -- backward of causal grouped-query attention on sm_103a.
+//
+// Given dO = dL/dO, with P recomputed from the forward's saved LSE
+// ("SnapKitty Transformer 8B", section "Protected Inventions": S/P
+// recomputation from the saved row statistics, dP = dO.V^T,
+// dS = P * (dP - D), dQ reduced across query tiles; the softmax backward
+// ds_j = a_j (g_j - sum_k a_k g_k) of "nx_f32_gqa_gate.nx source", test T4):
+//
+//   D_i   = sum_c dO_ic O_ic                         (= sum_j P_ij dP_ij)
+//   P_ij  = exp(scale q_i.k_j - LSE_i),  dP_ij = dO_i . v_j,  dS_ij = P_ij (dP_ij - D_i)
+//   dQ_i  = scale sum_j dS_ij k_j
+//   dK_j  = scale sum_{h in group} sum_i dS_ij q_i,    dV_j = sum_{h in group} sum_i P_ij dO_i
+//
+// Three launches on the caller's stream:
+//   prep   D (fp32), LSE * log2(e) (fp32), and the fp32 dQ accumulator cleared;
+//   main   one CTA per (b, kv head g, 128-key tile): for each of the R query
+//          heads of g and each query tile that sees the key tile, on tcgen05:
+//            S^T  = K Q^T       dP^T = V dO^T           (TMEM, fp32)
+//            P^T, dS^T (bf16) -> TMEM; dS (bf16) -> shared memory
+//            dV  += P^T dO      dK  += dS^T Q           (TMEM, fp32, whole CTA life)
+//            dQ   = dS K        -> fp32 TMA reduce-add into the accumulator
+//          dK, dV are summed over the group's heads inside the CTA
+//          (deterministic) and written once as bf16;
+//   convert dQ = bf16(scale * accumulator).
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
+#include <math_constants.h>
 
 #include <cstddef>
+#include <cstdint>
+
+#include "sm100_ptx.cuh"
+#include "timing.cuh"
 
 namespace gqa {
 namespace bwd {
+
+constexpr int BQ = 128;  // query rows per tile
+constexpr int BK = 128;  // keys per CTA
+constexpr int HD = 64;
+constexpr int TILE_BYTES = 128 * HD * 2;  // 16 KB bf16 tile, 128-byte rows
+constexpr int NSTAGE = 2;                 // Q/dO ring depth
+constexpr int NTHREADS = 512;
+constexpr uint32_t TMEM_COLS = 512;
+// TMEM columns
+constexpr uint32_t C_S = 0;     // S^T (128 fp32), then P^T (bf16 pairs)
+constexpr uint32_t C_DP = 128;  // dP^T (128 fp32), then dS^T (bf16 pairs)
+constexpr uint32_t C_DV = 256;  // dV accumulator (64 fp32)
+constexpr uint32_t C_DK = 320;  // dK accumulator (64 fp32)
+constexpr uint32_t C_DQ = 384;  // dQ tile, two buffers of 64 fp32
+
+// shared memory map (offsets from a 1024-aligned base)
+constexpr int SM_K = 0;
+constexpr int SM_V = SM_K + TILE_BYTES;
+constexpr int SM_Q = SM_V + TILE_BYTES;                 // NSTAGE tiles
+constexpr int SM_DO = SM_Q + NSTAGE * TILE_BYTES;       // NSTAGE tiles
+constexpr int SM_DS = SM_DO + NSTAGE * TILE_BYTES;      // 32 KB: dS, two 64-query halves
+constexpr int SM_DQ = SM_DS + 2 * TILE_BYTES;           // 2 x 32 KB fp32 dQ staging
+constexpr int SM_VEC = SM_DQ + 2 * 2 * TILE_BYTES;      // NSTAGE x (LSE2[128], D[128]) fp32
+constexpr int SM_BARS = SM_VEC + NSTAGE * 2 * BQ * 4;
+
+struct Bars {
+  uint64_t kv_full;
+  uint64_t qdo_full[NSTAGE];
+  uint64_t qdo_empty[NSTAGE];
+  uint64_t st_full;
+  uint64_t ds_ready;
+  uint64_t dq_full[2];
+  uint64_t dq_free[2];
+  uint64_t dkv_done;
+  uint32_t tmem_base;
+  AbortState abort;
+};
+
+constexpr int SMEM_BYTES = 1024 + SM_BARS + static_cast<int>(sizeof(Bars));
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 struct Problem {
   int B, H, G, S;
@@ -16,17 +85,533 @@ struct Problem {
   float scale;
 };
 
+struct MainParams {
+  int B, H, G, S, R, S_pad;
+  int causal, window, n_sink;
+  float scale;
+  float scale_log2;
+  int n_ktiles;
+  const float *lse2;  // [B*H][S_pad]
+  const float *delta; // [B*H][S_pad]
+  __nv_bfloat16 *dk;
+  __nv_bfloat16 *dv;
+  int *status;
+};
+
+enum : int { kTimeoutCode = -9 };
+
+__host__ __device__ inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
 inline size_t workspace_bytes(int B, int H, int S) {
-  const size_t rows = static_cast<size_t>(B) * H * S;
-  return rows * 64 * sizeof(float) + rows * sizeof(float);
+  const size_t rows = static_cast<size_t>(B) * H;
+  const size_t s_pad = static_cast<size_t>(round_up(S, BQ));
+  return rows * S * HD * sizeof(float) + 2 * rows * s_pad * sizeof(float);
 }
 
-inline int configure_kernels() { return 0; }
+// Query tiles [qlo, qhi] that see at least one key of key tile kb.
+__device__ __forceinline__ void q_range(int kb, const MainParams &p, int &qlo, int &qhi) {
+  const int nq = (p.S + BQ - 1) / BQ;
+  if (!p.causal) {
+    qlo = 0;
+    qhi = nq - 1;
+    return;
+  }
+  const int j0 = kb * BK, j1 = min(j0 + BK - 1, p.S - 1);
+  qlo = j0 / BQ;
+  if (p.window > 0 && j0 >= p.n_sink) {
+    const long long last = static_cast<long long>(j1) + p.window - 1;  // newest query seeing j1
+    qhi = static_cast<int>(min(static_cast<long long>(nq - 1), last / BQ));
+  } else {
+    qhi = nq - 1;
+  }
+}
 
-inline int launch(const Problem &, const void *, const void *, const void *, const void *,
-                  const void *, const float *, void *, void *, void *, void *, int *,
-                  PFN_cuTensorMapEncodeTiled_v12000, cudaStream_t) {
-  return -8;
+// True when some (query, key) pair of the tile pair is masked.
+__device__ __forceinline__ bool pair_needs_mask(int qb, int kb, const MainParams &p) {
+  const int i0 = qb * BQ, i1 = i0 + BQ - 1, j0 = kb * BK, j1 = j0 + BK - 1;
+  if (i1 >= p.S || j1 >= p.S) return true;
+  if (!p.causal) return false;
+  if (j1 > i0) return true;
+  if (p.window > 0) {
+    const bool all_in_window = j0 > i1 - p.window;
+    const bool all_sinks = j1 < p.n_sink;
+    if (!all_in_window && !all_sinks) return true;
+  }
+  return false;
+}
+
+// ------------------------------------------------------------------- prep
+
+// D = rowsum(dO * O) and LSE2 = LSE * log2(e) over [B*H][S_pad] (zeros past S),
+// and the fp32 dQ accumulator [B*H][S][64] set to zero.  Eight lanes share one
+// 128-byte row, so a warp covers four rows per pass with coalesced 16-B loads.
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__restrict__ o,
+                                                       const __nv_bfloat16 *__restrict__ dout,
+                                                       const float *__restrict__ lse,
+                                                       float *__restrict__ lse2,
+                                                       float *__restrict__ delta,
+                                                       float *__restrict__ dq_acc,
+                                                       long long rows_pad, int S, int S_pad) {
+  const int lane = threadIdx.x & 31;
+  const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  const int sub = lane >> 3;  // row within the group of four
+  const int ch = lane & 7;    // 16-byte chunk of the row
+  for (long long r0 = warp * 4; r0 < rows_pad; r0 += nwarps * 4) {
+    const long long r = r0 + sub;
+    float acc = 0.f;
+    long long src = -1;
+    if (r < rows_pad) {
+      const long long bh = r / S_pad;
+      const int i = static_cast<int>(r - bh * S_pad);
+      if (i < S) {
+        src = bh * S + i;
+        const uint4 a = reinterpret_cast<const uint4 *>(o + src * HD)[ch];
+        const uint4 c = reinterpret_cast<const uint4 *>(dout + src * HD)[ch];
+        const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&a);
+        const __nv_bfloat162 *c2 = reinterpret_cast<const __nv_bfloat162 *>(&c);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 x = __bfloat1622float2(a2[e]);
+          const float2 y = __bfloat1622float2(c2[e]);
+          acc = fmaf(x.x, y.x, acc);
+          acc = fmaf(x.y, y.y, acc);
+        }
+        float4 *z = reinterpret_cast<float4 *>(dq_acc + src * HD) + 2 * ch;
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    if (r < rows_pad && ch == 0) {
+      delta[r] = src >= 0 ? acc : 0.f;
+      lse2[r] = src >= 0 ? lse[src] * 1.4426950408889634f : 0.f;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- convert
+
+// dq = bf16(scale * dq_acc), eight elements per thread and pass.
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float *__restrict__ dq_acc,
+                                                             __nv_bfloat16 *__restrict__ dq,
+                                                             long long n8, float scale) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < n8;
+       e += stride) {
+    const float4 a = reinterpret_cast<const float4 *>(dq_acc)[2 * e];
+    const float4 b = reinterpret_cast<const float4 *>(dq_acc)[2 * e + 1];
+    uint4 w;
+    w.x = pack_bf16x2(a.x * scale, a.y * scale);
+    w.y = pack_bf16x2(a.z * scale, a.w * scale);
+    w.z = pack_bf16x2(b.x * scale, b.y * scale);
+    w.w = pack_bf16x2(b.z * scale, b.w * scale);
+    reinterpret_cast<uint4 *>(dq)[e] = w;
+  }
+}
+
+// ------------------------------------------------------------------- main
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_dq, const MainParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  Bars *bars = reinterpret_cast<Bars *>(smem + SM_BARS);
+  float *vec = reinterpret_cast<float *>(smem + SM_VEC);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // work unit: key tiles with the most query tiles first
+  const int u = blockIdx.x;
+  const int per_kb = p.B * p.G;
+  const int kb = u / per_kb;
+  const int b = (u % per_kb) / p.G;
+  const int g = u % p.G;
+  int qlo, qhi;
+  q_range(kb, p, qlo, qhi);
+  const int nqt = qhi - qlo + 1;
+  const int nsteps = p.R * nqt;  // (head, query tile) steps, heads outer
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->kv_full, 1);
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&bars->qdo_full[s], 1);
+      mbar_init(&bars->qdo_empty[s], 1);
+    }
+    mbar_init(&bars->st_full, 1);
+    mbar_init(&bars->ds_ready, 256);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->dq_full[t], 1);
+      mbar_init(&bars->dq_free[t], 128);
+    }
+    mbar_init(&bars->dkv_done, 1);
+    bars->abort.flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(&bars->tmem_base, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tbase = bars->tmem_base;
+  AbortState *ab = &bars->abort;
+
+  if (warp == 0) {
+    // ============================================================ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      const int kvz = b * p.G + g;
+      mbar_arrive_expect_tx(&bars->kv_full, 2 * TILE_BYTES);
+      tma_load_3d(smem + SM_K, &tm_k, &bars->kv_full, 0, kb * BK, kvz);
+      tma_load_3d(smem + SM_V, &tm_v, &bars->kv_full, 0, kb * BK, kvz);
+      int issued = 0;
+      for (int n = 0; n < nsteps; ++n) {
+        const int st = n % NSTAGE;
+        const uint32_t ph = (n / NSTAGE) & 1;
+        const int h = g * p.R + n / nqt;
+        const int qb = qlo + n % nqt;
+        const int bh = b * p.H + h;
+        if (!mbar_wait(&bars->qdo_empty[st], ph ^ 1, ab, p.status, kTimeoutCode)) break;
+        mbar_arrive_expect_tx(&bars->qdo_full[st], 2 * TILE_BYTES + 2 * BQ * 4);
+        tma_load_3d(smem + SM_Q + st * TILE_BYTES, &tm_q, &bars->qdo_full[st], 0, qb * BQ, bh);
+        tma_load_3d(smem + SM_DO + st * TILE_BYTES, &tm_do, &bars->qdo_full[st], 0, qb * BQ, bh);
+        const size_t voff = static_cast<size_t>(bh) * p.S_pad + static_cast<size_t>(qb) * BQ;
+        bulk_load(vec + st * 2 * BQ, p.lse2 + voff, BQ * 4, &bars->qdo_full[st]);
+        bulk_load(vec + st * 2 * BQ + BQ, p.delta + voff, BQ * 4, &bars->qdo_full[st]);
+        issued = n + 1;
+      }
+      mbar_wait_drain(&bars->kv_full, 0);
+      for (int n = max(0, issued - NSTAGE); n < issued; ++n)
+        mbar_wait_drain(&bars->qdo_full[n % NSTAGE], (n / NSTAGE) & 1);
+    }
+  } else if (warp == 1) {
+    // ============================================================ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_nn = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
+      const uint32_t id_ts = idesc_bf16_f32(128, 64, false, true);    // dV, dK
+      const uint32_t id_dq = idesc_bf16_f32(128, 64, true, true);     // dQ
+      const uint32_t k_addr = smem_u32(smem + SM_K);
+      const uint32_t v_addr = smem_u32(smem + SM_V);
+      const uint32_t q_addr = smem_u32(smem + SM_Q);
+      const uint32_t do_addr = smem_u32(smem + SM_DO);
+      const uint32_t ds_addr = smem_u32(smem + SM_DS);
+      const uint64_t k_kmaj = sdesc_sw128(k_addr, 16, 1024);
+      const uint64_t v_kmaj = sdesc_sw128(v_addr, 16, 1024);
+      const uint64_t k_mn = sdesc_sw128(k_addr, TILE_BYTES, 1024);
+      const uint64_t ds_mn = sdesc_sw128(ds_addr, TILE_BYTES, 1024);  // LBO: next 64-query half
+      bool ok = mbar_wait(&bars->kv_full, 0, ab, p.status, kTimeoutCode);
+      for (int n = 0; ok && n < nsteps; ++n) {
+        const int st = n % NSTAGE;
+        const uint32_t ph = (n / NSTAGE) & 1;
+        const uint64_t q_kmaj = sdesc_sw128(q_addr + st * TILE_BYTES, 16, 1024);
+        const uint64_t do_kmaj = sdesc_sw128(do_addr + st * TILE_BYTES, 16, 1024);
+        const uint64_t q_mn = sdesc_sw128(q_addr + st * TILE_BYTES, TILE_BYTES, 1024);
+        const uint64_t do_mn = sdesc_sw128(do_addr + st * TILE_BYTES, TILE_BYTES, 1024);
+        if (!mbar_wait(&bars->qdo_full[st], ph, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        tc_fence_after_sync();
+#pragma unroll
+        for (int ks = 0; ks < HD / 16; ++ks)
+          mma_bf16_ss(tbase + C_S, k_kmaj + 2 * ks, q_kmaj + 2 * ks, id_nn, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < HD / 16; ++ks)
+          mma_bf16_ss(tbase + C_DP, v_kmaj + 2 * ks, do_kmaj + 2 * ks, id_nn, ks > 0);
+        mma_commit(&bars->st_full);
+        if (!mbar_wait(&bars->ds_ready, n & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        tc_fence_after_sync();
+        // P^T / dS^T: queries 0-63 in packed columns 0-31, queries 64-127 in 64-95
+#pragma unroll
+        for (int ks = 0; ks < BQ / 16; ++ks) {
+          const uint32_t acol = (ks < 4 ? ks * 8 : 64 + (ks - 4) * 8);
+          mma_bf16_ts(tbase + C_DV, tbase + C_S + acol, do_mn + ks * 128, id_ts, (n > 0 || ks > 0));
+        }
+#pragma unroll
+        for (int ks = 0; ks < BQ / 16; ++ks) {
+          const uint32_t acol = (ks < 4 ? ks * 8 : 64 + (ks - 4) * 8);
+          mma_bf16_ts(tbase + C_DK, tbase + C_DP + acol, q_mn + ks * 128, id_ts, (n > 0 || ks > 0));
+        }
+        const int buf = n & 1;
+        if (!mbar_wait(&bars->dq_free[buf], ((n >> 1) & 1) ^ 1, ab, p.status, kTimeoutCode)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+#pragma unroll
+        for (int ks = 0; ks < BK / 16; ++ks)  // 16 keys = 2048 B of the MN-major operands
+          mma_bf16_ss(tbase + C_DQ + 64 * buf, ds_mn + ks * 128, k_mn + ks * 128, id_dq, ks > 0);
+        mma_commit(&bars->dq_full[buf]);
+        mma_commit(&bars->qdo_empty[st]);
+      }
+      mma_commit(&bars->dkv_done);
+      if (!ok) mbar_wait_drain(&bars->dkv_done, 0);
+    }
+  } else if (warp >= 4 && warp < 12) {
+    // ============================================================ P / dS
+    const int wg = (warp - 4) >> 2;         // query columns 64*wg .. 64*wg+63
+    const int lane_base = 32 * (warp & 3);
+    const int r = lane_base + lane;         // key row of the tile
+    const int j = kb * BK + r;              // key index
+    const float sl2 = p.scale_log2;
+    const bool win = p.causal && p.window > 0;
+    const uint32_t lane_off = static_cast<uint32_t>(lane_base) << 16;
+    bool ok = true;
+    for (int n = 0; n < nsteps; ++n) {
+      const int st = n % NSTAGE;
+      const int qb = qlo + n % nqt;
+      const int i0 = qb * BQ;
+      const float *lse2 = vec + st * 2 * BQ;
+      const float *dlt = lse2 + BQ;
+      if (!mbar_wait(&bars->st_full, n & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+      tc_fence_after_sync();
+      const bool masked = pair_needs_mask(qb, kb, p);
+#pragma unroll
+      for (int chunk = 0; chunk < 2; ++chunk) {
+        const int cb = 64 * wg + 32 * chunk;  // first query column of the chunk
+        uint32_t sr[32], dr[32];
+        tmem_ld_32x32b_x32(tbase + lane_off + C_S + cb, sr);
+        tmem_ld_32x32b_x32(tbase + lane_off + C_DP + cb, dr);
+        tmem_wait_ld();
+        reg_fence(sr);
+        reg_fence(dr);
+        uint32_t pp[16], pd[16];
+#pragma unroll
+        for (int c2 = 0; c2 < 16; ++c2) {
+          float pv[2], dv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int c = 2 * c2 + e;
+            float pr = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lse2[cb + c]));
+            if (masked) {
+              const int i = i0 + cb + c;
+              const bool vis = (i < p.S) && (j < p.S) &&
+                               (!p.causal || (j <= i && (!win || j > i - p.window || j < p.n_sink)));
+              pr = vis ? pr : 0.f;
+            }
+            pv[e] = pr;
+            dv[e] = pr * (__uint_as_float(dr[c]) - dlt[cb + c]);
+          }
+          pp[c2] = pack_bf16x2(pv[0], pv[1]);
+          pd[c2] = pack_bf16x2(dv[0], dv[1]);
+        }
+        // packed columns: this group's 64 queries -> columns 64*wg + 16*chunk .. +15
+        tmem_st_32x32b_x16(tbase + lane_off + C_S + 64 * wg + 16 * chunk, pp);
+        tmem_st_32x32b_x16(tbase + lane_off + C_DP + 64 * wg + 16 * chunk, pd);
+        // dS for dQ = dS K: half wg of the MN-major A operand, key row r, chunks of
+        // 8 queries at (chunk ^ (r & 7)) inside the 128-byte row
+        uint8_t *ds_row = smem + SM_DS + wg * TILE_BYTES + r * 128;
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {
+          const int cch = 4 * chunk + q8;
+          uint4 w;
+          w.x = pd[4 * q8 + 0];
+          w.y = pd[4 * q8 + 1];
+          w.z = pd[4 * q8 + 2];
+          w.w = pd[4 * q8 + 3];
+          *reinterpret_cast<uint4 *>(ds_row + ((cch ^ (r & 7)) << 4)) = w;
+        }
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      mbar_arrive(&bars->ds_ready);
+    }
+    // epilogue: group 0 writes dV, group 1 writes dK (x scale), one key row per thread
+    if (ok && mbar_wait(&bars->dkv_done, 0, ab, p.status, kTimeoutCode)) {
+      tc_fence_after_sync();
+      uint32_t a0[32], a1[32];
+      const uint32_t col = wg == 0 ? C_DV : C_DK;
+      tmem_ld_32x32b_x32(tbase + lane_off + col, a0);
+      tmem_ld_32x32b_x32(tbase + lane_off + col + 32, a1);
+      tmem_wait_ld();
+      reg_fence(a0);
+      reg_fence(a1);
+      if (j < p.S) {
+        const float f = wg == 0 ? 1.f : p.scale;
+        __nv_bfloat16 *dst = (wg == 0 ? p.dv : p.dk) +
+                             ((static_cast<size_t>(b) * p.G + g) * p.S + j) * HD;
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(a0[8 * c + 0]) * f, __uint_as_float(a0[8 * c + 1]) * f);
+          w.y = pack_bf16x2(__uint_as_float(a0[8 * c + 2]) * f, __uint_as_float(a0[8 * c + 3]) * f);
+          w.z = pack_bf16x2(__uint_as_float(a0[8 * c + 4]) * f, __uint_as_float(a0[8 * c + 5]) * f);
+          w.w = pack_bf16x2(__uint_as_float(a0[8 * c + 6]) * f, __uint_as_float(a0[8 * c + 7]) * f);
+          d4[c] = w;
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(a1[8 * c + 0]) * f, __uint_as_float(a1[8 * c + 1]) * f);
+          w.y = pack_bf16x2(__uint_as_float(a1[8 * c + 2]) * f, __uint_as_float(a1[8 * c + 3]) * f);
+          w.z = pack_bf16x2(__uint_as_float(a1[8 * c + 4]) * f, __uint_as_float(a1[8 * c + 5]) * f);
+          w.w = pack_bf16x2(__uint_as_float(a1[8 * c + 6]) * f, __uint_as_float(a1[8 * c + 7]) * f);
+          d4[4 + c] = w;
+        }
+      }
+    }
+  } else if (warp >= 12) {
+    // ============================================================ dQ drain
+    const int lane_base = 32 * (warp & 3);
+    const int r = lane_base + lane;  // query row of the tile
+    const uint32_t lane_off = static_cast<uint32_t>(lane_base) << 16;
+    const bool leader = (warp == 12 && lane == 0);
+    for (int n = 0; n < nsteps; ++n) {
+      const int buf = n & 1;
+      const int h = g * p.R + n / nqt;
+      const int qb = qlo + n % nqt;
+      if (!mbar_wait(&bars->dq_full[buf], (n >> 1) & 1, ab, p.status, kTimeoutCode)) break;
+      tc_fence_after_sync();
+      uint32_t a0[32], a1[32];
+      tmem_ld_32x32b_x32(tbase + lane_off + C_DQ + 64 * buf, a0);
+      tmem_ld_32x32b_x32(tbase + lane_off + C_DQ + 64 * buf + 32, a1);
+      tmem_wait_ld();
+      reg_fence(a0);
+      reg_fence(a1);
+      tc_fence_before_sync();
+      mbar_arrive(&bars->dq_free[buf]);
+      // staging buffer `buf` was last read by the reduce issued two steps ago
+      if (leader) bulk_wait_group_read<1>();
+      named_bar_sync(1, 128);
+      // two boxes [128 rows][32 fp32], 128-byte swizzle: 16-B chunk c of row r at c ^ (r & 7)
+      uint8_t *stg = smem + SM_DQ + buf * 2 * TILE_BYTES + r * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        *reinterpret_cast<uint4 *>(stg + ((c ^ (r & 7)) << 4)) =
+            make_uint4(a0[4 * c], a0[4 * c + 1], a0[4 * c + 2], a0[4 * c + 3]);
+        *reinterpret_cast<uint4 *>(stg + TILE_BYTES + ((c ^ (r & 7)) << 4)) =
+            make_uint4(a1[4 * c], a1[4 * c + 1], a1[4 * c + 2], a1[4 * c + 3]);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (leader) {
+        const int bh = b * p.H + h;
+        uint8_t *box = smem + SM_DQ + buf * 2 * TILE_BYTES;
+        tma_reduce_add_3d(&tm_dq, box, 0, qb * BQ, bh);
+        tma_reduce_add_3d(&tm_dq, box + TILE_BYTES, 32, qb * BQ, bh);
+        bulk_commit_group();
+      }
+    }
+    if (leader) bulk_wait_group_all();
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after_sync();
+    tmem_dealloc(tbase, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------- host
+
+inline int configure_kernels() {
+  return cudaFuncSetAttribute(bwd_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              SMEM_BYTES) == cudaSuccess
+             ? 0
+             : -1;
+}
+
+inline int encode_3d(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap *map,
+                     CUtensorMapDataType dt, int esize, const void *base, uint64_t inner,
+                     uint64_t rows, uint64_t outer, uint32_t box_inner, uint32_t box_rows) {
+  cuuint64_t dims[3] = {inner, rows, outer};
+  cuuint64_t strides[2] = {inner * esize, rows * inner * esize};
+  cuuint32_t box[3] = {box_inner, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+             ? 0
+             : -1;
+}
+
+// Launches prep, main and convert on `st`.  Returns a gqa_status value.
+inline int launch(const Problem &pr, const void *q, const void *k, const void *v, const void *o,
+                  const void *dout, const float *lse, void *dq, void *dk, void *dv, void *ws,
+                  int *status, int sm_count, PFN_cuTensorMapEncodeTiled_v12000 enc,
+                  cudaStream_t st) {
+  const int B = pr.B, H = pr.H, G = pr.G, S = pr.S;
+  const int S_pad = round_up(S, BQ);
+  const long long rows = static_cast<long long>(B) * H * S;
+  const long long rows_pad = static_cast<long long>(B) * H * S_pad;
+  float *dq_acc = static_cast<float *>(ws);
+  float *lse2 = dq_acc + rows * HD;
+  float *delta = lse2 + rows_pad;
+
+  CUtensorMap tq, tk, tv, tdo, tdq;
+  if (encode_3d(enc, &tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, HD, S,
+                static_cast<uint64_t>(B) * H, HD, BQ) ||
+      encode_3d(enc, &tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, HD, S,
+                static_cast<uint64_t>(B) * G, HD, BK) ||
+      encode_3d(enc, &tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v, HD, S,
+                static_cast<uint64_t>(B) * G, HD, BK) ||
+      encode_3d(enc, &tdo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dout, HD, S,
+                static_cast<uint64_t>(B) * H, HD, BQ) ||
+      encode_3d(enc, &tdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dq_acc, HD, S,
+                static_cast<uint64_t>(B) * H, 32, BQ))
+    return -8;
+
+  {
+    const long long warps_needed = (rows_pad + 3) / 4;
+    long long blocks = (warps_needed * 32 + 255) / 256;
+    blocks = blocks < 1 ? 1 : (blocks > 8LL * sm_count ? 8LL * sm_count : blocks);
+    timing_begin(1, st);
+    bwd_prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+        static_cast<const __nv_bfloat16 *>(o), static_cast<const __nv_bfloat16 *>(dout), lse,
+        lse2, delta, dq_acc, rows_pad, S, S_pad);
+    timing_end(1, st);
+    if (cudaGetLastError() != cudaSuccess) return -8;
+  }
+  {
+    MainParams p{};
+    p.B = B;
+    p.H = H;
+    p.G = G;
+    p.S = S;
+    p.R = H / G;
+    p.S_pad = S_pad;
+    p.causal = pr.causal;
+    p.window = pr.window;
+    p.n_sink = pr.n_sink;
+    p.scale = pr.scale;
+    p.scale_log2 = pr.scale * 1.4426950408889634f;
+    p.n_ktiles = (S + BK - 1) / BK;
+    p.lse2 = lse2;
+    p.delta = delta;
+    p.dk = static_cast<__nv_bfloat16 *>(dk);
+    p.dv = static_cast<__nv_bfloat16 *>(dv);
+    p.status = status;
+    const long long units = static_cast<long long>(p.n_ktiles) * B * G;
+    if (units > 0x7fffffffLL) return -2;
+    timing_begin(2, st);
+    bwd_main_kernel<<<static_cast<unsigned>(units), NTHREADS, SMEM_BYTES, st>>>(tq, tk, tv, tdo,
+                                                                               tdq, p);
+    timing_end(2, st);
+    if (cudaGetLastError() != cudaSuccess) return -8;
+  }
+  {
+    const long long n8 = rows * HD / 8;
+    long long blocks = (n8 + 255) / 256;
+    blocks = blocks < 1 ? 1 : (blocks > 8LL * sm_count ? 8LL * sm_count : blocks);
+    timing_begin(3, st);
+    bwd_dq_convert_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+        dq_acc, static_cast<__nv_bfloat16 *>(dq), n8, pr.scale);
+    timing_end(3, st);
+    if (cudaGetLastError() != cudaSuccess) return -8;
+  }
+  return 0;
 }
 
 }  // namespace bwd

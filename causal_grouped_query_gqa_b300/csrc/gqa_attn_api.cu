@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "../../include/gqa_attn.h"
+#include "timing.cuh"
 #include "bwd_kernels.cuh"
 #include "fwd_kernel.cuh"
 
@@ -161,8 +162,11 @@ int gqa_attn_fwd(const void *q, const void *k, const void *v, void *o, float *ls
 #else
   constexpr bool kPTmem = true;
 #endif
-  gqa_fwd_kernel<kPTmem><<<static_cast<unsigned>(units), NTHREADS, smem_bytes<kPTmem>(),
-                           static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, p);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  gqa::timing_begin(GQA_KERNEL_FWD, st);
+  gqa_fwd_kernel<kPTmem><<<static_cast<unsigned>(units), NTHREADS, smem_bytes<kPTmem>(), st>>>(
+      tq, tk, tv, p);
+  gqa::timing_end(GQA_KERNEL_FWD, st);
   return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
@@ -200,9 +204,49 @@ int gqa_attn_bwd(const void *q, const void *k, const void *v, const void *o, con
   pr.window = (causal && window > 0) ? window : 0;
   pr.n_sink = pr.window > 0 ? n_sink : 0;
   pr.scale = scale;
-  rc = gqa::bwd::launch(pr, q, k, v, o, dout, lse, dq, dk, dv, ws, ds->status, g_encode, st);
+  rc = gqa::bwd::launch(pr, q, k, v, o, dout, lse, dq, dk, dv, ws, ds->status, ds->sm_count,
+                        g_encode, st);
+  if (rc == -2) rc = GQA_ERR_SHAPE;
+  else if (rc != 0) rc = GQA_ERR_CUDA;
   if (!workspace) {
     if (cudaFreeAsync(ws, st) != cudaSuccess && rc == GQA_OK) rc = GQA_ERR_CUDA;
+  }
+  return rc;
+}
+
+int gqa_attn_timing_enable(int on) {
+  gqa::TimingState &t = gqa::timing_state();
+  if (on) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
+    if (t.device != dev) {
+      for (int i = 0; i < gqa::kNumKernelIds; ++i) {
+        if (cudaEventCreate(&t.start[i]) != cudaSuccess ||
+            cudaEventCreate(&t.stop[i]) != cudaSuccess)
+          return GQA_ERR_CUDA;
+        t.recorded[i] = false;
+      }
+      t.device = dev;
+    }
+  }
+  t.on = on != 0;
+  return GQA_OK;
+}
+
+int gqa_attn_timing_collect(float *ms, int n) {
+  if (!ms) return GQA_ERR_NULL;
+  gqa::TimingState &t = gqa::timing_state();
+  int rc = GQA_OK;
+  for (int i = 0; i < gqa::kNumKernelIds && i < n; ++i) {
+    ms[i] = -1.f;
+    if (t.device >= 0 && t.recorded[i]) {
+      if (cudaEventSynchronize(t.stop[i]) != cudaSuccess ||
+          cudaEventElapsedTime(&ms[i], t.start[i], t.stop[i]) != cudaSuccess) {
+        ms[i] = -1.f;
+        rc = GQA_ERR_CUDA;
+      }
+      t.recorded[i] = false;
+    }
   }
   return rc;
 }

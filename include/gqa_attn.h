@@ -78,8 +78,9 @@ GQA_API int gqa_attn_fwd(const void *q, const void *k, const void *v, void *o, f
 
 /*
  * Bytes of scratch that gqa_attn_bwd needs for these sizes: an fp32 dq
- * accumulator [B][H][S][d] and the fp32 row term D = rowsum(dout * o) [B][H][S].
- * Returns 0 for invalid sizes.
+ * accumulator [B][H][S][d], then two fp32 row arrays [B][H][S_pad] with
+ * S_pad = S rounded up to a multiple of 128: lse * log2(e) and the row term
+ * D = rowsum(dout * o).  Returns 0 for invalid sizes.
  */
 GQA_API size_t gqa_attn_bwd_workspace_size(int B, int H, int G, int S, int d);
 
@@ -113,6 +114,26 @@ GQA_API const char *gqa_attn_strerror(int status);
  * (GQA_ERR_CUDA if the synchronisation itself failed).
  */
 GQA_API int gqa_attn_last_device_status(void *stream);
+
+/*
+ * Kernel timing (a profiling aid, not thread-safe).  While enabled, every
+ * kernel the library launches is bracketed by CUDA events recorded on its own
+ * launch stream.  gqa_attn_timing_collect() waits for the events of the last
+ * launch of each kernel and writes its duration in milliseconds to ms[id]
+ * (-1 when that kernel has not run since the previous collect), for
+ * id < min(n, GQA_KERNEL_COUNT).  No page describes this; it backs the
+ * per-kernel roofline the benchmark reports.
+ */
+typedef enum {
+    GQA_KERNEL_FWD = 0,       /* forward (one launch per gqa_attn_fwd) */
+    GQA_KERNEL_BWD_PREP = 1,  /* backward: D = rowsum(dout * o), dq accumulator cleared */
+    GQA_KERNEL_BWD_MAIN = 2,  /* backward: dk, dv and the dq accumulation */
+    GQA_KERNEL_BWD_DQ = 3,    /* backward: dq accumulator -> bf16 dq */
+    GQA_KERNEL_COUNT = 4
+} gqa_kernel_id;
+
+GQA_API int gqa_attn_timing_enable(int on);
+GQA_API int gqa_attn_timing_collect(float *ms, int n);
 
 #ifdef __cplusplus
 }

@@ -56,6 +56,12 @@ def _declare(lib):
     lib.oracle_attn_bwd_group.argtypes = [dp, dp, dp, dp, dp, dp, dp,
                                           i, i, i, i, i, i, i, i, d, i, i]
     lib.oracle_attn_bwd_group.restype = None
+    lib.oracle_attn_bwd_group_rows.argtypes = [dp, dp, dp, dp, dp, dp, dp,
+                                               i, i, i, i, i, i, i, i, d, i, i,
+                                               ctypes.c_long, ctypes.c_long]
+    lib.oracle_attn_bwd_group_rows.restype = None
+    lib.oracle_num_threads.argtypes = []
+    lib.oracle_num_threads.restype = i
     return lib
 
 
@@ -142,6 +148,28 @@ def attn_bwd_group(q, k, v, dO, b, g, *, causal=True, window=0, n_sink=0, scale=
                               B, H, G, S, d, int(causal), int(window), int(n_sink), scale,
                               int(b), int(g))
     return dq, dk, dv
+
+
+def attn_bwd_group_rows(q, k, v, dO, b, g, i_begin, i_end, *, causal=True, window=0,
+                        n_sink=0, scale=None, lib=None):
+    """Backward of one kv group restricted to query rows [i_begin, i_end): the
+    dq of those rows and their contributions to dk, dv (a bounded sample)."""
+    lib = lib or load()
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    B, H, G, S, d = _shape(q, k)
+    R = H // G
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    dq = np.zeros((R, S, d))
+    dk = np.zeros((S, d))
+    dv = np.zeros((S, d))
+    lib.oracle_attn_bwd_group_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(dq), _ptr(dk),
+                                   _ptr(dv), B, H, G, S, d, int(causal), int(window),
+                                   int(n_sink), scale, int(b), int(g), int(i_begin), int(i_end))
+    return dq, dk, dv
+
+
+def num_threads(lib=None) -> int:
+    return int((lib or load()).oracle_num_threads())
 
 
 def visible(i: int, j: int, *, causal=True, window=0, n_sink=0, lib=None) -> bool:

@@ -37,6 +37,9 @@
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 /* The mask, exactly as read above.  Returns 1 when query i may see key j. */
 int oracle_visible(long i, long j, int causal, int window, int n_sink)
@@ -162,9 +165,10 @@ void oracle_attn_fwd_rows(const double *q, const double *k, const double *v,
     }
 }
 
-/* Backward of one kv group (b, g): the R query heads h = g*R .. g*R+R-1.
- *   dq_g : [R][S][d]   gradients of those query heads
- *   dk_g, dv_g : [S][d] gradients of kv head g
+/* Backward of one kv group (b, g): the R query heads h = g*R .. g*R+R-1,
+ * restricted to query rows i_begin <= i < i_end (all rows: 0 .. S).
+ *   dq_g : [R][S][d]   gradients of those query heads (rows in range only)
+ *   dk_g, dv_g : [S][d] gradients of kv head g from the rows in range
  * For each query row (exact P from its own forward, never a saved O/LSE):
  *   dP_ij = dO_i . v_j ;  D_i = sum_j P_ij dP_ij ;  dS_ij = P_ij (dP_ij - D_i)
  *   dq_i  = scale * sum_j dS_ij k_j
@@ -172,11 +176,11 @@ void oracle_attn_fwd_rows(const double *q, const double *k, const double *v,
  * Rows are spread over threads; each thread keeps private dk/dv sums that are
  * added into the outputs one thread at a time at the end (float64, so the
  * order of those few additions does not matter at the tolerances used). */
-void oracle_attn_bwd_group(const double *q, const double *k, const double *v, const double *dO,
-                           double *dq_g, double *dk_g, double *dv_g,
-                           int B, int H, int G, int S, int d,
-                           int causal, int window, int n_sink, double scale,
-                           int b, int g)
+void oracle_attn_bwd_group_rows(const double *q, const double *k, const double *v,
+                                const double *dO, double *dq_g, double *dk_g, double *dv_g,
+                                int B, int H, int G, int S, int d,
+                                int causal, int window, int n_sink, double scale,
+                                int b, int g, long i_begin, long i_end)
 {
     (void)B;
     const int R = H / G;
@@ -185,7 +189,12 @@ void oracle_attn_bwd_group(const double *q, const double *k, const double *v, co
     const long sd = (long)S * d;
     memset(dk_g, 0, sizeof(double) * sd);
     memset(dv_g, 0, sizeof(double) * sd);
-    const long nrows = (long)R * S;
+    if (i_begin < 0)
+        i_begin = 0;
+    if (i_end > S)
+        i_end = S;
+    const long span = i_end > i_begin ? i_end - i_begin : 0;
+    const long nrows = (long)R * span;
 #pragma omp parallel
     {
         double *s = (double *)malloc(sizeof(double) * (S > 0 ? S : 1));
@@ -195,8 +204,8 @@ void oracle_attn_bwd_group(const double *q, const double *k, const double *v, co
         double *dv_t = (double *)calloc(sd > 0 ? sd : 1, sizeof(double));
 #pragma omp for schedule(dynamic, 8)
         for (long r = 0; r < nrows; ++r) {
-            int hh = (int)(r / S);
-            long i = r % S;
+            int hh = (int)(r / span);
+            long i = i_begin + r % span;
             int h = g * R + hh;
             const double *qi = q + (((long)b * H + h) * S + i) * d;
             const double *doi = dO + (((long)b * H + h) * S + i) * d;
@@ -237,6 +246,27 @@ void oracle_attn_bwd_group(const double *q, const double *k, const double *v, co
         free(dk_t);
         free(dv_t);
     }
+}
+
+/* Whole group: every query row of its R heads. */
+void oracle_attn_bwd_group(const double *q, const double *k, const double *v, const double *dO,
+                           double *dq_g, double *dk_g, double *dv_g,
+                           int B, int H, int G, int S, int d,
+                           int causal, int window, int n_sink, double scale,
+                           int b, int g)
+{
+    oracle_attn_bwd_group_rows(q, k, v, dO, dq_g, dk_g, dv_g, B, H, G, S, d,
+                               causal, window, n_sink, scale, b, g, 0, S);
+}
+
+/* Threads the OpenMP runtime will use (reported with CPU timings). */
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
 }
 
 /* Backward over every group.  dq: [B][H][S][d], dk, dv: [B][G][S][d]. */

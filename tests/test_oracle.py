@@ -289,3 +289,20 @@ def test_rows_and_group_entry_points_match_full():
     np.testing.assert_allclose(gq, dq[1, 2:4], atol=1e-15)
     np.testing.assert_allclose(gk, dk[1, 1], atol=1e-15)
     np.testing.assert_allclose(gv, dv[1, 1], atol=1e-15)
+
+
+def test_row_range_backward_sums_to_group():
+    """Row ranges partition the group's backward: dq rows match, dk/dv add up."""
+    rng = np.random.default_rng(8)
+    B, H, G, S, d = 1, 4, 2, 12, 3
+    kw = dict(causal=True, window=5, n_sink=2)
+    q, dO = rng.standard_normal((B, H, S, d)), rng.standard_normal((B, H, S, d))
+    k, v = rng.standard_normal((B, G, S, d)), rng.standard_normal((B, G, S, d))
+    gq_, gk, gv = oracle.attn_bwd_group(q, k, v, dO, 0, 1, **kw)
+    a = oracle.attn_bwd_group_rows(q, k, v, dO, 0, 1, 0, 7, **kw)
+    c = oracle.attn_bwd_group_rows(q, k, v, dO, 0, 1, 7, S, **kw)
+    np.testing.assert_allclose(a[1] + c[1], gk, atol=1e-14)
+    np.testing.assert_allclose(a[2] + c[2], gv, atol=1e-14)
+    np.testing.assert_allclose(a[0][:, :7], gq_[:, :7], atol=1e-15)
+    np.testing.assert_allclose(c[0][:, 7:], gq_[:, 7:], atol=1e-15)
+    assert oracle.num_threads() >= 1
