@@ -35,6 +35,7 @@
 
 #include "sm100_ptx.cuh"
 #include "timing.cuh"
+#include "trace.cuh"
 
 namespace gqa {
 namespace bwd {
@@ -220,9 +221,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_dq, const MainParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte alignment for the swizzled tiles, by pointer arithmetic on the
+  // __shared__ array so that accesses stay shared-space (ld/st.shared).
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Bars *bars = reinterpret_cast<Bars *>(smem + SM_BARS);
   float *vec = reinterpret_cast<float *>(smem + SM_VEC);
   const int warp = threadIdx.x >> 5;
@@ -264,6 +266,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   tc_fence_after_sync();
   const uint32_t tbase = bars->tmem_base;
   AbortState *ab = &bars->abort;
+  if (threadIdx.x == 0) GQA_TRACE_EVENT(1, 15, 0);
 
   if (warp == 0) {
     // ============================================================ producer
@@ -284,12 +287,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int qb = qlo + n % nqt;
         const int bh = b * p.H + h;
         if (!mbar_wait(&bars->qdo_empty[st], ph ^ 1, ab, p.status, kTimeoutCode)) break;
+        GQA_TRACE_EVENT(1, 0, n);
         mbar_arrive_expect_tx(&bars->qdo_full[st], 2 * TILE_BYTES + 2 * BQ * 4);
         tma_load_3d(smem + SM_Q + st * TILE_BYTES, &tm_q, &bars->qdo_full[st], 0, qb * BQ, bh);
         tma_load_3d(smem + SM_DO + st * TILE_BYTES, &tm_do, &bars->qdo_full[st], 0, qb * BQ, bh);
         const size_t voff = static_cast<size_t>(bh) * p.S_pad + static_cast<size_t>(qb) * BQ;
         bulk_load(vec + st * 2 * BQ, p.lse2 + voff, BQ * 4, &bars->qdo_full[st]);
         bulk_load(vec + st * 2 * BQ + BQ, p.delta + voff, BQ * 4, &bars->qdo_full[st]);
+        GQA_TRACE_EVENT(1, 1, n);
         issued = n + 1;
       }
       mbar_wait_drain(&bars->kv_full, 0);
@@ -320,6 +325,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint64_t q_mn = sdesc_sw128(q_addr + st * TILE_BYTES, TILE_BYTES, 1024);
         const uint64_t do_mn = sdesc_sw128(do_addr + st * TILE_BYTES, TILE_BYTES, 1024);
         if (!mbar_wait(&bars->qdo_full[st], ph, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        GQA_TRACE_EVENT(1, 2, n);
         tc_fence_after_sync();
 #pragma unroll
         for (int ks = 0; ks < HD / 16; ++ks)
@@ -328,7 +334,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int ks = 0; ks < HD / 16; ++ks)
           mma_bf16_ss(tbase + C_DP, v_kmaj + 2 * ks, do_kmaj + 2 * ks, id_nn, ks > 0);
         mma_commit(&bars->st_full);
+        GQA_TRACE_EVENT(1, 3, n);
         if (!mbar_wait(&bars->ds_ready, n & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        GQA_TRACE_EVENT(1, 4, n);
         tc_fence_after_sync();
         // P^T / dS^T: queries 0-63 in packed columns 0-31, queries 64-127 in 64-95
 #pragma unroll
@@ -342,16 +350,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           mma_bf16_ts(tbase + C_DK, tbase + C_DP + acol, q_mn + ks * 128, id_ts, (n > 0 || ks > 0));
         }
         const int buf = n & 1;
+        GQA_TRACE_EVENT(1, 5, n);
         if (!mbar_wait(&bars->dq_free[buf], ((n >> 1) & 1) ^ 1, ab, p.status, kTimeoutCode)) {
           ok = false;
           break;
         }
+        GQA_TRACE_EVENT(1, 6, n);
         tc_fence_after_sync();
 #pragma unroll
         for (int ks = 0; ks < BK / 16; ++ks)  // 16 keys = 2048 B of the MN-major operands
           mma_bf16_ss(tbase + C_DQ + 64 * buf, ds_mn + ks * 128, k_mn + ks * 128, id_dq, ks > 0);
         mma_commit(&bars->dq_full[buf]);
         mma_commit(&bars->qdo_empty[st]);
+        GQA_TRACE_EVENT(1, 7, n);
       }
       mma_commit(&bars->dkv_done);
       if (!ok) mbar_wait_drain(&bars->dkv_done, 0);
@@ -373,6 +384,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const float *lse2 = vec + st * 2 * BQ;
       const float *dlt = lse2 + BQ;
       if (!mbar_wait(&bars->st_full, n & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+      if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 8, n);
       tc_fence_after_sync();
       const bool masked = pair_needs_mask(qb, kb, p);
 #pragma unroll
@@ -384,29 +396,48 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tmem_wait_ld();
         reg_fence(sr);
         reg_fence(dr);
+        if (chunk == 0 && warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 9, n);
+        if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 16 + 4 * chunk, n);
+        // P and dS in sub-chunks of 8 query columns: the 8 LSE2 and 8 D values of a
+        // sub-chunk are two broadcast 16-byte shared loads each, so few values
+        // are live at once.
         uint32_t pp[16], pd[16];
 #pragma unroll
-        for (int c2 = 0; c2 < 16; ++c2) {
-          float pv[2], dv[2];
+        for (int sc = 0; sc < 4; ++sc) {
+          const float4 la = reinterpret_cast<const float4 *>(lse2 + cb)[2 * sc];
+          const float4 lb = reinterpret_cast<const float4 *>(lse2 + cb)[2 * sc + 1];
+          const float4 da = reinterpret_cast<const float4 *>(dlt + cb)[2 * sc];
+          const float4 db = reinterpret_cast<const float4 *>(dlt + cb)[2 * sc + 1];
+          const float l8[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
+          const float d8[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
+          float pv[8], dv[8];
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int c = 2 * c2 + e;
-            float pr = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lse2[cb + c]));
-            if (masked) {
-              const int i = i0 + cb + c;
+          for (int e = 0; e < 8; ++e) {
+            const int c = 8 * sc + e;
+            pv[e] = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -l8[e]));
+          }
+          if (masked) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int i = i0 + cb + 8 * sc + e;
               const bool vis = (i < p.S) && (j < p.S) &&
                                (!p.causal || (j <= i && (!win || j > i - p.window || j < p.n_sink)));
-              pr = vis ? pr : 0.f;
+              pv[e] = vis ? pv[e] : 0.f;
             }
-            pv[e] = pr;
-            dv[e] = pr * (__uint_as_float(dr[c]) - dlt[cb + c]);
           }
-          pp[c2] = pack_bf16x2(pv[0], pv[1]);
-          pd[c2] = pack_bf16x2(dv[0], dv[1]);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) dv[e] = pv[e] * (__uint_as_float(dr[8 * sc + e]) - d8[e]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            pp[4 * sc + e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
+            pd[4 * sc + e] = pack_bf16x2(dv[2 * e], dv[2 * e + 1]);
+          }
         }
+        if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 17 + 4 * chunk, n);
         // packed columns: this group's 64 queries -> columns 64*wg + 16*chunk .. +15
         tmem_st_32x32b_x16(tbase + lane_off + C_S + 64 * wg + 16 * chunk, pp);
         tmem_st_32x32b_x16(tbase + lane_off + C_DP + 64 * wg + 16 * chunk, pd);
+        if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 18 + 4 * chunk, n);
         // dS for dQ = dS K: half wg of the MN-major A operand, key row r, chunks of
         // 8 queries at (chunk ^ (r & 7)) inside the 128-byte row
         uint8_t *ds_row = smem + SM_DS + wg * TILE_BYTES + r * 128;
@@ -420,10 +451,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           w.w = pd[4 * q8 + 3];
           *reinterpret_cast<uint4 *>(ds_row + ((cch ^ (r & 7)) << 4)) = w;
         }
+        if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 19 + 4 * chunk, n);
       }
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before_sync();
+      if (lane == 0 && (warp == 4 || warp == 8)) GQA_TRACE_EVENT(1, warp == 4 ? 10 : 11, n);
       mbar_arrive(&bars->ds_ready);
     }
     // epilogue: group 0 writes dV, group 1 writes dK (x scale), one key row per thread
@@ -472,6 +505,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int h = g * p.R + n / nqt;
       const int qb = qlo + n % nqt;
       if (!mbar_wait(&bars->dq_full[buf], (n >> 1) & 1, ab, p.status, kTimeoutCode)) break;
+      if (leader) GQA_TRACE_EVENT(1, 12, n);
       tc_fence_after_sync();
       uint32_t a0[32], a1[32];
       tmem_ld_32x32b_x32(tbase + lane_off + C_DQ + 64 * buf, a0);
@@ -483,6 +517,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_arrive(&bars->dq_free[buf]);
       // staging buffer `buf` was last read by the reduce issued two steps ago
       if (leader) bulk_wait_group_read<1>();
+      if (leader) GQA_TRACE_EVENT(1, 13, n);
       named_bar_sync(1, 128);
       // two boxes [128 rows][32 fp32], 128-byte swizzle: 16-B chunk c of row r at c ^ (r & 7)
       uint8_t *stg = smem + SM_DQ + buf * 2 * TILE_BYTES + r * 128;
@@ -501,6 +536,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tma_reduce_add_3d(&tm_dq, box, 0, qb * BQ, bh);
         tma_reduce_add_3d(&tm_dq, box + TILE_BYTES, 32, qb * BQ, bh);
         bulk_commit_group();
+        GQA_TRACE_EVENT(1, 14, n);
       }
     }
     if (leader) bulk_wait_group_all();
@@ -508,6 +544,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   tc_fence_before_sync();
   __syncthreads();
+  if (threadIdx.x == 0) GQA_TRACE_EVENT(1, 15, 1);
   if (warp == 2) {
     tc_fence_after_sync();
     tmem_dealloc(tbase, TMEM_COLS);

@@ -28,6 +28,7 @@
 #include <math_constants.h>
 
 #include "sm100_ptx.cuh"
+#include "trace.cuh"
 
 namespace gqa {
 namespace fwd {
@@ -137,9 +138,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     gqa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const Params p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte alignment for the swizzled tiles, by pointer arithmetic on the
+  // __shared__ array so that accesses stay shared-space (ld/st.shared).
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Bars *bars = reinterpret_cast<Bars *>(smem + bars_offset<P_TMEM>());
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -182,6 +184,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   tc_fence_after_sync();
   const uint32_t tbase = bars->tmem_base;
   AbortState *ab = &bars->abort;
+  if (threadIdx.x == 0) GQA_TRACE_EVENT(0, 14, 0);
 
   if (warp == 0) {
     // ================================================================ producer
@@ -200,6 +203,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t ph = (it / NSTAGE) & 1;
         const int kb = kr.tile(it);
         if (!mbar_wait(&bars->k_empty[st], ph ^ 1, ab, p.status, kTimeoutCode)) break;
+        GQA_TRACE_EVENT(0, 0, it);
         mbar_arrive_expect_tx(&bars->k_full[st], TILE_BYTES);
         tma_load_3d(smem + SM_K + st * TILE_BYTES, &tm_k, &bars->k_full[st], 0, kb * BN, kvz);
         if (!mbar_wait(&bars->v_empty[st], ph ^ 1, ab, p.status, kTimeoutCode)) {
@@ -210,6 +214,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         mbar_arrive_expect_tx(&bars->v_full[st], TILE_BYTES);
         tma_load_3d(smem + SM_V + st * TILE_BYTES, &tm_v, &bars->v_full[st], 0, kb * BN, kvz);
+        GQA_TRACE_EVENT(0, 1, it);
         issued = it + 1;
       }
       // Exit drain: every copy this CTA issued must have landed before the CTA
@@ -272,6 +277,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const uint32_t ph2 = ((it + 1) / NSTAGE) & 1;
           if (!mbar_wait(&bars->v_full[st], ph, ab, p.status, kTimeoutCode)) { ok = false; break; }
           if (!mbar_wait(&bars->p_full[0], pp, ab, p.status, kTimeoutCode)) { ok = false; break; }
+          GQA_TRACE_EVENT(0, 2, it);
           tc_fence_after_sync();
           issue_pv(0, st, it > 0);
           if (more) {
@@ -280,7 +286,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             issue_qk(0, st2);
           }
           if (two) {
+            GQA_TRACE_EVENT(0, 3, it);
             if (!mbar_wait(&bars->p_full[1], pp, ab, p.status, kTimeoutCode)) { ok = false; break; }
+            GQA_TRACE_EVENT(0, 4, it);
             tc_fence_after_sync();
             issue_pv(1, st, it > 0);
           }
@@ -289,6 +297,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (two) issue_qk(1, st2);
             mma_commit(&bars->k_empty[st2]);
           }
+          GQA_TRACE_EVENT(0, 5, it);
         }
       }
       // Final commit: on the normal path it releases the epilogue; on the abort
@@ -320,6 +329,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int it = 0; it < n; ++it) {
         const int kb = kr.tile(it);
         if (!mbar_wait(&bars->s_full[t], it & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        if (lane == 0 && (warp == 4 || warp == 8)) GQA_TRACE_EVENT(0, warp == 4 ? 6 : 10, it);
         tc_fence_after_sync();
         float s[BN];
         {
@@ -333,6 +343,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           reg_fence(r1);
           reg_fence(r2);
           reg_fence(r3);
+          if (lane == 0 && warp == 4) GQA_TRACE_EVENT(0, 7, it);
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             s[c] = __uint_as_float(r0[c]);
@@ -350,18 +361,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             s[c] = vis ? s[c] : -CUDART_INF_F;
           }
         }
-        float mx = s[0];
+        // row max and row sum as 8 independent chains (short dependency depth)
+        float mx8[8];
 #pragma unroll
-        for (int c = 1; c < BN; ++c) mx = fmaxf(mx, s[c]);
+        for (int a = 0; a < 8; ++a) mx8[a] = s[a];
+#pragma unroll
+        for (int c = 8; c < BN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         const float m_new = fmaxf(m_run, mx * sl2);
         const float m_use = (m_new == -CUDART_INF_F) ? 0.f : m_new;
         const float alpha = ex2_approx(m_run - m_use);
-        float sum = 0.f;
+        float sum8[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) sum8[a] = 0.f;
 #pragma unroll
         for (int c = 0; c < BN; ++c) {
           s[c] = ex2_approx(fmaf(s[c], sl2, -m_use));
-          sum += s[c];
+          sum8[c & 7] += s[c];
         }
+        const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+                          ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
         // P (bf16) for the P.V product
         if constexpr (P_TMEM) {
 #pragma unroll
@@ -385,6 +405,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             *reinterpret_cast<uint4 *>(p_smem + sub * TILE_BYTES + r * 128 + ((cc ^ (r & 7)) << 4)) = w;
           }
         }
+        if (lane == 0 && warp == 4) GQA_TRACE_EVENT(0, 8, it);
         // O correction: rescale the accumulator when the row max grew.  S_t of
         // this tile was committed after P.V of the previous tile, so O_t is final
         // for the previous tile here.
@@ -409,11 +430,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tmem_wait_st();
         if constexpr (!P_TMEM) fence_proxy_async_smem();
         tc_fence_before_sync();
+        if (lane == 0 && (warp == 4 || warp == 8)) GQA_TRACE_EVENT(0, warp == 4 ? 9 : 11, it);
         mbar_arrive(&bars->p_full[t]);
         l_run = l_run * alpha + sum;
         m_run = m_new;
       }
       if (ok && mbar_wait(&bars->o_full, 0, ab, p.status, kTimeoutCode)) {
+        if (lane == 0 && warp == 4) GQA_TRACE_EVENT(0, 12, 0);
         tc_fence_after_sync();
         uint32_t o0[32], o1[32];
         tmem_ld_32x32b_x32(t_o + 0, o0);
@@ -447,12 +470,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           // natural-log LSE of the scaled scores: (m + log2 l) * ln 2
           p.lse[row] = (m_run + __log2f(l_run)) * 0.69314718055994530942f;
         }
+        if (lane == 0 && warp == 4) GQA_TRACE_EVENT(0, 13, 0);
       }
     }
   }
 
   tc_fence_before_sync();
   __syncthreads();
+  if (threadIdx.x == 0) GQA_TRACE_EVENT(0, 15, 0);
   if (warp == 2) {
     tc_fence_after_sync();
     tmem_dealloc(tbase, TMEM_COLS);

@@ -12,6 +12,7 @@
 
 #include "../../include/gqa_attn.h"
 #include "timing.cuh"
+#include "trace.cuh"
 #include "bwd_kernels.cuh"
 #include "fwd_kernel.cuh"
 
@@ -250,6 +251,18 @@ int gqa_attn_timing_collect(float *ms, int n) {
   }
   return rc;
 }
+
+#ifdef GQA_TRACE
+// Trace builds only (not part of the public header): copies the clock64 event
+// table [kernel][cta][event][step] (unsigned 64-bit) to host memory.
+GQA_API int gqa_attn_trace_read(void *host, size_t bytes) {
+  if (!host || bytes < sizeof(g_gqa_trace)) return GQA_ERR_NULL;
+  if (cudaDeviceSynchronize() != cudaSuccess) return GQA_ERR_CUDA;
+  return cudaMemcpyFromSymbol(host, g_gqa_trace, sizeof(g_gqa_trace)) == cudaSuccess
+             ? GQA_OK
+             : GQA_ERR_CUDA;
+}
+#endif
 
 int gqa_attn_last_device_status(void *stream) {
   DeviceState *ds = nullptr;

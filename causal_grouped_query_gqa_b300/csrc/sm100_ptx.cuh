@@ -56,9 +56,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that lets the hardware suspend the thread until the phase completes
+// or `suspend_ns` elapses, so waiting warps do not spin on the shared-memory pipe.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
+                                                    uint32_t suspend_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(suspend_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Budget of one wait.  Legitimate waits inside one CTA last microseconds; a
 // wait that lasts this long means the pipeline is broken.
 constexpr uint64_t kWaitBudgetNs = 2000000000ull;  // 2 s
+// Longest single hardware suspension inside a wait (the thread wakes earlier
+// when the phase completes); the budget above is checked between suspensions.
+constexpr uint32_t kSuspendNs = 1000000u;  // 1 ms
 
 // Shared abort state of one CTA: once any role gives up, the others stop
 // waiting too and everyone reaches the common exit (where TMEM is freed).
@@ -74,15 +92,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, AbortS
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(a, parity)) return true;
-    if ((it & 63u) == 0u) {
-      if (ab->flag) return false;
-      if (globaltimer_ns() - t0 > kWaitBudgetNs) {
-        ab->flag = 1;
-        if (status) atomicCAS(status, 0, code);
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_wait_sleep(a, parity, kSuspendNs)) return true;
+    if (ab->flag) return false;
+    if (globaltimer_ns() - t0 > kWaitBudgetNs) {
+      ab->flag = 1;
+      if (status) atomicCAS(status, 0, code);
+      return false;
     }
   }
 }
@@ -91,7 +107,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, AbortS
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity) {
   const uint32_t a = smem_u32(bar);
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(a, parity)) {
+  while (!mbar_try_wait_sleep(a, parity, kSuspendNs)) {
     if (globaltimer_ns() - t0 > kWaitBudgetNs) return false;
   }
   return true;
