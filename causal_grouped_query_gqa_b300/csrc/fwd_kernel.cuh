@@ -15,13 +15,21 @@
 // Roles (384 threads):
 //   warp 0        TMA producer: Q tiles once, then K and V tiles through an
 //                 NSTAGE-deep shared-memory ring (full/empty mbarriers).
-//   warp 1        MMA issuer (one thread): S_t = Q_t K^T into TMEM, then
-//                 O_t += P_t V with P_t read from TMEM (or shared memory).
+//   warps 1, 3    MMA issuers, one thread per query head t: S_t = Q_t K^T into
+//                 TMEM, then O_t += P_t V with P_t read from TMEM (A operand in
+//                 TMEM).  Two issuing threads keep the tensor pipe fed while
+//                 either one waits on a barrier (an mbarrier wait costs about as
+//                 much as two MMAs, and the tensor queue is only a few deep).
 //   warp 2        allocates / frees the 512 TMEM columns.
 //   warps 4..7    softmax + O correction + epilogue of head 0 (one row per thread)
 //   warps 8..11   the same for head 1
-// TMEM columns: S0 [0,128) S1 [128,256) O0 [256,320) O1 [320,384); P_t (bf16
-// pairs) overwrites the first 64 columns of S_t once S_t has been read.
+// TMEM columns: S0 [0,128) S1 [128,256) O0 [256,320) O1 [320,384)
+//               P0 [384,448) P1 [448,512) (bf16 pairs).
+// Because P has its own columns, S_t(j+1) = Q_t K_{j+1}^T is issued as soon as
+// the softmax of head t has read S_t(j) into registers; only the P store and
+// the O correction wait for P_t V_j to finish.  Each head's issuer runs
+//   QK_t(j+1) PV_t(j) QK_t(j+2) PV_t(j+1) ...
+// and each head's softmax of tile j+1 overlaps the other head's products.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -39,37 +47,40 @@ constexpr int HD = 64;   // head dimension
 constexpr int NSTAGE = 3;
 constexpr int TILE_BYTES = BM * HD * 2;  // 16 KB, 128-byte rows
 constexpr int NTHREADS = 384;
+// Registers per thread after the split: warps 0-3 (producer, MMA, TMEM alloc)
+// drop to kRegsControl, the two softmax warpgroups rise to kRegsSoftmax.
+constexpr int kRegsControl = 80;
+constexpr int kRegsSoftmax = 200;
+// the launch allocation must cover the split (checked on the host)
+constexpr int kMinLaunchRegs = (128 * kRegsControl + 256 * kRegsSoftmax + NTHREADS - 1) / NTHREADS;
 constexpr uint32_t TMEM_COLS = 512;
+// A row keeps its running max until a tile's max exceeds it by more than this
+// (base-2 units), so P stays below 2^8 and O is rescaled only rarely; the
+// result is exact because O and l are normalised with the same running max.
+constexpr float kRescaleThreshold = 8.0f;
 __device__ __forceinline__ uint32_t col_s(int t) { return static_cast<uint32_t>(t) * 128u; }
 __device__ __forceinline__ uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(t) * 64u; }
+__device__ __forceinline__ uint32_t col_p(int t) { return 384u + static_cast<uint32_t>(t) * 64u; }
 
 constexpr int SM_Q = 0;
 constexpr int SM_K = SM_Q + 2 * TILE_BYTES;
 constexpr int SM_V = SM_K + NSTAGE * TILE_BYTES;
-constexpr int SM_P = SM_V + NSTAGE * TILE_BYTES;  // P tiles when P goes through smem
-
-template <bool P_TMEM>
-constexpr int bars_offset() {
-  return P_TMEM ? SM_P : SM_P + 2 * 2 * TILE_BYTES;
-}
+constexpr int SM_BARS = SM_V + NSTAGE * TILE_BYTES;
 
 struct Bars {
   uint64_t q_full;
-  uint64_t k_full[NSTAGE];
-  uint64_t k_empty[NSTAGE];
-  uint64_t v_full[NSTAGE];
-  uint64_t v_empty[NSTAGE];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t o_full;
+  uint64_t kv_full[NSTAGE];   // K and V tile landed (TMA transaction bytes)
+  uint64_t kv_empty[NSTAGE];  // every head's products with the tile finished
+  uint64_t s_full[2];  // S_t ready (MMA commit)
+  uint64_t s_free[2];  // S_t read into registers (128 softmax threads)
+  uint64_t p_full[2];  // P_t stored and O_t corrected (128 softmax threads)
+  uint64_t o_done[2];  // P_t V finished (MMA commit)
+  uint64_t o_full[2];  // every product of head t finished (MMA commit)
   uint32_t tmem_base;
   AbortState abort;
 };
 
-template <bool P_TMEM>
-constexpr int smem_bytes() {
-  return 1024 /* alignment slack */ + bars_offset<P_TMEM>() + static_cast<int>(sizeof(Bars));
-}
+constexpr int SMEM_BYTES = 1024 /* alignment slack */ + SM_BARS + static_cast<int>(sizeof(Bars));
 
 struct Params {
   int B, H, G, S, R;
@@ -133,7 +144,6 @@ __device__ __forceinline__ bool tile_needs_mask(int qb, int kb, const Params &p)
   return false;
 }
 
-template <bool P_TMEM>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gqa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
@@ -142,7 +152,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // 1024-byte alignment for the swizzled tiles, by pointer arithmetic on the
   // __shared__ array so that accesses stay shared-space (ld/st.shared).
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  Bars *bars = reinterpret_cast<Bars *>(smem + bars_offset<P_TMEM>());
+  Bars *bars = reinterpret_cast<Bars *>(smem + SM_BARS);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -162,16 +172,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
     for (int s = 0; s < NSTAGE; ++s) {
-      mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->k_empty[s], 1);
-      mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->v_empty[s], 1);
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], two ? 2 : 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->s_free[t], 128);
       mbar_init(&bars->p_full[t], 128);
+      mbar_init(&bars->o_done[t], 1);
+      mbar_init(&bars->o_full[t], 1);
     }
-    mbar_init(&bars->o_full, 1);
     bars->abort.flag = 0;
     fence_mbar_init();
   }
@@ -186,6 +196,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   AbortState *ab = &bars->abort;
   if (threadIdx.x == 0) GQA_TRACE_EVENT(0, 14, 0);
 
+  if (warp < 4) {
+  setmaxnreg_dec<kRegsControl>();
   if (warp == 0) {
     // ================================================================ producer
     if (lane == 0) {
@@ -202,111 +214,77 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int st = it % NSTAGE;
         const uint32_t ph = (it / NSTAGE) & 1;
         const int kb = kr.tile(it);
-        if (!mbar_wait(&bars->k_empty[st], ph ^ 1, ab, p.status, kTimeoutCode)) break;
+        if (!mbar_wait(&bars->kv_empty[st], ph ^ 1, ab, p.status, kTimeoutCode)) break;
         GQA_TRACE_EVENT(0, 0, it);
-        mbar_arrive_expect_tx(&bars->k_full[st], TILE_BYTES);
-        tma_load_3d(smem + SM_K + st * TILE_BYTES, &tm_k, &bars->k_full[st], 0, kb * BN, kvz);
-        if (!mbar_wait(&bars->v_empty[st], ph ^ 1, ab, p.status, kTimeoutCode)) {
-          issued = it + 1;  // K of this tile is in flight, V is not
-          mbar_wait_drain(&bars->k_full[st], ph);
-          issued = it;  // drained
-          break;
-        }
-        mbar_arrive_expect_tx(&bars->v_full[st], TILE_BYTES);
-        tma_load_3d(smem + SM_V + st * TILE_BYTES, &tm_v, &bars->v_full[st], 0, kb * BN, kvz);
+        mbar_arrive_expect_tx(&bars->kv_full[st], 2 * TILE_BYTES);
+        tma_load_3d(smem + SM_K + st * TILE_BYTES, &tm_k, &bars->kv_full[st], 0, kb * BN, kvz);
+        tma_load_3d(smem + SM_V + st * TILE_BYTES, &tm_v, &bars->kv_full[st], 0, kb * BN, kvz);
         GQA_TRACE_EVENT(0, 1, it);
         issued = it + 1;
       }
       // Exit drain: every copy this CTA issued must have landed before the CTA
       // leaves (no-op on the normal path, where the consumers already saw them).
       mbar_wait_drain(&bars->q_full, 0);
-      for (int it = max(0, issued - NSTAGE); it < issued; ++it) {
+      for (int it = max(0, issued - NSTAGE); it < issued; ++it)
+        mbar_wait_drain(&bars->kv_full[it % NSTAGE], (it / NSTAGE) & 1);
+    }
+  } else if ((warp == 1 || warp == 3) && lane == 0 && (warp == 1 || two)) {
+    // ================================================================ MMA issuers
+    const int t = warp == 1 ? 0 : 1;  // the query head this thread serves
+    const uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false, false);
+    const uint32_t idesc_pv = idesc_bf16_f32(BM, HD, false, true);
+    const uint32_t q_addr = smem_u32(smem + SM_Q + t * TILE_BYTES);
+    const uint32_t k_addr0 = smem_u32(smem + SM_K);
+    const uint32_t v_addr0 = smem_u32(smem + SM_V);
+    const uint32_t d_s = tbase + col_s(t), d_o = tbase + col_o(t), a_p = tbase + col_p(t);
+
+    auto issue_qk = [&](int st) {
+      const uint64_t ad = sdesc_sw128(q_addr, 16, 1024);
+      const uint64_t bd = sdesc_sw128(k_addr0 + st * TILE_BYTES, 16, 1024);
+#pragma unroll
+      for (int ks = 0; ks < HD / 16; ++ks)  // K step 16 bf16 = 32 B inside the 128-B row
+        mma_bf16_ss(d_s, ad + 2 * ks, bd + 2 * ks, idesc_qk, ks > 0);
+      mma_commit(&bars->s_full[t]);
+    };
+    auto issue_pv = [&](int st, bool acc) {
+      const uint64_t bd = sdesc_sw128(v_addr0 + st * TILE_BYTES, TILE_BYTES, 1024);
+#pragma unroll
+      for (int ks = 0; ks < BN / 16; ++ks)  // 16 keys = two 8-row groups = 2048 B
+        mma_bf16_ts(d_o, a_p + ks * 8, bd + (ks * 2048 >> 4), idesc_pv, (acc || ks > 0) ? 1u : 0u);
+      mma_commit(&bars->o_done[t]);
+    };
+
+    bool ok = mbar_wait(&bars->q_full, 0, ab, p.status, kTimeoutCode);
+    ok = ok && mbar_wait(&bars->kv_full[0], 0, ab, p.status, kTimeoutCode);
+    if (ok) {
+      tc_fence_after_sync();
+      issue_qk(0);
+      for (int it = 0; it < n; ++it) {
         const int st = it % NSTAGE;
-        const uint32_t ph = (it / NSTAGE) & 1;
-        mbar_wait_drain(&bars->k_full[st], ph);
-        mbar_wait_drain(&bars->v_full[st], ph);
-      }
-    }
-  } else if (warp == 1) {
-    // ================================================================ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false, false);
-      const uint32_t idesc_pv = idesc_bf16_f32(BM, HD, false, true);
-      const uint32_t q_addr0 = smem_u32(smem + SM_Q);
-      const uint32_t k_addr0 = smem_u32(smem + SM_K);
-      const uint32_t v_addr0 = smem_u32(smem + SM_V);
-      const uint32_t p_addr0 = smem_u32(smem + SM_P);
-
-      auto issue_qk = [&](int t, int st) {
-        const uint64_t ad = sdesc_sw128(q_addr0 + t * TILE_BYTES, 16, 1024);
-        const uint64_t bd = sdesc_sw128(k_addr0 + st * TILE_BYTES, 16, 1024);
-#pragma unroll
-        for (int ks = 0; ks < HD / 16; ++ks)  // K step 16 bf16 = 32 B inside the 128-B row
-          mma_bf16_ss(tbase + col_s(t), ad + 2 * ks, bd + 2 * ks, idesc_qk, ks > 0);
-        mma_commit(&bars->s_full[t]);
-      };
-      auto issue_pv = [&](int t, int st, bool acc) {
-        const uint64_t bd = sdesc_sw128(v_addr0 + st * TILE_BYTES, TILE_BYTES, 1024);
-#pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks) {  // 16 keys = two 8-row groups = 2048 B
-          const uint32_t acc_k = (acc || ks > 0) ? 1u : 0u;
-          if constexpr (P_TMEM) {
-            mma_bf16_ts(tbase + col_o(t), tbase + col_s(t) + ks * 8, bd + (ks * 2048 >> 4),
-                        idesc_pv, acc_k);
-          } else {
-            const uint32_t pa = p_addr0 + t * 2 * TILE_BYTES + (ks / 4) * TILE_BYTES + (ks % 4) * 32;
-            mma_bf16_ss(tbase + col_o(t), sdesc_sw128(pa, 16, 1024), bd + (ks * 2048 >> 4),
-                        idesc_pv, acc_k);
-          }
-        }
-      };
-
-      bool ok = mbar_wait(&bars->q_full, 0, ab, p.status, kTimeoutCode);
-      ok = ok && mbar_wait(&bars->k_full[0], 0, ab, p.status, kTimeoutCode);
-      if (ok) {
-        tc_fence_after_sync();
-        issue_qk(0, 0);
-        if (two) issue_qk(1, 0);
-        mma_commit(&bars->k_empty[0]);
-        for (int it = 0; it < n; ++it) {
-          const int st = it % NSTAGE;
-          const uint32_t ph = (it / NSTAGE) & 1;
-          const uint32_t pp = it & 1;
-          const bool more = it + 1 < n;
+        const uint32_t pp = it & 1;
+        if (it + 1 < n) {
           const int st2 = (it + 1) % NSTAGE;
-          const uint32_t ph2 = ((it + 1) / NSTAGE) & 1;
-          if (!mbar_wait(&bars->v_full[st], ph, ab, p.status, kTimeoutCode)) { ok = false; break; }
-          if (!mbar_wait(&bars->p_full[0], pp, ab, p.status, kTimeoutCode)) { ok = false; break; }
-          GQA_TRACE_EVENT(0, 2, it);
+          if (!mbar_wait(&bars->kv_full[st2], ((it + 1) / NSTAGE) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+          if (!mbar_wait(&bars->s_free[t], pp, ab, p.status, kTimeoutCode)) { ok = false; break; }
           tc_fence_after_sync();
-          issue_pv(0, st, it > 0);
-          if (more) {
-            if (!mbar_wait(&bars->k_full[st2], ph2, ab, p.status, kTimeoutCode)) { ok = false; break; }
-            tc_fence_after_sync();
-            issue_qk(0, st2);
-          }
-          if (two) {
-            GQA_TRACE_EVENT(0, 3, it);
-            if (!mbar_wait(&bars->p_full[1], pp, ab, p.status, kTimeoutCode)) { ok = false; break; }
-            GQA_TRACE_EVENT(0, 4, it);
-            tc_fence_after_sync();
-            issue_pv(1, st, it > 0);
-          }
-          mma_commit(&bars->v_empty[st]);
-          if (more) {
-            if (two) issue_qk(1, st2);
-            mma_commit(&bars->k_empty[st2]);
-          }
-          GQA_TRACE_EVENT(0, 5, it);
+          issue_qk(st2);
         }
+        if (!mbar_wait(&bars->p_full[t], pp, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        if (t == 0) GQA_TRACE_EVENT(0, 2, it); else GQA_TRACE_EVENT(0, 4, it);
+        tc_fence_after_sync();
+        issue_pv(st, it > 0);
+        mma_commit(&bars->kv_empty[st]);  // this head is done with K_it (earlier) and V_it
+        if (t == 0) GQA_TRACE_EVENT(0, 3, it); else GQA_TRACE_EVENT(0, 5, it);
       }
-      // Final commit: on the normal path it releases the epilogue; on the abort
-      // path it lets this thread wait until the tensor pipe is idle before TMEM
-      // is freed.
-      mma_commit(&bars->o_full);
-      if (!ok) mbar_wait_drain(&bars->o_full, 0);
     }
-  } else if (warp >= 4) {
+    // Final commit: on the normal path it releases this head's epilogue; on
+    // the abort path it lets this thread wait until its products are done
+    // before TMEM is freed.
+    mma_commit(&bars->o_full[t]);
+    if (!ok) mbar_wait_drain(&bars->o_full[t], 0);
+  }
+  } else {
+    setmaxnreg_inc<kRegsSoftmax>();
     // ================================================================ softmax
     const int t = (warp - 4) >> 2;
     if (t == 0 || two) {
@@ -319,9 +297,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const bool win = p.causal && p.window > 0;
       const int lo = win ? i - p.window : -1;
       const int ns = win ? p.n_sink : 0;
-      const uint32_t t_s = tbase + (static_cast<uint32_t>(lane_base) << 16) + col_s(t);
-      const uint32_t t_o = tbase + (static_cast<uint32_t>(lane_base) << 16) + col_o(t);
-      uint8_t *p_smem = smem + SM_P + t * 2 * TILE_BYTES;
+      const uint32_t lane_off = static_cast<uint32_t>(lane_base) << 16;
+      const uint32_t t_s = tbase + lane_off + col_s(t);
+      const uint32_t t_o = tbase + lane_off + col_o(t);
+      const uint32_t t_p = tbase + lane_off + col_p(t);
+      const uint64_t sl2x2 = f32x2(sl2, sl2);
 
       float m_run = -CUDART_INF_F;  // running max of scaled scores, base-2 units
       float l_run = 0.f;            // running sum of 2^(s - m_run)
@@ -331,26 +311,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!mbar_wait(&bars->s_full[t], it & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
         if (lane == 0 && (warp == 4 || warp == 8)) GQA_TRACE_EVENT(0, warp == 4 ? 6 : 10, it);
         tc_fence_after_sync();
+        uint32_t s0[32], s1[32], s2[32], s3[32];
+        tmem_ld_32x32b_x32(t_s + 0, s0);
+        tmem_ld_32x32b_x32(t_s + 32, s1);
+        tmem_ld_32x32b_x32(t_s + 64, s2);
+        tmem_ld_32x32b_x32(t_s + 96, s3);
+        tmem_wait_ld();
+        reg_fence(s0);
+        reg_fence(s1);
+        reg_fence(s2);
+        reg_fence(s3);
+        // S_t is in registers: the next Q_t K^T may overwrite it
+        tc_fence_before_sync();
+        mbar_arrive(&bars->s_free[t]);
+        if (lane == 0 && warp == 4) GQA_TRACE_EVENT(0, 7, it);
         float s[BN];
-        {
-          uint32_t r0[32], r1[32], r2[32], r3[32];
-          tmem_ld_32x32b_x32(t_s + 0, r0);
-          tmem_ld_32x32b_x32(t_s + 32, r1);
-          tmem_ld_32x32b_x32(t_s + 64, r2);
-          tmem_ld_32x32b_x32(t_s + 96, r3);
-          tmem_wait_ld();
-          reg_fence(r0);
-          reg_fence(r1);
-          reg_fence(r2);
-          reg_fence(r3);
-          if (lane == 0 && warp == 4) GQA_TRACE_EVENT(0, 7, it);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            s[c] = __uint_as_float(r0[c]);
-            s[32 + c] = __uint_as_float(r1[c]);
-            s[64 + c] = __uint_as_float(r2[c]);
-            s[96 + c] = __uint_as_float(r3[c]);
-          }
+        for (int c = 0; c < 32; ++c) {
+          s[c] = __uint_as_float(s0[c]);
+          s[32 + c] = __uint_as_float(s1[c]);
+          s[64 + c] = __uint_as_float(s2[c]);
+          s[96 + c] = __uint_as_float(s3[c]);
         }
         if (tile_needs_mask(qb, kb, p)) {
           const int j0 = kb * BN;
@@ -361,56 +342,45 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             s[c] = vis ? s[c] : -CUDART_INF_F;
           }
         }
-        // row max and row sum as 8 independent chains (short dependency depth)
-        float mx8[8];
+        // row max: 4 independent chains of 3-input max over elements 8..127,
+        // seeded with elements 0..7
+        float mx4[4];
 #pragma unroll
-        for (int a = 0; a < 8; ++a) mx8[a] = s[a];
+        for (int a = 0; a < 4; ++a) mx4[a] = fmaxf(s[2 * a], s[2 * a + 1]);
 #pragma unroll
-        for (int c = 8; c < BN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-        const float m_new = fmaxf(m_run, mx * sl2);
+        for (int c = 8; c < BN; c += 8) {
+#pragma unroll
+          for (int a = 0; a < 4; ++a) mx4[a] = max3f(mx4[a], s[c + 2 * a], s[c + 2 * a + 1]);
+        }
+        const float mx = fmaxf(max3f(mx4[0], mx4[1], mx4[2]), mx4[3]);
+        const float m_tile = mx * sl2;
+        // lazy rescale: keep the running max unless this tile exceeds it by > threshold
+        const bool need = m_tile > m_run + kRescaleThreshold;
+        const float m_new = need ? m_tile : m_run;
         const float m_use = (m_new == -CUDART_INF_F) ? 0.f : m_new;
-        const float alpha = ex2_approx(m_run - m_use);
-        float sum8[8];
+        const float alpha = need ? ex2_approx(m_run - m_use) : 1.f;
+        const uint64_t negm = f32x2(-m_use, -m_use);
+        uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};  // four chains of fp32 pairs (0.0f bits)
+        uint32_t pk[BN / 2];
 #pragma unroll
-        for (int a = 0; a < 8; ++a) sum8[a] = 0.f;
-#pragma unroll
-        for (int c = 0; c < BN; ++c) {
-          s[c] = ex2_approx(fmaf(s[c], sl2, -m_use));
-          sum8[c & 7] += s[c];
+        for (int c2 = 0; c2 < BN / 2; ++c2) {
+          const uint64_t x = fma_f32x2(f32x2(s[2 * c2], s[2 * c2 + 1]), sl2x2, negm);
+          float x0, x1;
+          f32x2_split(x, x0, x1);
+          const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+          sum2[c2 & 3] = add_f32x2(sum2[c2 & 3], f32x2(e0, e1));
+          pk[c2] = pack_bf16x2(e0, e1);
         }
-        const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
-                          ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-        // P (bf16) for the P.V product
-        if constexpr (P_TMEM) {
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t pk[32];
-#pragma unroll
-            for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(s[half * 64 + 2 * c], s[half * 64 + 2 * c + 1]);
-            tmem_st_32x32b_x32(t_s + half * 32, pk);
-          }
-        } else {
-          // 128-byte-swizzled K-major tile: row r, 16-byte chunk c of the
-          // 64-key sub-tile lands at chunk (c ^ (r & 7)).
-#pragma unroll
-          for (int ch = 0; ch < 16; ++ch) {
-            const int sub = ch >> 3, cc = ch & 7;
-            uint4 w;
-            w.x = pack_bf16x2(s[ch * 8 + 0], s[ch * 8 + 1]);
-            w.y = pack_bf16x2(s[ch * 8 + 2], s[ch * 8 + 3]);
-            w.z = pack_bf16x2(s[ch * 8 + 4], s[ch * 8 + 5]);
-            w.w = pack_bf16x2(s[ch * 8 + 6], s[ch * 8 + 7]);
-            *reinterpret_cast<uint4 *>(p_smem + sub * TILE_BYTES + r * 128 + ((cc ^ (r & 7)) << 4)) = w;
-          }
-        }
+        float sa, sb, sc, sd;
+        f32x2_split(add_f32x2(sum2[0], sum2[1]), sa, sb);
+        f32x2_split(add_f32x2(sum2[2], sum2[3]), sc, sd);
+        const float sum = (sa + sb) + (sc + sd);
         if (lane == 0 && warp == 4) GQA_TRACE_EVENT(0, 8, it);
-        // O correction: rescale the accumulator when the row max grew.  S_t of
-        // this tile was committed after P.V of the previous tile, so O_t is final
-        // for the previous tile here.
+        // P_t V of the previous tile must be finished before P_t is overwritten
+        // and O_t rescaled.
         if (it > 0) {
-          const bool need = alpha != 1.f;
+          if (!mbar_wait(&bars->o_done[t], (it - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+          tc_fence_after_sync();
           if (__any_sync(0xffffffffu, need)) {
             uint32_t o0[32], o1[32];
             tmem_ld_32x32b_x32(t_o + 0, o0);
@@ -418,24 +388,39 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tmem_wait_ld();
             reg_fence(o0);
             reg_fence(o1);
+            const uint64_t a2 = f32x2(alpha, alpha);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              o0[c] = __float_as_uint(__uint_as_float(o0[c]) * alpha);
-              o1[c] = __float_as_uint(__uint_as_float(o1[c]) * alpha);
+            for (int c = 0; c < 32; c += 2) {
+              float x0, x1;
+              f32x2_split(mul_f32x2(f32x2(__uint_as_float(o0[c]), __uint_as_float(o0[c + 1])), a2), x0, x1);
+              o0[c] = __float_as_uint(x0);
+              o0[c + 1] = __float_as_uint(x1);
+              f32x2_split(mul_f32x2(f32x2(__uint_as_float(o1[c]), __uint_as_float(o1[c + 1])), a2), x0, x1);
+              o1[c] = __float_as_uint(x0);
+              o1[c + 1] = __float_as_uint(x1);
             }
             tmem_st_32x32b_x32(t_o + 0, o0);
             tmem_st_32x32b_x32(t_o + 32, o1);
           }
         }
+        {
+          uint32_t p0[32], p1[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            p0[c] = pk[c];
+            p1[c] = pk[32 + c];
+          }
+          tmem_st_32x32b_x32(t_p + 0, p0);
+          tmem_st_32x32b_x32(t_p + 32, p1);
+        }
         tmem_wait_st();
-        if constexpr (!P_TMEM) fence_proxy_async_smem();
         tc_fence_before_sync();
         if (lane == 0 && (warp == 4 || warp == 8)) GQA_TRACE_EVENT(0, warp == 4 ? 9 : 11, it);
         mbar_arrive(&bars->p_full[t]);
         l_run = l_run * alpha + sum;
         m_run = m_new;
       }
-      if (ok && mbar_wait(&bars->o_full, 0, ab, p.status, kTimeoutCode)) {
+      if (ok && mbar_wait(&bars->o_full[t], 0, ab, p.status, kTimeoutCode)) {
         if (lane == 0 && warp == 4) GQA_TRACE_EVENT(0, 12, 0);
         tc_fence_after_sync();
         uint32_t o0[32], o1[32];

@@ -53,14 +53,14 @@ int device_state(DeviceState **out) {
       return GQA_ERR_CUDA;
     if (cudaGetSymbolAddress(reinterpret_cast<void **>(&st.status), g_device_status) != cudaSuccess)
       return GQA_ERR_CUDA;
-#ifdef GQA_FWD_P_IN_SMEM
-    constexpr bool kPTmem = false;
-#else
-    constexpr bool kPTmem = true;
-#endif
-    if (cudaFuncSetAttribute(gqa::fwd::gqa_fwd_kernel<kPTmem>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             gqa::fwd::smem_bytes<kPTmem>()) != cudaSuccess)
+    if (cudaFuncSetAttribute(gqa::fwd::gqa_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             gqa::fwd::SMEM_BYTES) != cudaSuccess)
+      return GQA_ERR_CUDA;
+    // The forward rebalances registers between warpgroups (setmaxnreg); that is
+    // only safe when the compiled launch allocation covers the split.
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, gqa::fwd::gqa_fwd_kernel) != cudaSuccess ||
+        fa.numRegs < gqa::fwd::kMinLaunchRegs)
       return GQA_ERR_CUDA;
     int rc = gqa::bwd::configure_kernels();
     if (rc != 0) return GQA_ERR_CUDA;
@@ -158,15 +158,9 @@ int gqa_attn_fwd(const void *q, const void *k, const void *v, void *o, float *ls
   const long long units = static_cast<long long>(p.n_qblocks) * B * G * p.n_pairs;
   if (units > 0x7fffffffLL) return GQA_ERR_SHAPE;
 
-#ifdef GQA_FWD_P_IN_SMEM
-  constexpr bool kPTmem = false;
-#else
-  constexpr bool kPTmem = true;
-#endif
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   gqa::timing_begin(GQA_KERNEL_FWD, st);
-  gqa_fwd_kernel<kPTmem><<<static_cast<unsigned>(units), NTHREADS, smem_bytes<kPTmem>(), st>>>(
-      tq, tk, tv, p);
+  gqa_fwd_kernel<<<static_cast<unsigned>(units), NTHREADS, SMEM_BYTES, st>>>(tq, tk, tv, p);
   gqa::timing_end(GQA_KERNEL_FWD, st);
   return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
