@@ -76,6 +76,8 @@ struct Bars {
   uint64_t p_full[2];  // P_t stored and O_t corrected (128 softmax threads)
   uint64_t o_done[2];  // P_t V finished (MMA commit)
   uint64_t o_full[2];  // every product of head t finished (MMA commit)
+  uint64_t turn[2];    // ping-pong of the exp2 sections: turn[t] opens head t's
+                       // section (arrived by the other head's 128 threads)
   uint32_t tmem_base;
   AbortState abort;
 };
@@ -181,6 +183,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&bars->p_full[t], 128);
       mbar_init(&bars->o_done[t], 1);
       mbar_init(&bars->o_full[t], 1);
+      mbar_init(&bars->turn[t], 128);
     }
     bars->abort.flag = 0;
     fence_mbar_init();
@@ -360,6 +363,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const float m_use = (m_new == -CUDART_INF_F) ? 0.f : m_new;
         const float alpha = need ? ex2_approx(m_run - m_use) : 1.f;
         const uint64_t negm = f32x2(-m_use, -m_use);
+        // Ping-pong: the two heads take turns on the exp2 section (MUFU-bound), so
+        // each runs at the full MUFU rate while the other head's products keep
+        // the tensor pipe busy.  Head 0 goes first in every tile.
+        if (two) {
+          const bool wait_turn = (t == 1) || it > 0;
+          const uint32_t par = t == 0 ? ((it - 1) & 1) : (it & 1);
+          if (wait_turn && !mbar_wait(&bars->turn[t], par, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        }
         uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};  // four chains of fp32 pairs (0.0f bits)
         uint32_t pk[BN / 2];
 #pragma unroll
@@ -371,6 +382,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           sum2[c2 & 3] = add_f32x2(sum2[c2 & 3], f32x2(e0, e1));
           pk[c2] = pack_bf16x2(e0, e1);
         }
+        if (two) mbar_arrive(&bars->turn[1 - t]);
         float sa, sb, sc, sd;
         f32x2_split(add_f32x2(sum2[0], sum2[1]), sa, sb);
         f32x2_split(add_f32x2(sum2[2], sum2[3]), sc, sd);
