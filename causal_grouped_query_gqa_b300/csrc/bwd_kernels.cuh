@@ -14,11 +14,15 @@
 // Three launches on the caller's stream:
 //   prep   D (fp32), LSE * log2(e) (fp32), and the fp32 dQ accumulator cleared;
 //   main   one CTA per (b, kv head g, 128-key tile): for each of the R query
-//          heads of g and each query tile that sees the key tile, on tcgen05:
+//          heads of g and each query tile that sees the key tile (a "step"),
+//          on tcgen05:
 //            S^T  = K Q^T       dP^T = V dO^T           (TMEM, fp32)
-//            P^T, dS^T (bf16) -> TMEM; dS (bf16) -> shared memory
+//            P^T (bf16) -> TMEM; dS (bf16) -> shared memory, which serves as
+//            dS^T (K-major) for dK and as dS (MN-major) for dQ
 //            dV  += P^T dO      dK  += dS^T Q           (TMEM, fp32, whole CTA life)
 //            dQ   = dS K        -> fp32 TMA reduce-add into the accumulator
+//          S^T, dP^T of step n+1 are issued as soon as the P/dS warps have read
+//          step n into registers, so those warps overlap step n's dV, dK, dQ.
 //          dK, dV are summed over the group's heads inside the CTA
 //          (deterministic) and written once as bf16;
 //   convert dQ = bf16(scale * accumulator).
@@ -44,15 +48,24 @@ constexpr int BQ = 128;  // query rows per tile
 constexpr int BK = 128;  // keys per CTA
 constexpr int HD = 64;
 constexpr int TILE_BYTES = 128 * HD * 2;  // 16 KB bf16 tile, 128-byte rows
-constexpr int NSTAGE = 2;                 // Q/dO ring depth
+constexpr int NSTAGE = 3;                 // Q/dO ring depth
 constexpr int NTHREADS = 512;
+// Registers per thread after the split: warps 0-3 (producer, two MMA issuers,
+// TMEM alloc), the two P/dS warpgroups, the dQ drain warpgroup.
+constexpr int kRegsControl = 72;
+constexpr int kRegsSoftmax = 168;
+constexpr int kRegsDrain = 96;
+// the launch allocation must cover the split (checked on the host)
+constexpr int kMinLaunchRegs =
+    (128 * (kRegsControl + kRegsDrain) + 256 * kRegsSoftmax + NTHREADS - 1) / NTHREADS;
 constexpr uint32_t TMEM_COLS = 512;
 // TMEM columns
-constexpr uint32_t C_S = 0;     // S^T (128 fp32), then P^T (bf16 pairs)
-constexpr uint32_t C_DP = 128;  // dP^T (128 fp32), then dS^T (bf16 pairs)
-constexpr uint32_t C_DV = 256;  // dV accumulator (64 fp32)
-constexpr uint32_t C_DK = 320;  // dK accumulator (64 fp32)
-constexpr uint32_t C_DQ = 384;  // dQ tile, two buffers of 64 fp32
+constexpr uint32_t C_S = 0;     // S^T (128 fp32)
+constexpr uint32_t C_DP = 128;  // dP^T (128 fp32)
+constexpr uint32_t C_PT = 256;  // P^T (64 columns of bf16 pairs: 128 queries)
+constexpr uint32_t C_DV = 320;  // dV accumulator (64 fp32)
+constexpr uint32_t C_DK = 384;  // dK accumulator (64 fp32)
+constexpr uint32_t C_DQ = 448;  // dQ tile (64 fp32)
 
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int SM_K = 0;
@@ -60,19 +73,22 @@ constexpr int SM_V = SM_K + TILE_BYTES;
 constexpr int SM_Q = SM_V + TILE_BYTES;                 // NSTAGE tiles
 constexpr int SM_DO = SM_Q + NSTAGE * TILE_BYTES;       // NSTAGE tiles
 constexpr int SM_DS = SM_DO + NSTAGE * TILE_BYTES;      // 32 KB: dS, two 64-query halves
-constexpr int SM_DQ = SM_DS + 2 * TILE_BYTES;           // 2 x 32 KB fp32 dQ staging
-constexpr int SM_VEC = SM_DQ + 2 * 2 * TILE_BYTES;      // NSTAGE x (LSE2[128], D[128]) fp32
+constexpr int SM_DQ = SM_DS + 2 * TILE_BYTES;           // 32 KB fp32 dQ staging
+constexpr int SM_VEC = SM_DQ + 2 * TILE_BYTES;          // NSTAGE x (LSE2[128], D[128]) fp32
 constexpr int SM_BARS = SM_VEC + NSTAGE * 2 * BQ * 4;
 
 struct Bars {
   uint64_t kv_full;
   uint64_t qdo_full[NSTAGE];
   uint64_t qdo_empty[NSTAGE];
-  uint64_t st_full;
-  uint64_t ds_ready;
-  uint64_t dq_full[2];
-  uint64_t dq_free[2];
-  uint64_t dkv_done;
+  uint64_t st_full;   // S^T, dP^T of the step ready (issuer A commit)
+  uint64_t st_free;   // S^T, dP^T read into registers (256 P/dS threads)
+  uint64_t ds_ready;  // P^T in TMEM and dS in shared memory (256 P/dS threads)
+  uint64_t pds_free;  // dV, dK, dQ of the step finished (issuer B commit)
+  uint64_t dq_full;   // dQ tile ready (issuer B commit)
+  uint64_t dq_free;   // dQ tile read out (128 drain threads)
+  uint64_t a_done;    // every product of issuer A finished
+  uint64_t dkv_done;  // every product of issuer B finished
   uint32_t tmem_base;
   AbortState abort;
 };
@@ -215,6 +231,59 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float *__rest
 
 // ------------------------------------------------------------------- main
 
+// P and dS of 32 query columns [cb, cb+32) for this thread's key row j.
+__device__ __forceinline__ void p_ds_chunk(const uint32_t (&sr)[32], const uint32_t (&dr)[32],
+                                           const float *lse2, const float *dlt, int cb, int i0,
+                                           int j, bool masked, bool win, float sl2,
+                                           const MainParams &p, uint32_t (&pp)[16],
+                                           uint32_t (&pd)[16]) {
+  // sub-chunks of 8 query columns: two broadcast 16-byte shared loads for the
+  // 8 LSE2 and two for the 8 D values, so few values are live at once
+#pragma unroll
+  for (int sc = 0; sc < 4; ++sc) {
+    const float4 la = reinterpret_cast<const float4 *>(lse2 + cb)[2 * sc];
+    const float4 lb = reinterpret_cast<const float4 *>(lse2 + cb)[2 * sc + 1];
+    const float4 da = reinterpret_cast<const float4 *>(dlt + cb)[2 * sc];
+    const float4 db = reinterpret_cast<const float4 *>(dlt + cb)[2 * sc + 1];
+    const float l8[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
+    const float d8[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
+    float pv[8], dv[8];
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      float x0, x1;
+      f32x2_split(fma_f32x2(f32x2(__uint_as_float(sr[8 * sc + e]), __uint_as_float(sr[8 * sc + e + 1])),
+                            f32x2(sl2, sl2), f32x2(-l8[e], -l8[e + 1])),
+                  x0, x1);
+      pv[e] = ex2_approx(x0);
+      pv[e + 1] = ex2_approx(x1);
+    }
+    if (masked) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int i = i0 + cb + 8 * sc + e;
+        const bool vis = (i < p.S) && (j < p.S) &&
+                         (!p.causal || (j <= i && (!win || j > i - p.window || j < p.n_sink)));
+        pv[e] = vis ? pv[e] : 0.f;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      float y0, y1;
+      f32x2_split(mul_f32x2(f32x2(pv[e], pv[e + 1]),
+                            add_f32x2(f32x2(__uint_as_float(dr[8 * sc + e]), __uint_as_float(dr[8 * sc + e + 1])),
+                                      f32x2(-d8[e], -d8[e + 1]))),
+                  y0, y1);
+      dv[e] = y0;
+      dv[e + 1] = y1;
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      pp[4 * sc + e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
+      pd[4 * sc + e] = pack_bf16x2(dv[2 * e], dv[2 * e + 1]);
+    }
+  }
+}
+
 __global__ void __launch_bounds__(NTHREADS, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -248,11 +317,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&bars->qdo_empty[s], 1);
     }
     mbar_init(&bars->st_full, 1);
+    mbar_init(&bars->st_free, 256);
     mbar_init(&bars->ds_ready, 256);
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(&bars->dq_full[t], 1);
-      mbar_init(&bars->dq_free[t], 128);
-    }
+    mbar_init(&bars->pds_free, 1);
+    mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->dq_free, 128);
+    mbar_init(&bars->a_done, 1);
     mbar_init(&bars->dkv_done, 1);
     bars->abort.flag = 0;
     fence_mbar_init();
@@ -268,9 +338,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   AbortState *ab = &bars->abort;
   if (threadIdx.x == 0) GQA_TRACE_EVENT(1, 15, 0);
 
-  if (warp == 0) {
-    // ============================================================ producer
-    if (lane == 0) {
+  if (warp < 4) {
+    setmaxnreg_dec<kRegsControl>();
+    if (warp == 0 && lane == 0) {
+      // ========================================================== producer
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
@@ -300,33 +371,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_wait_drain(&bars->kv_full, 0);
       for (int n = max(0, issued - NSTAGE); n < issued; ++n)
         mbar_wait_drain(&bars->qdo_full[n % NSTAGE], (n / NSTAGE) & 1);
-    }
-  } else if (warp == 1) {
-    // ============================================================ MMA issuer
-    if (lane == 0) {
-      const uint32_t id_nn = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
-      const uint32_t id_ts = idesc_bf16_f32(128, 64, false, true);    // dV, dK
-      const uint32_t id_dq = idesc_bf16_f32(128, 64, true, true);     // dQ
-      const uint32_t k_addr = smem_u32(smem + SM_K);
-      const uint32_t v_addr = smem_u32(smem + SM_V);
+    } else if (warp == 1 && lane == 0) {
+      // ================================================= issuer A: S^T, dP^T
+      const uint32_t id_nn = idesc_bf16_f32(128, 128, false, false);
+      const uint64_t k_kmaj = sdesc_sw128(smem_u32(smem + SM_K), 16, 1024);
+      const uint64_t v_kmaj = sdesc_sw128(smem_u32(smem + SM_V), 16, 1024);
       const uint32_t q_addr = smem_u32(smem + SM_Q);
       const uint32_t do_addr = smem_u32(smem + SM_DO);
-      const uint32_t ds_addr = smem_u32(smem + SM_DS);
-      const uint64_t k_kmaj = sdesc_sw128(k_addr, 16, 1024);
-      const uint64_t v_kmaj = sdesc_sw128(v_addr, 16, 1024);
-      const uint64_t k_mn = sdesc_sw128(k_addr, TILE_BYTES, 1024);
-      const uint64_t ds_mn = sdesc_sw128(ds_addr, TILE_BYTES, 1024);  // LBO: next 64-query half
       bool ok = mbar_wait(&bars->kv_full, 0, ab, p.status, kTimeoutCode);
       for (int n = 0; ok && n < nsteps; ++n) {
         const int st = n % NSTAGE;
-        const uint32_t ph = (n / NSTAGE) & 1;
-        const uint64_t q_kmaj = sdesc_sw128(q_addr + st * TILE_BYTES, 16, 1024);
-        const uint64_t do_kmaj = sdesc_sw128(do_addr + st * TILE_BYTES, 16, 1024);
-        const uint64_t q_mn = sdesc_sw128(q_addr + st * TILE_BYTES, TILE_BYTES, 1024);
-        const uint64_t do_mn = sdesc_sw128(do_addr + st * TILE_BYTES, TILE_BYTES, 1024);
-        if (!mbar_wait(&bars->qdo_full[st], ph, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        if (!mbar_wait(&bars->qdo_full[st], (n / NSTAGE) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        // the P/dS warps must have read the previous step's S^T and dP^T
+        if (n > 0 && !mbar_wait(&bars->st_free, (n - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
         GQA_TRACE_EVENT(1, 2, n);
         tc_fence_after_sync();
+        const uint64_t q_kmaj = sdesc_sw128(q_addr + st * TILE_BYTES, 16, 1024);
+        const uint64_t do_kmaj = sdesc_sw128(do_addr + st * TILE_BYTES, 16, 1024);
 #pragma unroll
         for (int ks = 0; ks < HD / 16; ++ks)
           mma_bf16_ss(tbase + C_S, k_kmaj + 2 * ks, q_kmaj + 2 * ks, id_nn, ks > 0);
@@ -335,39 +396,53 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           mma_bf16_ss(tbase + C_DP, v_kmaj + 2 * ks, do_kmaj + 2 * ks, id_nn, ks > 0);
         mma_commit(&bars->st_full);
         GQA_TRACE_EVENT(1, 3, n);
+      }
+      mma_commit(&bars->a_done);
+      if (!ok) mbar_wait_drain(&bars->a_done, 0);
+    } else if (warp == 3 && lane == 0) {
+      // ============================================ issuer B: dV, dK, dQ
+      const uint32_t id_ts = idesc_bf16_f32(128, 64, false, true);  // dV, dK
+      const uint32_t id_dq = idesc_bf16_f32(128, 64, true, true);   // dQ
+      const uint32_t q_addr = smem_u32(smem + SM_Q);
+      const uint32_t do_addr = smem_u32(smem + SM_DO);
+      const uint32_t ds_addr = smem_u32(smem + SM_DS);
+      const uint64_t k_mn = sdesc_sw128(smem_u32(smem + SM_K), TILE_BYTES, 1024);
+      const uint64_t ds_mn = sdesc_sw128(ds_addr, TILE_BYTES, 1024);  // LBO: next 64-query half
+      bool ok = true;
+      for (int n = 0; n < nsteps; ++n) {
+        const int st = n % NSTAGE;
+        const uint64_t q_mn = sdesc_sw128(q_addr + st * TILE_BYTES, TILE_BYTES, 1024);
+        const uint64_t do_mn = sdesc_sw128(do_addr + st * TILE_BYTES, TILE_BYTES, 1024);
         if (!mbar_wait(&bars->ds_ready, n & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
         GQA_TRACE_EVENT(1, 4, n);
         tc_fence_after_sync();
-        // P^T / dS^T: queries 0-63 in packed columns 0-31, queries 64-127 in 64-95
+        // dV += P^T dO: P^T from TMEM (16 queries = 8 packed columns per step)
+#pragma unroll
+        for (int ks = 0; ks < BQ / 16; ++ks)
+          mma_bf16_ts(tbase + C_DV, tbase + C_PT + ks * 8, do_mn + ks * 128, id_ts, (n > 0 || ks > 0));
+        // dK += dS^T Q: dS^T is the shared dS tile read K-major (queries 0-63 in
+        // the first 16 KB half, 64-127 in the second; 32 B per 16 queries)
 #pragma unroll
         for (int ks = 0; ks < BQ / 16; ++ks) {
-          const uint32_t acol = (ks < 4 ? ks * 8 : 64 + (ks - 4) * 8);
-          mma_bf16_ts(tbase + C_DV, tbase + C_S + acol, do_mn + ks * 128, id_ts, (n > 0 || ks > 0));
+          const uint64_t a = sdesc_sw128(ds_addr + (ks >> 2) * TILE_BYTES + (ks & 3) * 32, 16, 1024);
+          mma_bf16_ss(tbase + C_DK, a, q_mn + ks * 128, id_ts, (n > 0 || ks > 0));
         }
-#pragma unroll
-        for (int ks = 0; ks < BQ / 16; ++ks) {
-          const uint32_t acol = (ks < 4 ? ks * 8 : 64 + (ks - 4) * 8);
-          mma_bf16_ts(tbase + C_DK, tbase + C_DP + acol, q_mn + ks * 128, id_ts, (n > 0 || ks > 0));
-        }
-        const int buf = n & 1;
+        mma_commit(&bars->qdo_empty[st]);
+        if (n > 0 && !mbar_wait(&bars->dq_free, (n - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
         GQA_TRACE_EVENT(1, 5, n);
-        if (!mbar_wait(&bars->dq_free[buf], ((n >> 1) & 1) ^ 1, ab, p.status, kTimeoutCode)) {
-          ok = false;
-          break;
-        }
-        GQA_TRACE_EVENT(1, 6, n);
         tc_fence_after_sync();
 #pragma unroll
         for (int ks = 0; ks < BK / 16; ++ks)  // 16 keys = 2048 B of the MN-major operands
-          mma_bf16_ss(tbase + C_DQ + 64 * buf, ds_mn + ks * 128, k_mn + ks * 128, id_dq, ks > 0);
-        mma_commit(&bars->dq_full[buf]);
-        mma_commit(&bars->qdo_empty[st]);
-        GQA_TRACE_EVENT(1, 7, n);
+          mma_bf16_ss(tbase + C_DQ, ds_mn + ks * 128, k_mn + ks * 128, id_dq, ks > 0);
+        mma_commit(&bars->dq_full);
+        mma_commit(&bars->pds_free);
+        GQA_TRACE_EVENT(1, 6, n);
       }
       mma_commit(&bars->dkv_done);
       if (!ok) mbar_wait_drain(&bars->dkv_done, 0);
     }
-  } else if (warp >= 4 && warp < 12) {
+  } else if (warp < 12) {
+    setmaxnreg_inc<kRegsSoftmax>();
     // ============================================================ P / dS
     const int wg = (warp - 4) >> 2;         // query columns 64*wg .. 64*wg+63
     const int lane_base = 32 * (warp & 3);
@@ -376,6 +451,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const float sl2 = p.scale_log2;
     const bool win = p.causal && p.window > 0;
     const uint32_t lane_off = static_cast<uint32_t>(lane_base) << 16;
+    uint8_t *ds_row = smem + SM_DS + wg * TILE_BYTES + r * 128;
     bool ok = true;
     for (int n = 0; n < nsteps; ++n) {
       const int st = n % NSTAGE;
@@ -387,76 +463,50 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 8, n);
       tc_fence_after_sync();
       const bool masked = pair_needs_mask(qb, kb, p);
-#pragma unroll
-      for (int chunk = 0; chunk < 2; ++chunk) {
-        const int cb = 64 * wg + 32 * chunk;  // first query column of the chunk
+      uint32_t pp0[16], pd0[16], pp1[16], pd1[16];
+      {
         uint32_t sr[32], dr[32];
-        tmem_ld_32x32b_x32(tbase + lane_off + C_S + cb, sr);
-        tmem_ld_32x32b_x32(tbase + lane_off + C_DP + cb, dr);
+        tmem_ld_32x32b_x32(tbase + lane_off + C_S + 64 * wg, sr);
+        tmem_ld_32x32b_x32(tbase + lane_off + C_DP + 64 * wg, dr);
         tmem_wait_ld();
         reg_fence(sr);
         reg_fence(dr);
-        if (chunk == 0 && warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 9, n);
-        if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 16 + 4 * chunk, n);
-        // P and dS in sub-chunks of 8 query columns: the 8 LSE2 and 8 D values of a
-        // sub-chunk are two broadcast 16-byte shared loads each, so few values
-        // are live at once.
-        uint32_t pp[16], pd[16];
+        p_ds_chunk(sr, dr, lse2, dlt, 64 * wg, i0, j, masked, win, sl2, p, pp0, pd0);
+      }
+      {
+        uint32_t sr[32], dr[32];
+        tmem_ld_32x32b_x32(tbase + lane_off + C_S + 64 * wg + 32, sr);
+        tmem_ld_32x32b_x32(tbase + lane_off + C_DP + 64 * wg + 32, dr);
+        tmem_wait_ld();
+        reg_fence(sr);
+        reg_fence(dr);
+        // S^T and dP^T of this step are in registers: the next step's may overwrite them
+        tc_fence_before_sync();
+        mbar_arrive(&bars->st_free);
+        if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 9, n);
+        p_ds_chunk(sr, dr, lse2, dlt, 64 * wg + 32, i0, j, masked, win, sl2, p, pp1, pd1);
+      }
+      // the previous step's dV, dK, dQ must be done with P^T and dS
+      if (n > 0) {
+        if (!mbar_wait(&bars->pds_free, (n - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        tc_fence_after_sync();
+      }
+      if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 10, n);
+      // P^T: this group's 64 queries are packed columns 32*wg .. 32*wg+31
+      tmem_st_32x32b_x16(tbase + lane_off + C_PT + 32 * wg, pp0);
+      tmem_st_32x32b_x16(tbase + lane_off + C_PT + 32 * wg + 16, pp1);
+      // dS: half wg of the tile, key row r, chunk c of 8 queries at (c ^ (r & 7))
 #pragma unroll
-        for (int sc = 0; sc < 4; ++sc) {
-          const float4 la = reinterpret_cast<const float4 *>(lse2 + cb)[2 * sc];
-          const float4 lb = reinterpret_cast<const float4 *>(lse2 + cb)[2 * sc + 1];
-          const float4 da = reinterpret_cast<const float4 *>(dlt + cb)[2 * sc];
-          const float4 db = reinterpret_cast<const float4 *>(dlt + cb)[2 * sc + 1];
-          const float l8[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
-          const float d8[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
-          float pv[8], dv[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int c = 8 * sc + e;
-            pv[e] = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -l8[e]));
-          }
-          if (masked) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int i = i0 + cb + 8 * sc + e;
-              const bool vis = (i < p.S) && (j < p.S) &&
-                               (!p.causal || (j <= i && (!win || j > i - p.window || j < p.n_sink)));
-              pv[e] = vis ? pv[e] : 0.f;
-            }
-          }
-#pragma unroll
-          for (int e = 0; e < 8; ++e) dv[e] = pv[e] * (__uint_as_float(dr[8 * sc + e]) - d8[e]);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            pp[4 * sc + e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
-            pd[4 * sc + e] = pack_bf16x2(dv[2 * e], dv[2 * e + 1]);
-          }
-        }
-        if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 17 + 4 * chunk, n);
-        // packed columns: this group's 64 queries -> columns 64*wg + 16*chunk .. +15
-        tmem_st_32x32b_x16(tbase + lane_off + C_S + 64 * wg + 16 * chunk, pp);
-        tmem_st_32x32b_x16(tbase + lane_off + C_DP + 64 * wg + 16 * chunk, pd);
-        if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 18 + 4 * chunk, n);
-        // dS for dQ = dS K: half wg of the MN-major A operand, key row r, chunks of
-        // 8 queries at (chunk ^ (r & 7)) inside the 128-byte row
-        uint8_t *ds_row = smem + SM_DS + wg * TILE_BYTES + r * 128;
-#pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8) {
-          const int cch = 4 * chunk + q8;
-          uint4 w;
-          w.x = pd[4 * q8 + 0];
-          w.y = pd[4 * q8 + 1];
-          w.z = pd[4 * q8 + 2];
-          w.w = pd[4 * q8 + 3];
-          *reinterpret_cast<uint4 *>(ds_row + ((cch ^ (r & 7)) << 4)) = w;
-        }
-        if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 19 + 4 * chunk, n);
+      for (int q8 = 0; q8 < 4; ++q8) {
+        *reinterpret_cast<uint4 *>(ds_row + ((q8 ^ (r & 7)) << 4)) =
+            make_uint4(pd0[4 * q8], pd0[4 * q8 + 1], pd0[4 * q8 + 2], pd0[4 * q8 + 3]);
+        *reinterpret_cast<uint4 *>(ds_row + (((4 + q8) ^ (r & 7)) << 4)) =
+            make_uint4(pd1[4 * q8], pd1[4 * q8 + 1], pd1[4 * q8 + 2], pd1[4 * q8 + 3]);
       }
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before_sync();
-      if (lane == 0 && (warp == 4 || warp == 8)) GQA_TRACE_EVENT(1, warp == 4 ? 10 : 11, n);
+      if (lane == 0 && (warp == 4 || warp == 8)) GQA_TRACE_EVENT(1, warp == 4 ? 11 : 7, n);
       mbar_arrive(&bars->ds_ready);
     }
     // epilogue: group 0 writes dV, group 1 writes dK (x scale), one key row per thread
@@ -494,33 +544,33 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
     }
-  } else if (warp >= 12) {
+  } else {
+    setmaxnreg_dec<kRegsDrain>();
     // ============================================================ dQ drain
     const int lane_base = 32 * (warp & 3);
     const int r = lane_base + lane;  // query row of the tile
     const uint32_t lane_off = static_cast<uint32_t>(lane_base) << 16;
     const bool leader = (warp == 12 && lane == 0);
+    uint8_t *stg = smem + SM_DQ + r * 128;
     for (int n = 0; n < nsteps; ++n) {
-      const int buf = n & 1;
       const int h = g * p.R + n / nqt;
       const int qb = qlo + n % nqt;
-      if (!mbar_wait(&bars->dq_full[buf], (n >> 1) & 1, ab, p.status, kTimeoutCode)) break;
+      if (!mbar_wait(&bars->dq_full, n & 1, ab, p.status, kTimeoutCode)) break;
       if (leader) GQA_TRACE_EVENT(1, 12, n);
       tc_fence_after_sync();
       uint32_t a0[32], a1[32];
-      tmem_ld_32x32b_x32(tbase + lane_off + C_DQ + 64 * buf, a0);
-      tmem_ld_32x32b_x32(tbase + lane_off + C_DQ + 64 * buf + 32, a1);
+      tmem_ld_32x32b_x32(tbase + lane_off + C_DQ, a0);
+      tmem_ld_32x32b_x32(tbase + lane_off + C_DQ + 32, a1);
       tmem_wait_ld();
       reg_fence(a0);
       reg_fence(a1);
       tc_fence_before_sync();
-      mbar_arrive(&bars->dq_free[buf]);
-      // staging buffer `buf` was last read by the reduce issued two steps ago
-      if (leader) bulk_wait_group_read<1>();
+      mbar_arrive(&bars->dq_free);
+      // the staging buffer was last read by the previous step's reduce
+      if (leader) bulk_wait_group_read<0>();
       if (leader) GQA_TRACE_EVENT(1, 13, n);
       named_bar_sync(1, 128);
       // two boxes [128 rows][32 fp32], 128-byte swizzle: 16-B chunk c of row r at c ^ (r & 7)
-      uint8_t *stg = smem + SM_DQ + buf * 2 * TILE_BYTES + r * 128;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         *reinterpret_cast<uint4 *>(stg + ((c ^ (r & 7)) << 4)) =
@@ -532,7 +582,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       named_bar_sync(1, 128);
       if (leader) {
         const int bh = b * p.H + h;
-        uint8_t *box = smem + SM_DQ + buf * 2 * TILE_BYTES;
+        uint8_t *box = smem + SM_DQ;
         tma_reduce_add_3d(&tm_dq, box, 0, qb * BQ, bh);
         tma_reduce_add_3d(&tm_dq, box + TILE_BYTES, 32, qb * BQ, bh);
         bulk_commit_group();
@@ -554,10 +604,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // ------------------------------------------------------------------- host
 
 inline int configure_kernels() {
-  return cudaFuncSetAttribute(bwd_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              SMEM_BYTES) == cudaSuccess
-             ? 0
-             : -1;
+  if (cudaFuncSetAttribute(bwd_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           SMEM_BYTES) != cudaSuccess)
+    return -1;
+  // the main kernel rebalances registers between warpgroups (setmaxnreg); that
+  // is only safe when the compiled launch allocation covers the split
+  cudaFuncAttributes fa{};
+  if (cudaFuncGetAttributes(&fa, bwd_main_kernel) != cudaSuccess || fa.numRegs < kMinLaunchRegs)
+    return -1;
+  return 0;
 }
 
 inline int encode_3d(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap *map,
