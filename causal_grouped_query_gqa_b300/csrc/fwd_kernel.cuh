@@ -363,6 +363,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const float m_use = (m_new == -CUDART_INF_F) ? 0.f : m_new;
         const float alpha = need ? ex2_approx(m_run - m_use) : 1.f;
         const uint64_t negm = f32x2(-m_use, -m_use);
+        if (lane == 0 && warp == 4) GQA_TRACE_EVENT(0, 16, it);
         // Ping-pong: the two heads take turns on the exp2 section (MUFU-bound), so
         // each runs at the full MUFU rate while the other head's products keep
         // the tensor pipe busy.  Head 0 goes first in every tile.
@@ -371,6 +372,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const uint32_t par = t == 0 ? ((it - 1) & 1) : (it & 1);
           if (wait_turn && !mbar_wait(&bars->turn[t], par, ab, p.status, kTimeoutCode)) { ok = false; break; }
         }
+        if (lane == 0 && warp == 4) GQA_TRACE_EVENT(0, 17, it);
         uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};  // four chains of fp32 pairs (0.0f bits)
         uint32_t pk[BN / 2];
 #pragma unroll
@@ -382,6 +384,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           sum2[c2 & 3] = add_f32x2(sum2[c2 & 3], f32x2(e0, e1));
           pk[c2] = pack_bf16x2(e0, e1);
         }
+        if (lane == 0 && warp == 4) GQA_TRACE_EVENT(0, 18, it);
         if (two) mbar_arrive(&bars->turn[1 - t]);
         float sa, sb, sc, sd;
         f32x2_split(add_f32x2(sum2[0], sum2[1]), sa, sb);
