@@ -11,6 +11,8 @@ Low-level calls (same names and argument order as the C header):
     gqa_attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, G, S, d, causal, window,
                  n_sink, scale, workspace, workspace_bytes, stream)
     gqa_attn_bwd_workspace_size(B, H, G, S, d)
+    gqa_attn_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, G, S, d, causal, window,
+                         n_sink, scale, stream)   (fixed library-held scratch, no allocation)
     gqa_attn_strerror(status), gqa_attn_last_device_status(stream)
     gqa_attn_timing_enable(on), gqa_attn_timing_collect(buf)  (per-kernel CUDA-event times)
 Tensor helpers: ``fwd(q, k, v, ...)`` and ``bwd(q, k, v, o, dout, lse, ...)``.
@@ -18,14 +20,16 @@ Tensor helpers: ``fwd(q, k, v, ...)`` and ``bwd(q, k, v, o, dout, lse, ...)``.
 from __future__ import annotations
 
 from ._lib import (GQA_ERR_ALIGN, GQA_ERR_CUDA, GQA_ERR_DEVICE_TIMEOUT, GQA_ERR_HEADDIM,
-                   GQA_ERR_MASK, GQA_ERR_NULL, GQA_ERR_SCALE, GQA_ERR_SHAPE,
-                   GQA_ERR_WORKSPACE, GQA_OK, GqaError, bwd, fwd, gqa_attn_bwd,
+                   GQA_ERR_MASK, GQA_ERR_NULL, GQA_ERR_SCALE, GQA_ERR_SHAPE, GQA_ERR_TOO_LARGE,
+                   GQA_ERR_WORKSPACE, GQA_NOALLOC_SCRATCH_BYTES, GQA_OK, GqaError, bwd, fwd,
+                   gqa_attn_bwd, gqa_attn_bwd_noalloc,
                    gqa_attn_bwd_workspace_size, gqa_attn_fwd, gqa_attn_last_device_status,
                    gqa_attn_strerror, gqa_attn_timing_collect, gqa_attn_timing_enable,
                    lib_path, load_library, timing_buffer)
 
 __all__ = [
-    "fwd", "bwd", "gqa_attn_fwd", "gqa_attn_bwd", "gqa_attn_bwd_workspace_size",
+    "fwd", "bwd", "gqa_attn_fwd", "gqa_attn_bwd", "gqa_attn_bwd_noalloc",
+    "gqa_attn_bwd_workspace_size", "GQA_ERR_TOO_LARGE", "GQA_NOALLOC_SCRATCH_BYTES",
     "gqa_attn_strerror", "gqa_attn_last_device_status", "gqa_attn_timing_enable",
     "gqa_attn_timing_collect", "timing_buffer", "load_library", "lib_path", "GqaError",
     "GQA_OK", "GQA_ERR_NULL", "GQA_ERR_SHAPE", "GQA_ERR_HEADDIM", "GQA_ERR_ALIGN",

@@ -20,6 +20,8 @@ GQA_ERR_SCALE = -6
 GQA_ERR_WORKSPACE = -7
 GQA_ERR_CUDA = -8
 GQA_ERR_DEVICE_TIMEOUT = -9
+GQA_ERR_TOO_LARGE = -10
+GQA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class GqaError(RuntimeError):
@@ -49,6 +51,9 @@ def load_library():
         lib.gqa_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                      i, i, i, i, i, i, i, i, f, vp, sz, vp]
         lib.gqa_attn_bwd.restype = i
+        lib.gqa_attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                             i, i, i, i, i, i, i, i, f, vp]
+        lib.gqa_attn_bwd_noalloc.restype = i
         lib.gqa_attn_bwd_workspace_size.argtypes = [i, i, i, i, i]
         lib.gqa_attn_bwd_workspace_size.restype = sz
         lib.gqa_attn_strerror.argtypes = [i]
@@ -95,6 +100,14 @@ def gqa_attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, G, S, d, causal, windo
                                        _p(dk), _p(dv), B, H, G, S, d, int(causal), int(window),
                                        int(n_sink), float(scale), _p(workspace),
                                        int(workspace_bytes), _stream(stream))
+
+
+def gqa_attn_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, G, S, d, causal, window,
+                         n_sink, scale, stream=None):
+    return load_library().gqa_attn_bwd_noalloc(_p(q), _p(k), _p(v), _p(o), _p(dout), _p(lse),
+                                               _p(dq), _p(dk), _p(dv), B, H, G, S, d, int(causal),
+                                               int(window), int(n_sink), float(scale),
+                                               _stream(stream))
 
 
 def gqa_attn_bwd_workspace_size(B, H, G, S, d):

@@ -102,6 +102,17 @@ int check_common(int B, int H, int G, int S, int d, int causal, int window, int 
   return GQA_OK;
 }
 
+// Scratch of gqa_attn_bwd_noalloc, for callers that cannot allocate: one
+// fixed array per device the library is loaded on.  Host code must not use the
+// symbol as an address; its device address is looked up once per device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[GQA_NOALLOC_SCRATCH_BYTES];
+
+struct NoAllocState {
+  bool ready = false;
+  void *scratch = nullptr;  // device address of g_noalloc_scratch on this device
+};
+NoAllocState g_noalloc[kMaxDevices];
+
 }  // namespace
 
 extern "C" {
@@ -118,6 +129,7 @@ const char *gqa_attn_strerror(int status) {
     case GQA_ERR_WORKSPACE: return "workspace too small";
     case GQA_ERR_CUDA: return "CUDA call or kernel launch failed";
     case GQA_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait";
+    case GQA_ERR_TOO_LARGE: return "problem needs more scratch than gqa_attn_bwd_noalloc holds";
     default: return "unknown status";
   }
 }
@@ -207,6 +219,47 @@ int gqa_attn_bwd(const void *q, const void *k, const void *v, const void *o, con
     if (cudaFreeAsync(ws, st) != cudaSuccess && rc == GQA_OK) rc = GQA_ERR_CUDA;
   }
   return rc;
+}
+
+int gqa_attn_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                         const void *dout, const float *lse, void *dq, void *dk, void *dv, int B,
+                         int H, int G, int S, int d, int causal, int window, int n_sink,
+                         float scale, void *stream) {
+  int rc = check_common(B, H, G, S, d, causal, window, n_sink, scale);
+  if (rc != GQA_OK) return rc;
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return GQA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return GQA_ERR_ALIGN;
+  if (gqa::bwd::workspace_bytes(B, H, S) > GQA_NOALLOC_SCRATCH_BYTES) return GQA_ERR_TOO_LARGE;
+  DeviceState *ds = nullptr;
+  if ((rc = device_state(&ds)) != GQA_OK) return rc;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GQA_ERR_CUDA;
+  void *scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    NoAllocState &na = g_noalloc[dev];
+    if (!na.ready) {
+      // once per device, with that device current
+      if (cudaGetSymbolAddress(&na.scratch, g_noalloc_scratch) != cudaSuccess) return GQA_ERR_CUDA;
+      na.ready = true;
+    }
+    scratch = na.scratch;
+  }
+  gqa::bwd::Problem pr{};
+  pr.B = B;
+  pr.H = H;
+  pr.G = G;
+  pr.S = S;
+  pr.causal = causal ? 1 : 0;
+  pr.window = (causal && window > 0) ? window : 0;
+  pr.n_sink = pr.window > 0 ? n_sink : 0;
+  pr.scale = scale;
+  rc = gqa::bwd::launch(pr, q, k, v, o, dout, lse, dq, dk, dv, scratch, ds->status, ds->sm_count,
+                        g_encode, static_cast<cudaStream_t>(stream));
+  if (rc == -2) return GQA_ERR_SHAPE;
+  return rc == 0 ? GQA_OK : GQA_ERR_CUDA;
 }
 
 int gqa_attn_timing_enable(int on) {

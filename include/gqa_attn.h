@@ -60,7 +60,8 @@ typedef enum {
     GQA_ERR_SCALE = -6,          /* scale not finite or not positive */
     GQA_ERR_WORKSPACE = -7,      /* workspace smaller than gqa_attn_bwd_workspace_size() */
     GQA_ERR_CUDA = -8,           /* a CUDA runtime/driver call or a launch failed */
-    GQA_ERR_DEVICE_TIMEOUT = -9  /* a kernel gave up a bounded wait (device status) */
+    GQA_ERR_DEVICE_TIMEOUT = -9, /* a kernel gave up a bounded wait (device status) */
+    GQA_ERR_TOO_LARGE = -10      /* needs more than the fixed scratch of gqa_attn_bwd_noalloc */
 } gqa_status;
 
 /*
@@ -104,6 +105,37 @@ GQA_API int gqa_attn_bwd(const void *q, const void *k, const void *v, const void
                  int B, int H, int G, int S, int d,
                  int causal, int window, int n_sink, float scale,
                  void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Backward that allocates nothing.  Same computation, arguments and results as
+ * gqa_attn_bwd, without the workspace: its scratch (the fp32 dq accumulator and
+ * the two row arrays) lives in a fixed array of GQA_NOALLOC_SCRATCH_BYTES that
+ * the library keeps in device memory; every GPU that loads the library holds
+ * that array until the process exits.
+ * It is meant for callers that cannot call cudaMalloc (or any allocator) when
+ * they run the backward: code whose stream is being captured into a CUDA graph,
+ * where a fresh allocation cannot be recorded; plug-ins that run inside a host
+ * framework that owns all device memory and hands them no scratch; real-time or
+ * latency-critical paths that must never enter the allocator.  The pages have
+ * no counterpart of this call.
+ *   - A problem whose scratch (gqa_attn_bwd_workspace_size) exceeds
+ *     GQA_NOALLOC_SCRATCH_BYTES is rejected with GQA_ERR_TOO_LARGE before
+ *     anything is launched (64 MiB holds about 250,000 query rows, B*H*S).
+ *   - The first call on a device looks up the device address of the array with
+ *     that device current; make that first call before any stream capture.
+ *   - All calls on a device share the one array, which keeps whatever the last
+ *     call left in it; each call clears what it needs zeroed.  Calls that may
+ *     run at the same time on the GPU (different streams without ordering)
+ *     race on the array and corrupt each other's results.
+ *   - Calls no cudaMalloc, cudaMallocAsync, cudaFree or allocating library
+ *     routine.
+ */
+#define GQA_NOALLOC_SCRATCH_BYTES (64u << 20)
+GQA_API int gqa_attn_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                 const void *dout, const float *lse,
+                 void *dq, void *dk, void *dv,
+                 int B, int H, int G, int S, int d,
+                 int causal, int window, int n_sink, float scale, void *stream);
 
 /* Static text for a gqa_status value (never NULL). */
 GQA_API const char *gqa_attn_strerror(int status);
