@@ -22,7 +22,9 @@
 //            dV  += P^T dO      dK  += dS^T Q           (TMEM, fp32, whole CTA life)
 //            dQ   = dS K        -> fp32 TMA reduce-add into the accumulator
 //          S^T, dP^T of step n+1 are issued as soon as the P/dS warps have read
-//          step n into registers, so those warps overlap step n's dV, dK, dQ.
+//          step n into registers, so those warps overlap step n's dV, dK, dQ;
+//          P^T and dS are handed over separately (dV starts while dS is still
+//          being written) and freed separately (after dV, after dK and dQ).
 //          dK, dV are summed over the group's heads inside the CTA
 //          (deterministic) and written once as bf16;
 //   convert dQ = bf16(scale * accumulator).
@@ -83,8 +85,10 @@ struct Bars {
   uint64_t qdo_empty[NSTAGE];
   uint64_t st_full;   // S^T, dP^T of the step ready (issuer A commit)
   uint64_t st_free;   // S^T, dP^T read into registers (256 P/dS threads)
-  uint64_t ds_ready;  // P^T in TMEM and dS in shared memory (256 P/dS threads)
-  uint64_t pds_free;  // dV, dK, dQ of the step finished (issuer B commit)
+  uint64_t pt_ready;  // P^T stored in TMEM (256 P/dS threads)
+  uint64_t ds_ready;  // dS stored in shared memory (256 P/dS threads)
+  uint64_t pt_free;   // dV of the step finished: P^T may be overwritten (issuer B commit)
+  uint64_t ds_free;   // dK, dQ of the step finished: dS may be overwritten (issuer B commit)
   uint64_t dq_full;   // dQ tile ready (issuer B commit)
   uint64_t dq_free;   // dQ tile read out (128 drain threads)
   uint64_t a_done;    // every product of issuer A finished
@@ -318,8 +322,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     mbar_init(&bars->st_full, 1);
     mbar_init(&bars->st_free, 256);
+    mbar_init(&bars->pt_ready, 256);
     mbar_init(&bars->ds_ready, 256);
-    mbar_init(&bars->pds_free, 1);
+    mbar_init(&bars->pt_free, 1);
+    mbar_init(&bars->ds_free, 1);
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_free, 128);
     mbar_init(&bars->a_done, 1);
@@ -413,13 +419,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int st = n % NSTAGE;
         const uint64_t q_mn = sdesc_sw128(q_addr + st * TILE_BYTES, TILE_BYTES, 1024);
         const uint64_t do_mn = sdesc_sw128(do_addr + st * TILE_BYTES, TILE_BYTES, 1024);
-        if (!mbar_wait(&bars->ds_ready, n & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        if (!mbar_wait(&bars->pt_ready, n & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
         GQA_TRACE_EVENT(1, 4, n);
         tc_fence_after_sync();
         // dV += P^T dO: P^T from TMEM (16 queries = 8 packed columns per step)
 #pragma unroll
         for (int ks = 0; ks < BQ / 16; ++ks)
           mma_bf16_ts(tbase + C_DV, tbase + C_PT + ks * 8, do_mn + ks * 128, id_ts, (n > 0 || ks > 0));
+        mma_commit(&bars->pt_free);
+        if (!mbar_wait(&bars->ds_ready, n & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        tc_fence_after_sync();
         // dK += dS^T Q: dS^T is the shared dS tile read K-major (queries 0-63 in
         // the first 16 KB half, 64-127 in the second; 32 B per 16 queries)
 #pragma unroll
@@ -435,7 +444,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int ks = 0; ks < BK / 16; ++ks)  // 16 keys = 2048 B of the MN-major operands
           mma_bf16_ss(tbase + C_DQ, ds_mn + ks * 128, k_mn + ks * 128, id_dq, ks > 0);
         mma_commit(&bars->dq_full);
-        mma_commit(&bars->pds_free);
+        mma_commit(&bars->ds_free);
         GQA_TRACE_EVENT(1, 6, n);
       }
       mma_commit(&bars->dkv_done);
@@ -486,15 +495,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 9, n);
         p_ds_chunk(sr, dr, lse2, dlt, 64 * wg + 32, i0, j, masked, win, sl2, p, pp1, pd1);
       }
-      // the previous step's dV, dK, dQ must be done with P^T and dS
+      // the previous step's dV must be done with P^T
       if (n > 0) {
-        if (!mbar_wait(&bars->pds_free, (n - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        if (!mbar_wait(&bars->pt_free, (n - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
         tc_fence_after_sync();
       }
       if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 10, n);
       // P^T: this group's 64 queries are packed columns 32*wg .. 32*wg+31
       tmem_st_32x32b_x16(tbase + lane_off + C_PT + 32 * wg, pp0);
       tmem_st_32x32b_x16(tbase + lane_off + C_PT + 32 * wg + 16, pp1);
+      tmem_wait_st();
+      tc_fence_before_sync();
+      mbar_arrive(&bars->pt_ready);
+      // the previous step's dK and dQ must be done with dS
+      if (n > 0 && !mbar_wait(&bars->ds_free, (n - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
       // dS: half wg of the tile, key row r, chunk c of 8 queries at (c ^ (r & 7))
 #pragma unroll
       for (int q8 = 0; q8 < 4; ++q8) {
@@ -503,9 +517,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         *reinterpret_cast<uint4 *>(ds_row + (((4 + q8) ^ (r & 7)) << 4)) =
             make_uint4(pd1[4 * q8], pd1[4 * q8 + 1], pd1[4 * q8 + 2], pd1[4 * q8 + 3]);
       }
-      tmem_wait_st();
       fence_proxy_async_smem();
-      tc_fence_before_sync();
       if (lane == 0 && (warp == 4 || warp == 8)) GQA_TRACE_EVENT(1, warp == 4 ? 11 : 7, n);
       mbar_arrive(&bars->ds_ready);
     }

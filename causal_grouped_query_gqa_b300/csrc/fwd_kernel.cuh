@@ -268,9 +268,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (it + 1 < n) {
           const int st2 = (it + 1) % NSTAGE;
           if (!mbar_wait(&bars->kv_full[st2], ((it + 1) / NSTAGE) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+          if (t == 0) GQA_TRACE_EVENT(0, 19, it);
           if (!mbar_wait(&bars->s_free[t], pp, ab, p.status, kTimeoutCode)) { ok = false; break; }
+          if (t == 0) GQA_TRACE_EVENT(0, 20, it);
           tc_fence_after_sync();
           issue_qk(st2);
+          if (t == 0) GQA_TRACE_EVENT(0, 21, it);
         }
         if (!mbar_wait(&bars->p_full[t], pp, ab, p.status, kTimeoutCode)) { ok = false; break; }
         if (t == 0) GQA_TRACE_EVENT(0, 2, it); else GQA_TRACE_EVENT(0, 4, it);
