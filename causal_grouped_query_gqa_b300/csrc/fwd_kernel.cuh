@@ -15,21 +15,23 @@
 // Roles (384 threads):
 //   warp 0        TMA producer: Q tiles once, then K and V tiles through an
 //                 NSTAGE-deep shared-memory ring (full/empty mbarriers).
-//   warps 1, 3    MMA issuers, one thread per query head t: S_t = Q_t K^T into
-//                 TMEM, then O_t += P_t V with P_t read from TMEM (A operand in
-//                 TMEM).  Two issuing threads keep the tensor pipe fed while
-//                 either one waits on a barrier (an mbarrier wait costs about as
-//                 much as two MMAs, and the tensor queue is only a few deep).
-//   warp 2        allocates / frees the 512 TMEM columns.
+//   warp 2        allocates / frees the 512 TMEM columns; its lane 0 issues
+//                 S_t = Q_t K^T into TMEM for both heads.
+//   warps 1, 3    one thread each issues O_t += P_t V for query head t, with
+//                 P_t read from TMEM (A operand in TMEM).
+//                 Three issuing threads keep the tensor pipe fed while any of
+//                 them waits on a barrier (an mbarrier wait costs about as much
+//                 as two MMAs, and the tensor queue is only a few deep), and the
+//                 next tile's S never waits behind this tile's P.V in program
+//                 order.
 //   warps 4..7    softmax + O correction + epilogue of head 0 (one row per thread)
 //   warps 8..11   the same for head 1
 // TMEM columns: S0 [0,128) S1 [128,256) O0 [256,320) O1 [320,384)
 //               P0 [384,448) P1 [448,512) (bf16 pairs).
 // Because P has its own columns, S_t(j+1) = Q_t K_{j+1}^T is issued as soon as
 // the softmax of head t has read S_t(j) into registers; only the P store and
-// the O correction wait for P_t V_j to finish.  Each head's issuer runs
-//   QK_t(j+1) PV_t(j) QK_t(j+2) PV_t(j+1) ...
-// and each head's softmax of tile j+1 overlaps the other head's products.
+// the O correction wait for P_t V_j to finish, and each head's softmax of
+// tile j+1 overlaps the other head's products.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -76,6 +78,7 @@ struct Bars {
   uint64_t p_full[2];  // P_t stored and O_t corrected (128 softmax threads)
   uint64_t o_done[2];  // P_t V finished (MMA commit)
   uint64_t o_full[2];  // every product of head t finished (MMA commit)
+  uint64_t qk_done;    // every S product finished (QK issuer commit, abort drain)
   uint64_t turn[2];    // ping-pong of the exp2 sections: turn[t] opens head t's
                        // section (arrived by the other head's 128 threads)
   uint32_t tmem_base;
@@ -175,7 +178,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(&bars->q_full, 1);
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], two ? 2 : 1);
+      mbar_init(&bars->kv_empty[s], two ? 3 : 2);  // the QK issuer and one P.V issuer per head
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
@@ -185,6 +188,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&bars->o_full[t], 1);
       mbar_init(&bars->turn[t], 128);
     }
+    mbar_init(&bars->qk_done, 1);
     bars->abort.flag = 0;
     fence_mbar_init();
   }
@@ -231,57 +235,56 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int it = max(0, issued - NSTAGE); it < issued; ++it)
         mbar_wait_drain(&bars->kv_full[it % NSTAGE], (it / NSTAGE) & 1);
     }
-  } else if ((warp == 1 || warp == 3) && lane == 0 && (warp == 1 || two)) {
-    // ================================================================ MMA issuers
-    const int t = warp == 1 ? 0 : 1;  // the query head this thread serves
+  } else if (warp == 2 && lane == 0) {
+    // ================================================================ QK issuer
     const uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false, false);
-    const uint32_t idesc_pv = idesc_bf16_f32(BM, HD, false, true);
-    const uint32_t q_addr = smem_u32(smem + SM_Q + t * TILE_BYTES);
+    const uint32_t q_addr0 = smem_u32(smem + SM_Q);
     const uint32_t k_addr0 = smem_u32(smem + SM_K);
-    const uint32_t v_addr0 = smem_u32(smem + SM_V);
-    const uint32_t d_s = tbase + col_s(t), d_o = tbase + col_o(t), a_p = tbase + col_p(t);
-
-    auto issue_qk = [&](int st) {
-      const uint64_t ad = sdesc_sw128(q_addr, 16, 1024);
+    auto issue_qk = [&](int t, int st) {
+      const uint64_t ad = sdesc_sw128(q_addr0 + t * TILE_BYTES, 16, 1024);
       const uint64_t bd = sdesc_sw128(k_addr0 + st * TILE_BYTES, 16, 1024);
 #pragma unroll
       for (int ks = 0; ks < HD / 16; ++ks)  // K step 16 bf16 = 32 B inside the 128-B row
-        mma_bf16_ss(d_s, ad + 2 * ks, bd + 2 * ks, idesc_qk, ks > 0);
+        mma_bf16_ss(tbase + col_s(t), ad + 2 * ks, bd + 2 * ks, idesc_qk, ks > 0);
       mma_commit(&bars->s_full[t]);
     };
-    auto issue_pv = [&](int st, bool acc) {
+    bool ok = mbar_wait(&bars->q_full, 0, ab, p.status, kTimeoutCode);
+    for (int it = 0; ok && it < n; ++it) {
+      const int st = it % NSTAGE;
+      if (!mbar_wait(&bars->kv_full[st], (it / NSTAGE) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+      for (int t = 0; t < (two ? 2 : 1); ++t) {
+        // the softmax must have read S_t of the previous tile
+        if (it > 0 && !mbar_wait(&bars->s_free[t], (it - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        tc_fence_after_sync();
+        issue_qk(t, st);
+      }
+      if (!ok) break;
+      GQA_TRACE_EVENT(0, 21, it);
+      mma_commit(&bars->kv_empty[st]);  // K_it read
+    }
+    mma_commit(&bars->qk_done);
+    if (!ok) mbar_wait_drain(&bars->qk_done, 0);
+  } else if ((warp == 1 || warp == 3) && lane == 0 && (warp == 1 || two)) {
+    // ================================================================ P.V issuers
+    const int t = warp == 1 ? 0 : 1;  // the query head this thread serves
+    const uint32_t idesc_pv = idesc_bf16_f32(BM, HD, false, true);
+    const uint32_t v_addr0 = smem_u32(smem + SM_V);
+    const uint32_t d_o = tbase + col_o(t), a_p = tbase + col_p(t);
+    bool ok = true;
+    for (int it = 0; it < n; ++it) {
+      const int st = it % NSTAGE;
+      // V_it landed (the softmax of tile it has started, so its K did too)
+      if (!mbar_wait(&bars->kv_full[st], (it / NSTAGE) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+      if (!mbar_wait(&bars->p_full[t], it & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+      if (t == 0) GQA_TRACE_EVENT(0, 2, it); else GQA_TRACE_EVENT(0, 4, it);
+      tc_fence_after_sync();
       const uint64_t bd = sdesc_sw128(v_addr0 + st * TILE_BYTES, TILE_BYTES, 1024);
 #pragma unroll
       for (int ks = 0; ks < BN / 16; ++ks)  // 16 keys = two 8-row groups = 2048 B
-        mma_bf16_ts(d_o, a_p + ks * 8, bd + (ks * 2048 >> 4), idesc_pv, (acc || ks > 0) ? 1u : 0u);
+        mma_bf16_ts(d_o, a_p + ks * 8, bd + (ks * 2048 >> 4), idesc_pv, (it > 0 || ks > 0) ? 1u : 0u);
       mma_commit(&bars->o_done[t]);
-    };
-
-    bool ok = mbar_wait(&bars->q_full, 0, ab, p.status, kTimeoutCode);
-    ok = ok && mbar_wait(&bars->kv_full[0], 0, ab, p.status, kTimeoutCode);
-    if (ok) {
-      tc_fence_after_sync();
-      issue_qk(0);
-      for (int it = 0; it < n; ++it) {
-        const int st = it % NSTAGE;
-        const uint32_t pp = it & 1;
-        if (it + 1 < n) {
-          const int st2 = (it + 1) % NSTAGE;
-          if (!mbar_wait(&bars->kv_full[st2], ((it + 1) / NSTAGE) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
-          if (t == 0) GQA_TRACE_EVENT(0, 19, it);
-          if (!mbar_wait(&bars->s_free[t], pp, ab, p.status, kTimeoutCode)) { ok = false; break; }
-          if (t == 0) GQA_TRACE_EVENT(0, 20, it);
-          tc_fence_after_sync();
-          issue_qk(st2);
-          if (t == 0) GQA_TRACE_EVENT(0, 21, it);
-        }
-        if (!mbar_wait(&bars->p_full[t], pp, ab, p.status, kTimeoutCode)) { ok = false; break; }
-        if (t == 0) GQA_TRACE_EVENT(0, 2, it); else GQA_TRACE_EVENT(0, 4, it);
-        tc_fence_after_sync();
-        issue_pv(st, it > 0);
-        mma_commit(&bars->kv_empty[st]);  // this head is done with K_it (earlier) and V_it
-        if (t == 0) GQA_TRACE_EVENT(0, 3, it); else GQA_TRACE_EVENT(0, 5, it);
-      }
+      mma_commit(&bars->kv_empty[st]);  // V_it read by this head
+      if (t == 0) GQA_TRACE_EVENT(0, 3, it); else GQA_TRACE_EVENT(0, 5, it);
     }
     // Final commit: on the normal path it releases this head's epilogue; on
     // the abort path it lets this thread wait until its products are done
