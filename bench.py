@@ -248,7 +248,7 @@ def run_ours(args, w, rank, world, local_rank):
 
     fwd_f, bwd_f = step_flops(w, with_bwd)
     flops_step = fwd_f + bwd_f
-    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_throughput(flops_step, args.steps, total_ms, world)
     peaks = measured_peaks()
 
     # ---- dominant kernel roofline
@@ -339,7 +339,7 @@ def run_e2e(args, dev, stream, with_bwd, dev_in, dev_out, host, step, world, flo
     b.record(stream)
     torch.cuda.synchronize()
     ms = _max_over_ranks(a.elapsed_time(b), world)
-    val = world * flops_step * n / (ms * 1e-3) / 1e12
+    val = job_throughput(flops_step, n, ms, world)
     return {"value": round(val, 2), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(ms / n, 4)}
 
@@ -443,6 +443,7 @@ def _barrier(world):
 
 
 def _max_over_ranks(x: float, world: int) -> float:
+    """Slowest rank's time: the job's time (timing reduction only, no data path)."""
     if world <= 1:
         return x
     import torch
@@ -451,6 +452,11 @@ def _max_over_ranks(x: float, world: int) -> float:
     t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(flops_per_rank_step: float, steps: int, max_ms: float, world: int) -> float:
+    """Whole-job TFLOPS: the work of every rank divided by the slowest rank's time."""
+    return world * flops_per_rank_step * steps / (max_ms * 1e-3) / 1e12
 
 
 DEFAULT_WORKLOAD = "wide_b1_h128_g16_s8192"
