@@ -27,7 +27,12 @@ GQA_NOALLOC_SCRATCH_BYTES = 64 << 20
 class GqaError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
-        super().__init__(f"{what}: {gqa_attn_strerror(status)} (status {status})")
+        msg = f"{what}: {gqa_attn_strerror(status)} (status {status})"
+        if status == GQA_ERR_CUDA:
+            detail = gqa_attn_last_error_detail()
+            if detail:
+                msg += f" -- {detail}"
+        super().__init__(msg)
 
 
 def lib_path() -> str:
@@ -58,6 +63,8 @@ def load_library():
         lib.gqa_attn_bwd_workspace_size.restype = sz
         lib.gqa_attn_strerror.argtypes = [i]
         lib.gqa_attn_strerror.restype = ctypes.c_char_p
+        lib.gqa_attn_last_error_detail.argtypes = []
+        lib.gqa_attn_last_error_detail.restype = ctypes.c_char_p
         lib.gqa_attn_last_device_status.argtypes = [vp]
         lib.gqa_attn_last_device_status.restype = i
         lib.gqa_attn_timing_enable.argtypes = [i]
@@ -116,6 +123,10 @@ def gqa_attn_bwd_workspace_size(B, H, G, S, d):
 
 def gqa_attn_strerror(status: int) -> str:
     return load_library().gqa_attn_strerror(int(status)).decode()
+
+
+def gqa_attn_last_error_detail() -> str:
+    return load_library().gqa_attn_last_error_detail().decode()
 
 
 def gqa_attn_last_device_status(stream=None) -> int:

@@ -39,6 +39,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "error_detail.cuh"
 #include "sm100_ptx.cuh"
 #include "timing.cuh"
 #include "trace.cuh"
@@ -235,12 +236,29 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float *__rest
 
 // ------------------------------------------------------------------- main
 
-// P and dS of 32 query columns [cb, cb+32) for this thread's key row j.
+// The n lowest bits set (n clamped to [0, 32]).
+__device__ __forceinline__ uint32_t low_bits(int n) {
+  return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : (1u << n) - 1u);
+}
+
+// Visibility of query columns [cb, cb+32) of the tile for key row j, one bit
+// per column.  For a fixed key the visible queries of a tile form one range
+// [c_lo, c_hi) of columns: causality bounds it below (i >= j), the window
+// above (i < j + window, unless j is a sink), and the sequence end above.
+__device__ __forceinline__ uint32_t visible_bits(int cb, int i0, int j, const MainParams &p) {
+  if (j >= p.S) return 0u;
+  const int c_lo = p.causal ? j - i0 : 0;
+  int c_hi = p.S - i0;
+  if (p.causal && p.window > 0 && j >= p.n_sink) c_hi = min(c_hi, j - i0 + min(p.window, p.S));
+  return low_bits(c_hi - cb) & ~low_bits(c_lo - cb);
+}
+
+// P and dS of 32 query columns [cb, cb+32) for this thread's key row; `vbits`
+// holds their visibility when the tile pair needs the mask.
 __device__ __forceinline__ void p_ds_chunk(const uint32_t (&sr)[32], const uint32_t (&dr)[32],
-                                           const float *lse2, const float *dlt, int cb, int i0,
-                                           int j, bool masked, bool win, float sl2,
-                                           const MainParams &p, uint32_t (&pp)[16],
-                                           uint32_t (&pd)[16]) {
+                                           const float *lse2, const float *dlt, int cb,
+                                           uint32_t vbits, bool masked, float sl2,
+                                           uint32_t (&pp)[16], uint32_t (&pd)[16]) {
   // sub-chunks of 8 query columns: two broadcast 16-byte shared loads for the
   // 8 LSE2 and two for the 8 D values, so few values are live at once
 #pragma unroll
@@ -263,12 +281,7 @@ __device__ __forceinline__ void p_ds_chunk(const uint32_t (&sr)[32], const uint3
     }
     if (masked) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int i = i0 + cb + 8 * sc + e;
-        const bool vis = (i < p.S) && (j < p.S) &&
-                         (!p.causal || (j <= i && (!win || j > i - p.window || j < p.n_sink)));
-        pv[e] = vis ? pv[e] : 0.f;
-      }
+      for (int e = 0; e < 8; ++e) pv[e] = ((vbits >> (8 * sc + e)) & 1u) ? pv[e] : 0.f;
     }
 #pragma unroll
     for (int e = 0; e < 8; e += 2) {
@@ -458,7 +471,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int r = lane_base + lane;         // key row of the tile
     const int j = kb * BK + r;              // key index
     const float sl2 = p.scale_log2;
-    const bool win = p.causal && p.window > 0;
     const uint32_t lane_off = static_cast<uint32_t>(lane_base) << 16;
     uint8_t *ds_row = smem + SM_DS + wg * TILE_BYTES + r * 128;
     bool ok = true;
@@ -480,7 +492,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tmem_wait_ld();
         reg_fence(sr);
         reg_fence(dr);
-        p_ds_chunk(sr, dr, lse2, dlt, 64 * wg, i0, j, masked, win, sl2, p, pp0, pd0);
+        p_ds_chunk(sr, dr, lse2, dlt, 64 * wg, masked ? visible_bits(64 * wg, i0, j, p) : 0u,
+                   masked, sl2, pp0, pd0);
       }
       {
         uint32_t sr[32], dr[32];
@@ -493,7 +506,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_before_sync();
         mbar_arrive(&bars->st_free);
         if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 9, n);
-        p_ds_chunk(sr, dr, lse2, dlt, 64 * wg + 32, i0, j, masked, win, sl2, p, pp1, pd1);
+        p_ds_chunk(sr, dr, lse2, dlt, 64 * wg + 32,
+                   masked ? visible_bits(64 * wg + 32, i0, j, p) : 0u, masked, sl2, pp1, pd1);
       }
       // the previous step's dV must be done with P^T
       if (n > 0) {
@@ -616,14 +630,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // ------------------------------------------------------------------- host
 
 inline int configure_kernels() {
-  if (cudaFuncSetAttribute(bwd_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           SMEM_BYTES) != cudaSuccess)
+  if (cuda_failed(cudaFuncSetAttribute(bwd_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       SMEM_BYTES),
+                  "cudaFuncSetAttribute(backward shared memory)"))
     return -1;
   // the main kernel rebalances registers between warpgroups (setmaxnreg); that
   // is only safe when the compiled launch allocation covers the split
   cudaFuncAttributes fa{};
-  if (cudaFuncGetAttributes(&fa, bwd_main_kernel) != cudaSuccess || fa.numRegs < kMinLaunchRegs)
+  if (cuda_failed(cudaFuncGetAttributes(&fa, bwd_main_kernel), "cudaFuncGetAttributes(backward)"))
     return -1;
+  if (fa.numRegs < kMinLaunchRegs) {
+    set_error_detail("backward kernel compiled with fewer registers than its warpgroup split needs");
+    return -1;
+  }
   return 0;
 }
 
@@ -664,8 +683,10 @@ inline int launch(const Problem &pr, const void *q, const void *k, const void *v
       encode_3d(enc, &tdo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dout, HD, S,
                 static_cast<uint64_t>(B) * H, HD, BQ) ||
       encode_3d(enc, &tdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dq_acc, HD, S,
-                static_cast<uint64_t>(B) * H, 32, BQ))
+                static_cast<uint64_t>(B) * H, 32, BQ)) {
+    set_error_detail("cuTensorMapEncodeTiled rejected a backward tensor map");
     return -8;
+  }
 
   {
     const long long warps_needed = (rows_pad + 3) / 4;
@@ -676,7 +697,7 @@ inline int launch(const Problem &pr, const void *q, const void *k, const void *v
         static_cast<const __nv_bfloat16 *>(o), static_cast<const __nv_bfloat16 *>(dout), lse,
         lse2, delta, dq_acc, rows_pad, S, S_pad);
     timing_end(1, st);
-    if (cudaGetLastError() != cudaSuccess) return -8;
+    if (cuda_failed(cudaGetLastError(), "launch of the backward prep kernel")) return -8;
   }
   {
     MainParams p{};
@@ -703,7 +724,7 @@ inline int launch(const Problem &pr, const void *q, const void *k, const void *v
     bwd_main_kernel<<<static_cast<unsigned>(units), NTHREADS, SMEM_BYTES, st>>>(tq, tk, tv, tdo,
                                                                                tdq, p);
     timing_end(2, st);
-    if (cudaGetLastError() != cudaSuccess) return -8;
+    if (cuda_failed(cudaGetLastError(), "launch of the backward main kernel")) return -8;
   }
   {
     const long long n8 = rows * HD / 8;
@@ -713,7 +734,7 @@ inline int launch(const Problem &pr, const void *q, const void *k, const void *v
     bwd_dq_convert_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
         dq_acc, static_cast<__nv_bfloat16 *>(dq), n8, pr.scale);
     timing_end(3, st);
-    if (cudaGetLastError() != cudaSuccess) return -8;
+    if (cuda_failed(cudaGetLastError(), "launch of the dQ convert kernel")) return -8;
   }
   return 0;
 }

@@ -134,6 +134,11 @@ __device__ __forceinline__ KvRange kv_range(int qb, const Params &p) {
   return r;
 }
 
+// The n lowest bits set (n clamped to [0, 32]).
+__device__ __forceinline__ uint32_t low_bits(int n) {
+  return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : (1u << n) - 1u);
+}
+
 // True when some (row, key) pair of the tile is masked, so the elementwise
 // mask must run.
 __device__ __forceinline__ bool tile_needs_mask(int qb, int kb, const Params &p) {
@@ -343,13 +348,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           s[96 + c] = __uint_as_float(s3[c]);
         }
         if (tile_needs_mask(qb, kb, p)) {
+          // Visibility of the tile's 128 keys as 4 words of bits, from three
+          // bounds (built with a few integer operations per word), then one
+          // bit test and select per score.  A boolean expression per key
+          // compiled to a far slower sequence on this path.
           const int j0 = kb * BN;
+          uint32_t vb[4];
 #pragma unroll
-          for (int c = 0; c < BN; ++c) {
-            const int j = j0 + c;
-            const bool vis = (j <= hi) && (j > lo || j < ns);
-            s[c] = vis ? s[c] : -CUDART_INF_F;
+          for (int w = 0; w < 4; ++w) {
+            const int base = j0 + 32 * w;
+            vb[w] = low_bits(hi - base + 1) & (~low_bits(lo - base + 1) | low_bits(ns - base));
           }
+#pragma unroll
+          for (int c = 0; c < BN; ++c) s[c] = ((vb[c >> 5] >> (c & 31)) & 1u) ? s[c] : -CUDART_INF_F;
         }
         // row max: 4 independent chains of 3-input max over elements 8..127,
         // seeded with elements 0..7

@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "../../include/gqa_attn.h"
+#include "error_detail.cuh"
 #include "timing.cuh"
 #include "trace.cuh"
 #include "bwd_kernels.cuh"
@@ -36,34 +37,51 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 int device_state(DeviceState **out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GQA_ERR_CUDA;
+  if (gqa::cuda_failed(cudaGetDevice(&dev), "cudaGetDevice")) return GQA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) {
+    gqa::set_error_detail("device ordinal beyond the library's per-device table");
+    return GQA_ERR_CUDA;
+  }
   std::lock_guard<std::mutex> lock(g_mutex);
   DeviceState &st = g_dev[dev];
   if (!st.ready) {
     if (!g_encode) {
       void *fn = nullptr;
       cudaDriverEntryPointQueryResult q{};
-      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                           &q) != cudaSuccess ||
-          q != cudaDriverEntryPointSuccess || fn == nullptr)
+      if (gqa::cuda_failed(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                            cudaEnableDefault, &q),
+                           "cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)"))
         return GQA_ERR_CUDA;
+      if (q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        gqa::set_error_detail("the driver does not provide cuTensorMapEncodeTiled");
+        return GQA_ERR_CUDA;
+      }
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
-    if (cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    if (gqa::cuda_failed(cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev),
+                         "cudaDeviceGetAttribute(MultiProcessorCount)"))
       return GQA_ERR_CUDA;
-    if (cudaGetSymbolAddress(reinterpret_cast<void **>(&st.status), g_device_status) != cudaSuccess)
+    if (gqa::cuda_failed(
+            cudaGetSymbolAddress(reinterpret_cast<void **>(&st.status), g_device_status),
+            "cudaGetSymbolAddress(device status word)"))
       return GQA_ERR_CUDA;
-    if (cudaFuncSetAttribute(gqa::fwd::gqa_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             gqa::fwd::SMEM_BYTES) != cudaSuccess)
+    if (gqa::cuda_failed(cudaFuncSetAttribute(gqa::fwd::gqa_fwd_kernel,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              gqa::fwd::SMEM_BYTES),
+                         "cudaFuncSetAttribute(forward shared memory)"))
       return GQA_ERR_CUDA;
     // The forward rebalances registers between warpgroups (setmaxnreg); that is
     // only safe when the compiled launch allocation covers the split.
     cudaFuncAttributes fa{};
-    if (cudaFuncGetAttributes(&fa, gqa::fwd::gqa_fwd_kernel) != cudaSuccess ||
-        fa.numRegs < gqa::fwd::kMinLaunchRegs)
+    if (gqa::cuda_failed(cudaFuncGetAttributes(&fa, gqa::fwd::gqa_fwd_kernel),
+                         "cudaFuncGetAttributes(forward)"))
       return GQA_ERR_CUDA;
+    if (fa.numRegs < gqa::fwd::kMinLaunchRegs) {
+      gqa::set_error_detail("forward kernel compiled with fewer registers than its warpgroup split needs");
+      return GQA_ERR_CUDA;
+    }
     int rc = gqa::bwd::configure_kernels();
-    if (rc != 0) return GQA_ERR_CUDA;
+    if (rc != 0) return GQA_ERR_CUDA;  // detail recorded by configure_kernels
     st.ready = true;
   }
   *out = &st;
@@ -82,7 +100,11 @@ int make_tmap_bf16(CUtensorMap *map, const void *base, uint64_t outer, uint64_t 
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? GQA_OK : GQA_ERR_CUDA;
+  if (r != CUDA_SUCCESS) {
+    gqa::set_error_detail("cuTensorMapEncodeTiled rejected a bf16 tensor map");
+    return GQA_ERR_CUDA;
+  }
+  return GQA_OK;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -174,7 +196,8 @@ int gqa_attn_fwd(const void *q, const void *k, const void *v, void *o, float *ls
   gqa::timing_begin(GQA_KERNEL_FWD, st);
   gqa_fwd_kernel<<<static_cast<unsigned>(units), NTHREADS, SMEM_BYTES, st>>>(tq, tk, tv, p);
   gqa::timing_end(GQA_KERNEL_FWD, st);
-  return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+  return gqa::cuda_failed(cudaGetLastError(), "launch of the forward kernel") ? GQA_ERR_CUDA
+                                                                               : GQA_OK;
 }
 
 size_t gqa_attn_bwd_workspace_size(int B, int H, int G, int S, int d) {
@@ -200,7 +223,8 @@ int gqa_attn_bwd(const void *q, const void *k, const void *v, const void *o, con
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   void *ws = workspace;
   if (!ws) {
-    if (cudaMallocAsync(&ws, need, st) != cudaSuccess) return GQA_ERR_CUDA;
+    if (gqa::cuda_failed(cudaMallocAsync(&ws, need, st), "cudaMallocAsync(backward workspace)"))
+      return GQA_ERR_CUDA;
   }
   gqa::bwd::Problem pr{};
   pr.B = B;
@@ -216,7 +240,9 @@ int gqa_attn_bwd(const void *q, const void *k, const void *v, const void *o, con
   if (rc == -2) rc = GQA_ERR_SHAPE;
   else if (rc != 0) rc = GQA_ERR_CUDA;
   if (!workspace) {
-    if (cudaFreeAsync(ws, st) != cudaSuccess && rc == GQA_OK) rc = GQA_ERR_CUDA;
+    if (gqa::cuda_failed(cudaFreeAsync(ws, st), "cudaFreeAsync(backward workspace)") &&
+        rc == GQA_OK)
+      rc = GQA_ERR_CUDA;
   }
   return rc;
 }
@@ -235,14 +261,16 @@ int gqa_attn_bwd_noalloc(const void *q, const void *k, const void *v, const void
   DeviceState *ds = nullptr;
   if ((rc = device_state(&ds)) != GQA_OK) return rc;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GQA_ERR_CUDA;
+  if (gqa::cuda_failed(cudaGetDevice(&dev), "cudaGetDevice")) return GQA_ERR_CUDA;
   void *scratch = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_mutex);
     NoAllocState &na = g_noalloc[dev];
     if (!na.ready) {
       // once per device, with that device current
-      if (cudaGetSymbolAddress(&na.scratch, g_noalloc_scratch) != cudaSuccess) return GQA_ERR_CUDA;
+      if (gqa::cuda_failed(cudaGetSymbolAddress(&na.scratch, g_noalloc_scratch),
+                           "cudaGetSymbolAddress(static backward scratch)"))
+        return GQA_ERR_CUDA;
       na.ready = true;
     }
     scratch = na.scratch;
@@ -261,6 +289,8 @@ int gqa_attn_bwd_noalloc(const void *q, const void *k, const void *v, const void
   if (rc == -2) return GQA_ERR_SHAPE;
   return rc == 0 ? GQA_OK : GQA_ERR_CUDA;
 }
+
+const char *gqa_attn_last_error_detail(void) { return gqa::error_detail_buffer(); }
 
 int gqa_attn_timing_enable(int on) {
   gqa::TimingState &t = gqa::timing_state();

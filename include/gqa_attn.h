@@ -141,6 +141,16 @@ GQA_API int gqa_attn_bwd_noalloc(const void *q, const void *k, const void *v, co
 GQA_API const char *gqa_attn_strerror(int status);
 
 /*
+ * After a call returned GQA_ERR_CUDA: which CUDA call (or set-up step) failed
+ * and the CUDA runtime's description of the error, e.g.
+ * "launch of the forward kernel: too many resources requested for launch
+ * (cudaErrorLaunchOutOfResources)".  Kept per host thread, overwritten by the
+ * next failure on that thread, never cleared by a success; the pointer stays
+ * valid for the life of the thread.  Empty string if nothing failed yet.
+ */
+GQA_API const char *gqa_attn_last_error_detail(void);
+
+/*
  * Synchronises `stream`, then returns and clears the device status word that
  * kernels set when a bounded wait expires: GQA_OK or GQA_ERR_DEVICE_TIMEOUT
  * (GQA_ERR_CUDA if the synchronisation itself failed).

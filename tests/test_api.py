@@ -115,3 +115,16 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(L, "_LIB_PATH", str(tmp_path / "libgqa_attn.so"))
     with pytest.raises(RuntimeError, match="missing"):
         L.load_library()
+
+
+def test_cuda_failure_names_the_failing_call(lib):
+    """Without a GPU, valid arguments reach the first CUDA call, which fails; the
+    status is GQA_ERR_CUDA and the detail names the call and CUDA's reason."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("needs a host without a usable GPU")
+    assert _fwd() == gq.GQA_ERR_CUDA
+    detail = gq.gqa_attn_last_error_detail()
+    assert detail.startswith("cudaGetDevice: ") and "cudaError" in detail
+    with pytest.raises(gq.GqaError, match="cudaGetDevice"):
+        raise gq.GqaError(gq.GQA_ERR_CUDA, "gqa_attn_fwd")
