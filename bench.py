@@ -184,7 +184,8 @@ def run_ours(args, w, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     gq.load_library()
-    with_bwd = w.backward or args.workload == DEFAULT_WORKLOAD
+    with_bwd = args.step == "fwd+bwd" or (
+        args.step == "auto" and (w.backward or args.workload == DEFAULT_WORKLOAD))
     B, H, G, S, d = w.B, w.H, w.G, w.S, w.d
     kw = dict(causal=w.causal, window=w.window, n_sink=w.n_sink, scale=w.scale)
 
@@ -469,6 +470,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--step", choices=["auto", "fwd", "fwd+bwd"], default="auto",
+                    help="what one step runs; auto: fwd+bwd on the default workload and on "
+                         "workloads stated with a backward, else fwd")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip timing the oracle (profiling runs only)")
     args = ap.parse_args(argv)

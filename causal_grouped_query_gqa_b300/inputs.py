@@ -37,7 +37,8 @@ class Workload:
         return 1.0 / float(self.d) ** 0.5
 
 
-# The five workloads the library is measured and checked on.
+# The workloads the library is measured and checked on: five stated ones, and
+# the model-spec mask (window 65536, 2048 sinks) at its longest context.
 WORKLOADS = {
     "tiny_b1_h4_g2_s128": Workload("tiny_b1_h4_g2_s128", 1, 4, 2, 128, backward=True),
     "gqa_b2_h32_g8_s2048": Workload("gqa_b2_h32_g8_s2048", 2, 32, 8, 2048),
@@ -45,6 +46,9 @@ WORKLOADS = {
     "window_b1_h128_g16_s32768_w4096_sink128": Workload(
         "window_b1_h128_g16_s32768_w4096_sink128", 1, 128, 16, 32768, window=4096, n_sink=128),
     "bwd_b4_h32_g8_s4096": Workload("bwd_b4_h32_g8_s4096", 4, 32, 8, 4096, backward=True),
+    "model_b1_h128_g16_s204800_w65536_sink2048": Workload(
+        "model_b1_h128_g16_s204800_w65536_sink2048", 1, 128, 16, 204800, window=65536,
+        n_sink=2048, backward=True),
 }
 
 

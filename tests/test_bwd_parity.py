@@ -121,6 +121,29 @@ def test_window_bwd_long_context_sampled():
     check_close("dQ", to64(dq[0, 2:4]), rq)
 
 
+def test_model_workload_bwd_tail():
+    """The model-spec mask (window 65536, 2048 sinks) at S = 204800: full
+    forward and backward on the GPU, checked on the last kv group: dQ of the
+    last 512 query rows (their window edge and the sinks are both in play) and
+    dK, dV of the last 512 keys, every visible query of which is among those
+    rows, so the oracle's restricted sums are complete there."""
+    w = WORKLOADS["model_b1_h128_g16_s204800_w65536_sink2048"]
+    q, k, v, do = make_inputs(w.B, w.H, w.G, w.S, seed=0, with_grad=True)
+    kw = dict(window=w.window, n_sink=w.n_sink)
+    dq, dk, dv = _gpu_fwd_bwd(q, k, v, do, **kw)
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t).all()
+    R, g, n = w.H // w.G, w.G - 1, 512
+    i0 = w.S - n
+    heads = slice(g * R, (g + 1) * R)
+    rq, rk, rv = oracle.attn_bwd_group_rows(to64(q[:, heads]), to64(k[:, g:g + 1]),
+                                            to64(v[:, g:g + 1]), to64(do[:, heads]), 0, 0,
+                                            i0, w.S, **kw)
+    check_close("dQ(last rows)", to64(dq[0, heads, i0:]), rq[:, i0:])
+    check_close("dK(last keys)", to64(dk[0, g, i0:]), rk[i0:])
+    check_close("dV(last keys)", to64(dv[0, g, i0:]), rv[i0:])
+
+
 def test_repeat_dk_dv_deterministic():
     q, k, v, do = [t.cuda() for t in make_inputs(1, 8, 2, 700, seed=4, with_grad=True)]
     o, lse = gq.fwd(q, k, v, window=200, n_sink=50)

@@ -65,7 +65,7 @@ def test_gqa_workload_full():
     _run_full(w.B, w.H, w.G, w.S)
 
 
-def _run_sampled(w, n_rows=48):
+def _run_sampled(w, n_rows=48, extra=()):
     """Full-size launch (the benchmark's), checked on sampled rows plus
     properties that hold at any size."""
     q, k, v = make_inputs(w.B, w.H, w.G, w.S, seed=0)
@@ -78,7 +78,7 @@ def _run_sampled(w, n_rows=48):
     R = w.H // w.G
     v_rep = v.cuda().repeat_interleave(R, dim=1)
     assert torch.equal(o[:, :, 0], v_rep[:, :, 0])
-    rows = sample_rows(w.B, w.H, w.S, n_rows, extra=[(0, w.H - 1, w.S - 1)])
+    rows = sample_rows(w.B, w.H, w.S, n_rows, extra=[(0, w.H - 1, w.S - 1), *extra])
     got_o = np.stack([to64(o[b, h, i]) for b, h, i in rows])
     got_l = np.array([float(lse[b, h, i]) for b, h, i in rows])
     ref_o = np.zeros_like(got_o)
@@ -107,6 +107,15 @@ def test_wide_workload_sampled():
 
 def test_window_workload_sampled():
     _run_sampled(WORKLOADS["window_b1_h128_g16_s32768_w4096_sink128"])
+
+
+def test_model_workload_sampled():
+    """The model-spec mask at S = 204800: rows around the window edge (65536)
+    and the sink boundary, plus the sampled ones."""
+    w = WORKLOADS["model_b1_h128_g16_s204800_w65536_sink2048"]
+    edges = [w.n_sink - 1, w.n_sink, w.window - 1, w.window, w.window + 1,
+             w.window + w.n_sink - 1, w.window + w.n_sink, w.S - 1]
+    _run_sampled(w, extra=[(0, (7 * t) % w.H, i) for t, i in enumerate(edges)])
 
 
 def test_repeat_is_deterministic():
