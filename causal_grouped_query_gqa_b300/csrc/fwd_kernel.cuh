@@ -6,24 +6,32 @@
 // head map of test T2; "SnapKitty Transformer 8B": online softmax over K/V
 // tiles, sliding window and attention sinks.)
 //
-// One CTA = one work unit = (batch b, kv head g, 128-row query block qb) x two
-// query heads of g.  Both heads read every K/V tile the CTA loads, so each tile
-// crosses HBM/L2 once per pair of heads.  Only key tiles with at least one
-// visible key are visited (sink tiles, then the window / causal range), and the
-// elementwise mask runs only on tiles that straddle a mask boundary.
+// Work unit = (batch b, kv head g, 128-row query block qb) x two query heads of
+// g.  Both heads read every K/V tile the CTA loads, so each tile crosses
+// HBM/L2 once per pair of heads.  Only key tiles with at least one visible key
+// are visited (sink tiles, then the window / causal range), and the elementwise
+// mask runs only on tiles that straddle a mask boundary.
+//
+// The grid is persistent: one CTA per SM walks the unit list (heaviest query
+// blocks first, in zig-zag rounds of one unit per CTA).  Every barrier phase is
+// counted across units, so the producer loads the next unit's Q and K/V while
+// the current one finishes, each head's next Q K^T starts as soon as its S
+// buffer is free, and its first P.V waits only until the epilogue has read O;
+// the CTA launch, barrier and TMEM set-up and the cold loads are paid once per
+// SM instead of once per unit.
 //
 // Roles (384 threads):
-//   warp 0        TMA producer: Q tiles once, then K and V tiles through an
-//                 NSTAGE-deep shared-memory ring (full/empty mbarriers).
+//   warp 0        TMA producer: each unit's Q tiles, then K and V tiles through
+//                 an NSTAGE-deep shared-memory ring (full/empty mbarriers).
 //   warp 2        allocates / frees the 512 TMEM columns; its lane 0 issues
 //                 S_t = Q_t K^T into TMEM for both heads.
 //   warps 1, 3    one thread each issues O_t += P_t V for query head t, with
 //                 P_t read from TMEM (A operand in TMEM).
 //                 Three issuing threads keep the tensor pipe fed while any of
-//                 them waits on a barrier (an mbarrier wait costs about as much
-//                 as two MMAs, and the tensor queue is only a few deep), and the
-//                 next tile's S never waits behind this tile's P.V in program
-//                 order.
+//                 them waits on a barrier (an mbarrier hand-off costs about as
+//                 much as three MMAs, and the tensor queue is only a few deep),
+//                 and the next tile's S never waits behind this tile's P.V in
+//                 program order.
 //   warps 4..7    softmax + O correction + epilogue of head 0 (one row per thread)
 //   warps 8..11   the same for head 1
 // TMEM columns: S0 [0,128) S1 [128,256) O0 [256,320) O1 [320,384)
@@ -70,15 +78,19 @@ constexpr int SM_V = SM_K + NSTAGE * TILE_BYTES;
 constexpr int SM_BARS = SM_V + NSTAGE * TILE_BYTES;
 
 struct Bars {
-  uint64_t q_full;
+  uint64_t q_full;     // the unit's Q tiles landed (TMA transaction bytes)
+  uint64_t q_empty;    // every Q K^T of the unit finished: Q may be reloaded
   uint64_t kv_full[NSTAGE];   // K and V tile landed (TMA transaction bytes)
-  uint64_t kv_empty[NSTAGE];  // every head's products with the tile finished
+  uint64_t kv_empty[NSTAGE];  // every head's products with the tile finished (the
+                              // QK issuer and both P.V issuers, always 3 arrivals)
   uint64_t s_full[2];  // S_t ready (MMA commit)
   uint64_t s_free[2];  // S_t read into registers (128 softmax threads)
   uint64_t p_full[2];  // P_t stored and O_t corrected (128 softmax threads)
   uint64_t o_done[2];  // P_t V finished (MMA commit)
-  uint64_t o_full[2];  // every product of head t finished (MMA commit)
+  uint64_t o_full[2];  // every product of head t in the unit finished (MMA commit)
+  uint64_t o_empty[2]; // the epilogue read O_t: the next unit may overwrite it (128 threads)
   uint64_t qk_done;    // every S product finished (QK issuer commit, abort drain)
+  uint64_t pv_done[2]; // every P.V product of head t finished (abort drain)
   uint64_t turn[2];    // ping-pong of the exp2 sections: turn[t] opens head t's
                        // section (arrived by the other head's 128 threads)
   uint32_t tmem_base;
@@ -93,6 +105,7 @@ struct Params {
   float scale_log2;  // scale * log2(e): scores are kept in the base-2 domain
   int n_qblocks;
   int n_pairs;  // ceil(R / 2) head pairs per kv head
+  int n_units;  // n_qblocks * B * G * n_pairs
   __nv_bfloat16 *o;
   float *lse;
   int *status;
@@ -154,6 +167,36 @@ __device__ __forceinline__ bool tile_needs_mask(int qb, int kb, const Params &p)
   return false;
 }
 
+// One work unit, heaviest (latest) query blocks first.
+struct Unit {
+  int qb, b, g, h0;
+  bool two;  // both heads of the pair exist (R odd leaves a single last head)
+};
+
+__device__ __forceinline__ Unit unit_of(int u, const Params &p) {
+  const int per_qb = p.B * p.G * p.n_pairs;
+  const int rem = u % per_qb;
+  Unit un;
+  un.qb = p.n_qblocks - 1 - u / per_qb;
+  un.b = rem / (p.G * p.n_pairs);
+  un.g = (rem / p.n_pairs) % p.G;
+  const int pair = rem % p.n_pairs;
+  un.h0 = un.g * p.R + 2 * pair;
+  un.two = (2 * pair + 1) < p.R;
+  return un;
+}
+
+// The k-th unit of this CTA, or -1 when none is left.  Rounds of gridDim.x
+// units alternate direction (CTA c takes unit c of even rounds and unit
+// grid - 1 - c of odd ones): unit sizes shrink along the heaviest-first list,
+// and the zig-zag evens out what a plain stride leaves to the first CTAs.
+__device__ __forceinline__ int unit_at(int k, const Params &p) {
+  const int base = k * static_cast<int>(gridDim.x);
+  if (base >= p.n_units) return -1;
+  const int c = (k & 1) ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
+  return base + c < p.n_units ? base + c : -1;
+}
+
 __global__ void __launch_bounds__(NTHREADS, 1)
     gqa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
@@ -166,24 +209,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- work unit: heaviest (latest) query blocks first
-  const int per_qb = p.B * p.G * p.n_pairs;
-  const int u = blockIdx.x;
-  const int qb = p.n_qblocks - 1 - u / per_qb;
-  const int rem = u % per_qb;
-  const int b = rem / (p.G * p.n_pairs);
-  const int g = (rem / p.n_pairs) % p.G;
-  const int pair = rem % p.n_pairs;
-  const int h0 = g * p.R + 2 * pair;
-  const bool two = (2 * pair + 1) < p.R;
-  const KvRange kr = kv_range(qb, p);
-  const int n = kr.count;
-
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], two ? 3 : 2);  // the QK issuer and one P.V issuer per head
+      mbar_init(&bars->kv_empty[s], 3);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
@@ -191,7 +222,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&bars->p_full[t], 128);
       mbar_init(&bars->o_done[t], 1);
       mbar_init(&bars->o_full[t], 1);
+      mbar_init(&bars->o_empty[t], 128);
       mbar_init(&bars->turn[t], 128);
+      mbar_init(&bars->pv_done[t], 1);
     }
     mbar_init(&bars->qk_done, 1);
     bars->abort.flag = 0;
@@ -216,114 +249,176 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      const int qrow = qb * BM;
-      mbar_arrive_expect_tx(&bars->q_full, (two ? 2 : 1) * TILE_BYTES);
-      tma_load_3d(smem + SM_Q, &tm_q, &bars->q_full, 0, qrow, b * p.H + h0);
-      if (two) tma_load_3d(smem + SM_Q + TILE_BYTES, &tm_q, &bars->q_full, 0, qrow, b * p.H + h0 + 1);
-      const int kvz = b * p.G + g;
-      int issued = 0;
-      for (int it = 0; it < n; ++it) {
-        const int st = it % NSTAGE;
-        const uint32_t ph = (it / NSTAGE) & 1;
-        const int kb = kr.tile(it);
-        if (!mbar_wait(&bars->kv_empty[st], ph ^ 1, ab, p.status, kTimeoutCode)) break;
-        GQA_TRACE_EVENT(0, 0, it);
-        mbar_arrive_expect_tx(&bars->kv_full[st], 2 * TILE_BYTES);
-        tma_load_3d(smem + SM_K + st * TILE_BYTES, &tm_k, &bars->kv_full[st], 0, kb * BN, kvz);
-        tma_load_3d(smem + SM_V + st * TILE_BYTES, &tm_v, &bars->kv_full[st], 0, kb * BN, kvz);
-        GQA_TRACE_EVENT(0, 1, it);
-        issued = it + 1;
+      int gt = 0;       // K/V tiles issued (all units): ring stage and phase
+      int q_loads = 0;  // units whose Q was issued
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int u = unit_at(k, p);
+        if (u < 0) break;
+        const Unit un = unit_of(u, p);
+        const KvRange kr = kv_range(un.qb, p);
+        // the previous unit's Q K^T products must have read Q
+        if (k > 0 && !mbar_wait(&bars->q_empty, (k - 1) & 1, ab, p.status, kTimeoutCode)) break;
+        const int qrow = un.qb * BM, qz = un.b * p.H + un.h0;
+        mbar_arrive_expect_tx(&bars->q_full, (un.two ? 2 : 1) * TILE_BYTES);
+        tma_load_3d(smem + SM_Q, &tm_q, &bars->q_full, 0, qrow, qz);
+        if (un.two) tma_load_3d(smem + SM_Q + TILE_BYTES, &tm_q, &bars->q_full, 0, qrow, qz + 1);
+        q_loads = k + 1;
+        const int kvz = un.b * p.G + un.g;
+        for (int it = 0; it < kr.count; ++it, ++gt) {
+          const int st = gt % NSTAGE;
+          const int kb = kr.tile(it);
+          if (!mbar_wait(&bars->kv_empty[st], ((gt / NSTAGE) & 1) ^ 1, ab, p.status, kTimeoutCode)) {
+            ok = false;
+            break;
+          }
+          GQA_TRACE_EVENT(0, 0, k == 0 ? it : kTraceSteps);
+          mbar_arrive_expect_tx(&bars->kv_full[st], 2 * TILE_BYTES);
+          tma_load_3d(smem + SM_K + st * TILE_BYTES, &tm_k, &bars->kv_full[st], 0, kb * BN, kvz);
+          tma_load_3d(smem + SM_V + st * TILE_BYTES, &tm_v, &bars->kv_full[st], 0, kb * BN, kvz);
+          GQA_TRACE_EVENT(0, 1, k == 0 ? it : kTraceSteps);
+        }
       }
       // Exit drain: every copy this CTA issued must have landed before the CTA
       // leaves (no-op on the normal path, where the consumers already saw them).
-      mbar_wait_drain(&bars->q_full, 0);
-      for (int it = max(0, issued - NSTAGE); it < issued; ++it)
-        mbar_wait_drain(&bars->kv_full[it % NSTAGE], (it / NSTAGE) & 1);
+      if (q_loads > 0) mbar_wait_drain(&bars->q_full, (q_loads - 1) & 1);
+      for (int x = max(0, gt - NSTAGE); x < gt; ++x)
+        mbar_wait_drain(&bars->kv_full[x % NSTAGE], (x / NSTAGE) & 1);
     }
   } else if (warp == 2 && lane == 0) {
     // ================================================================ QK issuer
     const uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false, false);
     const uint32_t q_addr0 = smem_u32(smem + SM_Q);
     const uint32_t k_addr0 = smem_u32(smem + SM_K);
-    auto issue_qk = [&](int t, int st) {
-      const uint64_t ad = sdesc_sw128(q_addr0 + t * TILE_BYTES, 16, 1024);
-      const uint64_t bd = sdesc_sw128(k_addr0 + st * TILE_BYTES, 16, 1024);
+    int gt = 0;             // K/V tiles consumed (all units)
+    int ts[2] = {0, 0};     // S products issued per head (all units)
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int u = unit_at(k, p);
+      if (u < 0) break;
+      const Unit un = unit_of(u, p);
+      const int n = kv_range(un.qb, p).count;
+      if (!mbar_wait(&bars->q_full, k & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+      for (int it = 0; it < n; ++it, ++gt) {
+        const int st = gt % NSTAGE;
+        if (!mbar_wait(&bars->kv_full[st], (gt / NSTAGE) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        for (int t = 0; t < (un.two ? 2 : 1); ++t) {
+          // the softmax must have read S_t of head t's previous tile
+          if (ts[t] > 0 && !mbar_wait(&bars->s_free[t], (ts[t] - 1) & 1, ab, p.status, kTimeoutCode)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint64_t ad = sdesc_sw128(q_addr0 + t * TILE_BYTES, 16, 1024);
+          const uint64_t bd = sdesc_sw128(k_addr0 + st * TILE_BYTES, 16, 1024);
 #pragma unroll
-      for (int ks = 0; ks < HD / 16; ++ks)  // K step 16 bf16 = 32 B inside the 128-B row
-        mma_bf16_ss(tbase + col_s(t), ad + 2 * ks, bd + 2 * ks, idesc_qk, ks > 0);
-      mma_commit(&bars->s_full[t]);
-    };
-    bool ok = mbar_wait(&bars->q_full, 0, ab, p.status, kTimeoutCode);
-    for (int it = 0; ok && it < n; ++it) {
-      const int st = it % NSTAGE;
-      if (!mbar_wait(&bars->kv_full[st], (it / NSTAGE) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
-      for (int t = 0; t < (two ? 2 : 1); ++t) {
-        // the softmax must have read S_t of the previous tile
-        if (it > 0 && !mbar_wait(&bars->s_free[t], (it - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
-        tc_fence_after_sync();
-        issue_qk(t, st);
+          for (int ks = 0; ks < HD / 16; ++ks)  // K step 16 bf16 = 32 B inside the 128-B row
+            mma_bf16_ss(tbase + col_s(t), ad + 2 * ks, bd + 2 * ks, idesc_qk, ks > 0);
+          mma_commit(&bars->s_full[t]);
+          ++ts[t];
+        }
+        if (!ok) break;
+        GQA_TRACE_EVENT(0, 21, k == 0 ? it : kTraceSteps);
+        mma_commit(&bars->kv_empty[st]);  // K read
       }
       if (!ok) break;
-      GQA_TRACE_EVENT(0, 21, it);
-      mma_commit(&bars->kv_empty[st]);  // K_it read
+      mma_commit(&bars->q_empty);  // this unit's Q read
     }
     mma_commit(&bars->qk_done);
     if (!ok) mbar_wait_drain(&bars->qk_done, 0);
-  } else if ((warp == 1 || warp == 3) && lane == 0 && (warp == 1 || two)) {
+  } else if ((warp == 1 || warp == 3) && lane == 0) {
     // ================================================================ P.V issuers
     const int t = warp == 1 ? 0 : 1;  // the query head this thread serves
     const uint32_t idesc_pv = idesc_bf16_f32(BM, HD, false, true);
     const uint32_t v_addr0 = smem_u32(smem + SM_V);
     const uint32_t d_o = tbase + col_o(t), a_p = tbase + col_p(t);
+    int gt = 0;  // K/V tiles seen (all units)
+    int tp = 0;  // P.V products of this head (all units)
+    int uo = 0;  // units of this head whose O was released
     bool ok = true;
-    for (int it = 0; it < n; ++it) {
-      const int st = it % NSTAGE;
-      // V_it landed (the softmax of tile it has started, so its K did too)
-      if (!mbar_wait(&bars->kv_full[st], (it / NSTAGE) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
-      if (!mbar_wait(&bars->p_full[t], it & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
-      if (t == 0) GQA_TRACE_EVENT(0, 2, it); else GQA_TRACE_EVENT(0, 4, it);
-      tc_fence_after_sync();
-      const uint64_t bd = sdesc_sw128(v_addr0 + st * TILE_BYTES, TILE_BYTES, 1024);
+    for (int k = 0; ok; ++k) {
+      const int u = unit_at(k, p);
+      if (u < 0) break;
+      const Unit un = unit_of(u, p);
+      const int n = kv_range(un.qb, p).count;
+      const bool mine = t == 0 || un.two;
+      for (int it = 0; it < n; ++it, ++gt) {
+        const int st = gt % NSTAGE;
+        // V landed (the softmax of the tile has started, so its K did too);
+        // for a single-head unit the absent head still releases the stage,
+        // after it was filled for this use
+        if (!mbar_wait(&bars->kv_full[st], (gt / NSTAGE) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        if (!mine) {
+          mbar_arrive(&bars->kv_empty[st]);
+          continue;
+        }
+        // the previous unit's epilogue must have read O_t before it is overwritten
+        if (it == 0 && uo > 0 && !mbar_wait(&bars->o_empty[t], (uo - 1) & 1, ab, p.status, kTimeoutCode)) {
+          ok = false;
+          break;
+        }
+        if (!mbar_wait(&bars->p_full[t], tp & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        if (t == 0) GQA_TRACE_EVENT(0, 2, k == 0 ? it : kTraceSteps); else GQA_TRACE_EVENT(0, 4, k == 0 ? it : kTraceSteps);
+        tc_fence_after_sync();
+        const uint64_t bd = sdesc_sw128(v_addr0 + st * TILE_BYTES, TILE_BYTES, 1024);
 #pragma unroll
-      for (int ks = 0; ks < BN / 16; ++ks)  // 16 keys = two 8-row groups = 2048 B
-        mma_bf16_ts(d_o, a_p + ks * 8, bd + (ks * 2048 >> 4), idesc_pv, (it > 0 || ks > 0) ? 1u : 0u);
-      mma_commit(&bars->o_done[t]);
-      mma_commit(&bars->kv_empty[st]);  // V_it read by this head
-      if (t == 0) GQA_TRACE_EVENT(0, 3, it); else GQA_TRACE_EVENT(0, 5, it);
+        for (int ks = 0; ks < BN / 16; ++ks)  // 16 keys = two 8-row groups = 2048 B
+          mma_bf16_ts(d_o, a_p + ks * 8, bd + (ks * 2048 >> 4), idesc_pv, (it > 0 || ks > 0) ? 1u : 0u);
+        mma_commit(&bars->o_done[t]);
+        mma_commit(&bars->kv_empty[st]);  // V read by this head
+        ++tp;
+        if (t == 0) GQA_TRACE_EVENT(0, 3, k == 0 ? it : kTraceSteps); else GQA_TRACE_EVENT(0, 5, k == 0 ? it : kTraceSteps);
+      }
+      if (!ok) break;
+      if (mine) {
+        mma_commit(&bars->o_full[t]);  // releases this head's epilogue of the unit
+        ++uo;
+      }
     }
-    // Final commit: on the normal path it releases this head's epilogue; on
-    // the abort path it lets this thread wait until its products are done
-    // before TMEM is freed.
-    mma_commit(&bars->o_full[t]);
-    if (!ok) mbar_wait_drain(&bars->o_full[t], 0);
+    // lets this thread wait, on the abort path, until its products are done
+    // before TMEM is freed
+    mma_commit(&bars->pv_done[t]);
+    if (!ok) mbar_wait_drain(&bars->pv_done[t], 0);
   }
   } else {
     setmaxnreg_inc<kRegsSoftmax>();
     // ================================================================ softmax
     const int t = (warp - 4) >> 2;
-    if (t == 0 || two) {
-      const int lane_base = 32 * (warp & 3);
-      const int r = lane_base + lane;  // row of the tile this thread owns
-      const int i = qb * BM + r;       // query index
-      const float sl2 = p.scale_log2;
+    const int lane_base = 32 * (warp & 3);
+    const int r = lane_base + lane;  // row of the tile this thread owns
+    const float sl2 = p.scale_log2;
+    const uint32_t lane_off = static_cast<uint32_t>(lane_base) << 16;
+    const uint32_t t_s = tbase + lane_off + col_s(t);
+    const uint32_t t_o = tbase + lane_off + col_o(t);
+    const uint32_t t_p = tbase + lane_off + col_p(t);
+    const uint64_t sl2x2 = f32x2(sl2, sl2);
+    int ts = 0;  // tiles of this head (all units): S, P and O-done phases
+    int uo = 0;  // units of this head: O-full / O-empty phases
+    int tt = 0;  // tiles of two-head units: ping-pong phases (same count in both heads)
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int u = unit_at(k, p);
+      if (u < 0) break;
+      const Unit un = unit_of(u, p);
+      if (t == 1 && !un.two) continue;
+      const KvRange kr = kv_range(un.qb, p);
+      const int n = kr.count;
+      const int qb = un.qb;
+      const int i = qb * BM + r;  // query index
       // mask bounds: key j visible iff j <= hi && (j > lo || j < ns)
       const int hi = p.causal ? min(i, p.S - 1) : p.S - 1;
       const bool win = p.causal && p.window > 0;
       const int lo = win ? i - p.window : -1;
       const int ns = win ? p.n_sink : 0;
-      const uint32_t lane_off = static_cast<uint32_t>(lane_base) << 16;
-      const uint32_t t_s = tbase + lane_off + col_s(t);
-      const uint32_t t_o = tbase + lane_off + col_o(t);
-      const uint32_t t_p = tbase + lane_off + col_p(t);
-      const uint64_t sl2x2 = f32x2(sl2, sl2);
 
       float m_run = -CUDART_INF_F;  // running max of scaled scores, base-2 units
       float l_run = 0.f;            // running sum of 2^(s - m_run)
-      bool ok = true;
-      for (int it = 0; it < n; ++it) {
+      for (int it = 0; it < n; ++it, ++ts) {
         const int kb = kr.tile(it);
-        if (!mbar_wait(&bars->s_full[t], it & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
-        if (lane == 0 && (warp == 4 || warp == 8)) GQA_TRACE_EVENT(0, warp == 4 ? 6 : 10, it);
+        const int step = k == 0 ? it : kTraceSteps;  // trace the first unit only
+        (void)step;
+        if (!mbar_wait(&bars->s_full[t], ts & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        if (lane == 0 && (warp == 4 || warp == 8)) GQA_TRACE_EVENT(0, warp == 4 ? 6 : 10, step);
         tc_fence_after_sync();
         uint32_t s0[32], s1[32], s2[32], s3[32];
         tmem_ld_32x32b_x32(t_s + 0, s0);
@@ -338,7 +433,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // S_t is in registers: the next Q_t K^T may overwrite it
         tc_fence_before_sync();
         mbar_arrive(&bars->s_free[t]);
-        if (lane == 0 && warp == 4) GQA_TRACE_EVENT(0, 7, it);
+        if (lane == 0 && warp == 4) GQA_TRACE_EVENT(0, 7, step);
         float s[BN];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
@@ -380,16 +475,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const float m_use = (m_new == -CUDART_INF_F) ? 0.f : m_new;
         const float alpha = need ? ex2_approx(m_run - m_use) : 1.f;
         const uint64_t negm = f32x2(-m_use, -m_use);
-        if (lane == 0 && warp == 4) GQA_TRACE_EVENT(0, 16, it);
+        if (lane == 0 && warp == 4) GQA_TRACE_EVENT(0, 16, step);
         // Ping-pong: the two heads take turns on the exp2 section (MUFU-bound), so
         // each runs at the full MUFU rate while the other head's products keep
         // the tensor pipe busy.  Head 0 goes first in every tile.
-        if (two) {
-          const bool wait_turn = (t == 1) || it > 0;
-          const uint32_t par = t == 0 ? ((it - 1) & 1) : (it & 1);
+        if (un.two) {
+          const bool wait_turn = (t == 1) || tt > 0;
+          const uint32_t par = t == 0 ? ((tt - 1) & 1) : (tt & 1);
           if (wait_turn && !mbar_wait(&bars->turn[t], par, ab, p.status, kTimeoutCode)) { ok = false; break; }
         }
-        if (lane == 0 && warp == 4) GQA_TRACE_EVENT(0, 17, it);
+        if (lane == 0 && warp == 4) GQA_TRACE_EVENT(0, 17, step);
         uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};  // four chains of fp32 pairs (0.0f bits)
         uint32_t pk[BN / 2];
 #pragma unroll
@@ -401,17 +496,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           sum2[c2 & 3] = add_f32x2(sum2[c2 & 3], f32x2(e0, e1));
           pk[c2] = pack_bf16x2(e0, e1);
         }
-        if (lane == 0 && warp == 4) GQA_TRACE_EVENT(0, 18, it);
-        if (two) mbar_arrive(&bars->turn[1 - t]);
+        if (lane == 0 && warp == 4) GQA_TRACE_EVENT(0, 18, step);
+        if (un.two) {
+          mbar_arrive(&bars->turn[1 - t]);
+          ++tt;
+        }
         float sa, sb, sc, sd;
         f32x2_split(add_f32x2(sum2[0], sum2[1]), sa, sb);
         f32x2_split(add_f32x2(sum2[2], sum2[3]), sc, sd);
         const float sum = (sa + sb) + (sc + sd);
-        if (lane == 0 && warp == 4) GQA_TRACE_EVENT(0, 8, it);
+        if (lane == 0 && warp == 4) GQA_TRACE_EVENT(0, 8, step);
         // P_t V of the previous tile must be finished before P_t is overwritten
-        // and O_t rescaled.
+        // and O_t rescaled.  (Before a unit's first tile the previous unit's
+        // epilogue already waited for all of its products.)
         if (it > 0) {
-          if (!mbar_wait(&bars->o_done[t], (it - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+          if (!mbar_wait(&bars->o_done[t], (ts - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
           tc_fence_after_sync();
           if (__any_sync(0xffffffffu, need)) {
             uint32_t o0[32], o1[32];
@@ -447,48 +546,53 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         tmem_wait_st();
         tc_fence_before_sync();
-        if (lane == 0 && (warp == 4 || warp == 8)) GQA_TRACE_EVENT(0, warp == 4 ? 9 : 11, it);
+        if (lane == 0 && (warp == 4 || warp == 8)) GQA_TRACE_EVENT(0, warp == 4 ? 9 : 11, step);
         mbar_arrive(&bars->p_full[t]);
         l_run = l_run * alpha + sum;
         m_run = m_new;
       }
-      if (ok && mbar_wait(&bars->o_full[t], 0, ab, p.status, kTimeoutCode)) {
-        if (lane == 0 && warp == 4) GQA_TRACE_EVENT(0, 12, 0);
-        tc_fence_after_sync();
-        uint32_t o0[32], o1[32];
-        tmem_ld_32x32b_x32(t_o + 0, o0);
-        tmem_ld_32x32b_x32(t_o + 32, o1);
-        tmem_wait_ld();
-        reg_fence(o0);
-        reg_fence(o1);
-        if (i < p.S) {
-          const int h = h0 + t;
-          const float inv_l = 1.f / l_run;
-          const size_t row = (static_cast<size_t>(b) * p.H + h) * p.S + i;
-          uint4 *dst = reinterpret_cast<uint4 *>(p.o + row * HD);
+      if (!ok) break;
+      // ---- epilogue of the unit: O_t / l -> bf16, LSE
+      if (!mbar_wait(&bars->o_full[t], uo & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+      if (lane == 0 && warp == 4 && k == 0) GQA_TRACE_EVENT(0, 12, 0);
+      tc_fence_after_sync();
+      uint32_t o0[32], o1[32];
+      tmem_ld_32x32b_x32(t_o + 0, o0);
+      tmem_ld_32x32b_x32(t_o + 32, o1);
+      tmem_wait_ld();
+      reg_fence(o0);
+      reg_fence(o1);
+      // O_t is in registers: the next unit's first P.V may overwrite it
+      tc_fence_before_sync();
+      mbar_arrive(&bars->o_empty[t]);
+      ++uo;
+      if (i < p.S) {
+        const int h = un.h0 + t;
+        const float inv_l = 1.f / l_run;
+        const size_t row = (static_cast<size_t>(un.b) * p.H + h) * p.S + i;
+        uint4 *dst = reinterpret_cast<uint4 *>(p.o + row * HD);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(o0[8 * c + 0]) * inv_l, __uint_as_float(o0[8 * c + 1]) * inv_l);
-            w.y = pack_bf16x2(__uint_as_float(o0[8 * c + 2]) * inv_l, __uint_as_float(o0[8 * c + 3]) * inv_l);
-            w.z = pack_bf16x2(__uint_as_float(o0[8 * c + 4]) * inv_l, __uint_as_float(o0[8 * c + 5]) * inv_l);
-            w.w = pack_bf16x2(__uint_as_float(o0[8 * c + 6]) * inv_l, __uint_as_float(o0[8 * c + 7]) * inv_l);
-            dst[c] = w;
-          }
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(o1[8 * c + 0]) * inv_l, __uint_as_float(o1[8 * c + 1]) * inv_l);
-            w.y = pack_bf16x2(__uint_as_float(o1[8 * c + 2]) * inv_l, __uint_as_float(o1[8 * c + 3]) * inv_l);
-            w.z = pack_bf16x2(__uint_as_float(o1[8 * c + 4]) * inv_l, __uint_as_float(o1[8 * c + 5]) * inv_l);
-            w.w = pack_bf16x2(__uint_as_float(o1[8 * c + 6]) * inv_l, __uint_as_float(o1[8 * c + 7]) * inv_l);
-            dst[4 + c] = w;
-          }
-          // natural-log LSE of the scaled scores: (m + log2 l) * ln 2
-          p.lse[row] = (m_run + __log2f(l_run)) * 0.69314718055994530942f;
+        for (int c = 0; c < 4; ++c) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(o0[8 * c + 0]) * inv_l, __uint_as_float(o0[8 * c + 1]) * inv_l);
+          w.y = pack_bf16x2(__uint_as_float(o0[8 * c + 2]) * inv_l, __uint_as_float(o0[8 * c + 3]) * inv_l);
+          w.z = pack_bf16x2(__uint_as_float(o0[8 * c + 4]) * inv_l, __uint_as_float(o0[8 * c + 5]) * inv_l);
+          w.w = pack_bf16x2(__uint_as_float(o0[8 * c + 6]) * inv_l, __uint_as_float(o0[8 * c + 7]) * inv_l);
+          dst[c] = w;
         }
-        if (lane == 0 && warp == 4) GQA_TRACE_EVENT(0, 13, 0);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(o1[8 * c + 0]) * inv_l, __uint_as_float(o1[8 * c + 1]) * inv_l);
+          w.y = pack_bf16x2(__uint_as_float(o1[8 * c + 2]) * inv_l, __uint_as_float(o1[8 * c + 3]) * inv_l);
+          w.z = pack_bf16x2(__uint_as_float(o1[8 * c + 4]) * inv_l, __uint_as_float(o1[8 * c + 5]) * inv_l);
+          w.w = pack_bf16x2(__uint_as_float(o1[8 * c + 6]) * inv_l, __uint_as_float(o1[8 * c + 7]) * inv_l);
+          dst[4 + c] = w;
+        }
+        // natural-log LSE of the scaled scores: (m + log2 l) * ln 2
+        p.lse[row] = (m_run + __log2f(l_run)) * 0.69314718055994530942f;
       }
+      if (lane == 0 && warp == 4 && k == 0) GQA_TRACE_EVENT(0, 13, 0);
     }
   }
 

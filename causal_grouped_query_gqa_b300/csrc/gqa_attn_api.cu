@@ -191,10 +191,13 @@ int gqa_attn_fwd(const void *q, const void *k, const void *v, void *o, float *ls
   p.status = ds->status;
   const long long units = static_cast<long long>(p.n_qblocks) * B * G * p.n_pairs;
   if (units > 0x7fffffffLL) return GQA_ERR_SHAPE;
+  p.n_units = static_cast<int>(units);
+  // persistent grid: one CTA per SM (the kernel's shared memory and TMEM allow one)
+  const int grid = static_cast<int>(units < ds->sm_count ? units : ds->sm_count);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   gqa::timing_begin(GQA_KERNEL_FWD, st);
-  gqa_fwd_kernel<<<static_cast<unsigned>(units), NTHREADS, SMEM_BYTES, st>>>(tq, tk, tv, p);
+  gqa_fwd_kernel<<<static_cast<unsigned>(grid), NTHREADS, SMEM_BYTES, st>>>(tq, tk, tv, p);
   gqa::timing_end(GQA_KERNEL_FWD, st);
   return gqa::cuda_failed(cudaGetLastError(), "launch of the forward kernel") ? GQA_ERR_CUDA
                                                                                : GQA_OK;
