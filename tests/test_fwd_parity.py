@@ -60,6 +60,18 @@ def test_scale_not_default():
     _run_full(1, 4, 2, 300, scale=0.37)
 
 
+@pytest.mark.parametrize("B,H,G,S,window,n_sink", [
+    (4, 6, 2, 2048, 0, 0),       # 256 units: each CTA of the persistent grid walks
+                                 # several, two-head and one-head pairs mixed (R = 3)
+    (2, 12, 4, 1536, 300, 70),   # the same with a window and sinks (192 units)
+    (3, 16, 2, 1100, 0, 0),      # R = 8, ragged tail, 216 units
+])
+def test_persistent_grid_many_units(B, H, G, S, window, n_sink):
+    """More work units than SMs, so every CTA carries its barrier phases, Q
+    buffers and O accumulators from one unit to the next."""
+    _run_full(B, H, G, S, window=window, n_sink=n_sink)
+
+
 def test_gqa_workload_full():
     w = WORKLOADS["gqa_b2_h32_g8_s2048"]
     _run_full(w.B, w.H, w.G, w.S)
