@@ -67,6 +67,10 @@ def load_library():
         lib.gqa_attn_last_error_detail.restype = ctypes.c_char_p
         lib.gqa_attn_last_device_status.argtypes = [vp]
         lib.gqa_attn_last_device_status.restype = i
+        lib.gqa_attn_selftest_timeout.argtypes = [ctypes.c_uint,
+                                                  ctypes.POINTER(ctypes.c_ulonglong),
+                                                  ctypes.POINTER(ctypes.c_int), vp]
+        lib.gqa_attn_selftest_timeout.restype = i
         lib.gqa_attn_timing_enable.argtypes = [i]
         lib.gqa_attn_timing_enable.restype = i
         lib.gqa_attn_timing_collect.argtypes = [ctypes.POINTER(ctypes.c_float), i]
@@ -131,6 +135,21 @@ def gqa_attn_last_error_detail() -> str:
 
 def gqa_attn_last_device_status(stream=None) -> int:
     return load_library().gqa_attn_last_device_status(_stream(stream))
+
+
+def gqa_attn_selftest_timeout(budget_ms: int, elapsed_ns=None, returned_ok=None, stream=0) -> int:
+    """C-ABI mirror; elapsed_ns / returned_ok may be ctypes arrays or None."""
+    return load_library().gqa_attn_selftest_timeout(int(budget_ms), elapsed_ns, returned_ok,
+                                                    _stream(stream))
+
+
+def selftest_timeout(budget_ms: int = 20, stream=None):
+    """Runs the device self-test of the bounded waits; returns (status,
+    [elapsed ns of the two waiters], [whether each wait reported success])."""
+    el = (ctypes.c_ulonglong * 2)()
+    ok = (ctypes.c_int * 2)()
+    rc = gqa_attn_selftest_timeout(budget_ms, el, ok, stream)
+    return rc, [int(x) for x in el], [int(x) for x in ok]
 
 
 GQA_KERNEL_COUNT = 4  # fwd, bwd prep, bwd main, bwd dq convert

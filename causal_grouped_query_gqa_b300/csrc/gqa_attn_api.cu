@@ -16,6 +16,7 @@
 #include "trace.cuh"
 #include "bwd_kernels.cuh"
 #include "fwd_kernel.cuh"
+#include "selftest_kernel.cuh"
 
 namespace {
 
@@ -343,6 +344,35 @@ GQA_API int gqa_attn_trace_read(void *host, size_t bytes) {
              : GQA_ERR_CUDA;
 }
 #endif
+
+int gqa_attn_selftest_timeout(unsigned budget_ms, unsigned long long *elapsed_ns,
+                              int *returned_ok, void *stream) {
+  if (!elapsed_ns || !returned_ok) return GQA_ERR_NULL;
+  if (budget_ms == 0 || budget_ms > 1000) return GQA_ERR_SHAPE;
+  DeviceState *ds = nullptr;
+  int rc = device_state(&ds);
+  if (rc != GQA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // start from a clear status word, so the result is this kernel's own
+  if (gqa::cuda_failed(cudaStreamSynchronize(st), "cudaStreamSynchronize")) return GQA_ERR_CUDA;
+  const int zero = 0;
+  if (gqa::cuda_failed(cudaMemcpy(ds->status, &zero, sizeof(int), cudaMemcpyHostToDevice),
+                       "cudaMemcpy(clear device status)"))
+    return GQA_ERR_CUDA;
+  gqa::selftest::selftest_wait_kernel<<<1, 64, 0, st>>>(
+      ds->status, static_cast<uint64_t>(budget_ms) * 1000000ull);
+  if (gqa::cuda_failed(cudaGetLastError(), "launch of the self-test kernel")) return GQA_ERR_CUDA;
+  if (gqa::cuda_failed(cudaStreamSynchronize(st), "cudaStreamSynchronize(self-test)"))
+    return GQA_ERR_CUDA;
+  if (gqa::cuda_failed(cudaMemcpyFromSymbol(elapsed_ns, gqa::selftest::g_selftest_elapsed_ns,
+                                            2 * sizeof(unsigned long long)),
+                       "cudaMemcpyFromSymbol(self-test times)") ||
+      gqa::cuda_failed(cudaMemcpyFromSymbol(returned_ok, gqa::selftest::g_selftest_returned,
+                                            2 * sizeof(int)),
+                       "cudaMemcpyFromSymbol(self-test results)"))
+    return GQA_ERR_CUDA;
+  return gqa_attn_last_device_status(stream);
+}
 
 int gqa_attn_last_device_status(void *stream) {
   DeviceState *ds = nullptr;

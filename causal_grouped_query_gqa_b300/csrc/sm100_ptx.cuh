@@ -88,14 +88,15 @@ struct AbortState {
 // Returns false (and raises the CTA abort flag and the global status) on timeout
 // or when another role of the CTA has already aborted.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, AbortState *ab,
-                                          int *status, int code) {
+                                          int *status, int code,
+                                          uint64_t budget_ns = kWaitBudgetNs) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait_sleep(a, parity, kSuspendNs)) return true;
     if (ab->flag) return false;
-    if (globaltimer_ns() - t0 > kWaitBudgetNs) {
+    if (globaltimer_ns() - t0 > budget_ns) {
       ab->flag = 1;
       if (status) atomicCAS(status, 0, code);
       return false;

@@ -158,6 +158,23 @@ GQA_API const char *gqa_attn_last_error_detail(void);
 GQA_API int gqa_attn_last_device_status(void *stream);
 
 /*
+ * Self-test of the failure detection, on the device, without faulting it.
+ * Launches one CTA on `stream` whose two waiting threads wait on mbarriers
+ * that nothing ever arrives on: the first gives up after `budget_ms`
+ * (1..1000), raises the CTA abort flag and records GQA_ERR_DEVICE_TIMEOUT; the
+ * second waits with the kernels' normal 2 s budget and must leave through the
+ * abort flag within about 1 ms of the first.  Synchronises `stream`.
+ * elapsed_ns[2] (host) receives each thread's wait in nanoseconds and
+ * returned_ok[2] (host) whether each wait reported success (expected 0, 0).
+ * Returns the device status word read (and cleared) afterwards, which is
+ * GQA_ERR_DEVICE_TIMEOUT when detection works; GQA_ERR_NULL / GQA_ERR_SHAPE
+ * for bad arguments, GQA_ERR_CUDA if a CUDA call failed.  The CUDA context
+ * stays usable: nothing traps, faults or hangs.
+ */
+GQA_API int gqa_attn_selftest_timeout(unsigned budget_ms, unsigned long long *elapsed_ns,
+                                      int *returned_ok, void *stream);
+
+/*
  * Kernel timing (a profiling aid, not thread-safe).  While enabled, every
  * kernel the library launches is bracketed by CUDA events recorded on its own
  * launch stream.  gqa_attn_timing_collect() waits for the events of the last
