@@ -48,10 +48,25 @@ def build(force: bool = False, verbose: bool = False, out: str = LIB, extra=()) 
     return out
 
 
+# Failure-detection test build: CTA 0's producers skip one load and every wait
+# gives up after 100 ms (see GQA_INJECT_STALL in the kernels).  Used only by
+# tests/test_failure_detection.py; never loaded by the package.
+STALL_TEST_LIB = os.path.join(PKG, "libgqa_attn_stalltest.so")
+STALL_TEST_FLAGS = ("-DGQA_INJECT_STALL", "-DGQA_WAIT_BUDGET_NS=100000000ull")
+
+
+def build_stall_test(force: bool = False, verbose: bool = False) -> str:
+    return build(force=force, verbose=verbose, out=STALL_TEST_LIB, extra=STALL_TEST_FLAGS)
+
+
 if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose", action="store_true")
+    ap.add_argument("--stall-test", action="store_true",
+                    help="also build the failure-detection test library")
     a = ap.parse_args()
     print(build(force=a.force, verbose=a.verbose))
+    if a.stall_test:
+        print(build_stall_test(force=a.force, verbose=a.verbose))
     sys.exit(0)

@@ -378,6 +378,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int bh = b * p.H + h;
         if (!mbar_wait(&bars->qdo_empty[st], ph ^ 1, ab, p.status, kTimeoutCode)) break;
         GQA_TRACE_EVENT(1, 0, n);
+#ifdef GQA_INJECT_STALL
+        // failure-detection test build only: CTA 0 never loads one step's Q/dO
+        if (blockIdx.x == 0 && n == min(1, nsteps - 1)) {
+          issued = n + 1;
+          continue;
+        }
+#endif
         mbar_arrive_expect_tx(&bars->qdo_full[st], 2 * TILE_BYTES + 2 * BQ * 4);
         tma_load_3d(smem + SM_Q + st * TILE_BYTES, &tm_q, &bars->qdo_full[st], 0, qb * BQ, bh);
         tma_load_3d(smem + SM_DO + st * TILE_BYTES, &tm_do, &bars->qdo_full[st], 0, qb * BQ, bh);
@@ -480,7 +487,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int i0 = qb * BQ;
       const float *lse2 = vec + st * 2 * BQ;
       const float *dlt = lse2 + BQ;
-      if (!mbar_wait(&bars->st_full, n & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+      if (!mbar_wait_warp(&bars->st_full, n & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
       if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 8, n);
       tc_fence_after_sync();
       const bool masked = pair_needs_mask(qb, kb, p);
@@ -511,7 +518,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       // the previous step's dV must be done with P^T
       if (n > 0) {
-        if (!mbar_wait(&bars->pt_free, (n - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        if (!mbar_wait_warp(&bars->pt_free, (n - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
         tc_fence_after_sync();
       }
       if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 10, n);
@@ -522,7 +529,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_before_sync();
       mbar_arrive(&bars->pt_ready);
       // the previous step's dK and dQ must be done with dS
-      if (n > 0 && !mbar_wait(&bars->ds_free, (n - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+      if (n > 0 && !mbar_wait_warp(&bars->ds_free, (n - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
       // dS: half wg of the tile, key row r, chunk c of 8 queries at (c ^ (r & 7))
 #pragma unroll
       for (int q8 = 0; q8 < 4; ++q8) {
@@ -536,7 +543,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_arrive(&bars->ds_ready);
     }
     // epilogue: group 0 writes dV, group 1 writes dK (x scale), one key row per thread
-    if (ok && mbar_wait(&bars->dkv_done, 0, ab, p.status, kTimeoutCode)) {
+    if (ok && mbar_wait_warp(&bars->dkv_done, 0, ab, p.status, kTimeoutCode)) {
       tc_fence_after_sync();
       uint32_t a0[32], a1[32];
       const uint32_t col = wg == 0 ? C_DV : C_DK;
@@ -581,7 +588,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int n = 0; n < nsteps; ++n) {
       const int h = g * p.R + n / nqt;
       const int qb = qlo + n % nqt;
-      if (!mbar_wait(&bars->dq_full, n & 1, ab, p.status, kTimeoutCode)) break;
+      // The four drain warps meet at named barriers below, so they decide
+      // together whether to go on: one warp must never leave while the others
+      // wait there for it.
+      if (!named_bar_and(1, 128, mbar_wait(&bars->dq_full, n & 1, ab, p.status, kTimeoutCode)))
+        break;
       if (leader) GQA_TRACE_EVENT(1, 12, n);
       tc_fence_after_sync();
       uint32_t a0[32], a1[32];

@@ -273,6 +273,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             break;
           }
           GQA_TRACE_EVENT(0, 0, k == 0 ? it : kTraceSteps);
+#ifdef GQA_INJECT_STALL
+          // failure-detection test build only: CTA 0 never loads one K/V tile
+          // of its first unit, so every role must leave through the bounded
+          // waits and the abort flag
+          if (blockIdx.x == 0 && k == 0 && it == min(1, kr.count - 1)) continue;
+#endif
           mbar_arrive_expect_tx(&bars->kv_full[st], 2 * TILE_BYTES);
           tma_load_3d(smem + SM_K + st * TILE_BYTES, &tm_k, &bars->kv_full[st], 0, kb * BN, kvz);
           tma_load_3d(smem + SM_V + st * TILE_BYTES, &tm_v, &bars->kv_full[st], 0, kb * BN, kvz);
@@ -392,6 +398,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t t_o = tbase + lane_off + col_o(t);
     const uint32_t t_p = tbase + lane_off + col_p(t);
     const uint64_t sl2x2 = f32x2(sl2, sl2);
+    // The waits below are per thread, without a warp vote (a vote on each of
+    // them cost 3-4 % of the forward): the warp is converged at every wait and
+    // inside the wait loop, so its lanes execute each try_wait, abort-flag load
+    // and clock read as one instruction and take the same branch; the result
+    // is warp-uniform before the warp-collective tcgen05.ld/st that follow.
     int ts = 0;  // tiles of this head (all units): S, P and O-done phases
     int uo = 0;  // units of this head: O-full / O-empty phases
     int tt = 0;  // tiles of two-head units: ping-pong phases (same count in both heads)

@@ -73,7 +73,11 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 
 // Budget of one wait.  Legitimate waits inside one CTA last microseconds; a
 // wait that lasts this long means the pipeline is broken.
-constexpr uint64_t kWaitBudgetNs = 2000000000ull;  // 2 s
+// (A test build of the library shortens it with -DGQA_WAIT_BUDGET_NS.)
+#ifndef GQA_WAIT_BUDGET_NS
+#define GQA_WAIT_BUDGET_NS 2000000000ull
+#endif
+constexpr uint64_t kWaitBudgetNs = GQA_WAIT_BUDGET_NS;  // 2 s
 // Longest single hardware suspension inside a wait (the thread wakes earlier
 // when the phase completes); the budget above is checked between suspensions.
 constexpr uint32_t kSuspendNs = 1000000u;  // 1 ms
@@ -102,6 +106,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, AbortS
       return false;
     }
   }
+}
+
+// The same wait with one result for the whole warp (every lane waits with
+// acquire semantics, then they vote), for warps whose next instructions are
+// warp-collective (tcgen05.ld/st): on the abort path a lane that saw the phase
+// complete and one that saw the abort flag must not split the warp.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, AbortState *ab,
+                                               int *status, int code) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, ab, status, code));
 }
 
 // Same, without abort bookkeeping: for drains at the exit (bounded, silent).
@@ -171,6 +184,20 @@ __device__ __forceinline__ void bulk_wait_group_all() {
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// Named barrier that also ANDs a predicate over the `count` participating
+// threads: every participant gets the same result.
+__device__ __forceinline__ bool named_bar_and(int id, int count, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "barrier.cta.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
 }
 
 // Orders this thread's generic-proxy shared-memory writes before later

@@ -48,3 +48,61 @@ def test_expired_wait_is_reported_and_the_context_survives(budget_ms):
     assert gq.gqa_attn_last_device_status() == gq.GQA_OK
     ro, _ = oracle.attn_fwd(to64(q), to64(k), to64(v))
     check_close("O after the self-test", to64(o), ro)
+
+
+def _stall_lib():
+    """The failure-detection test build of the library (a separate module with
+    its own device status word): CTA 0 of each kernel never gets one of its
+    loads, and every wait gives up after 100 ms."""
+    from causal_grouped_query_gqa_b300 import build as gbuild
+    path = gbuild.build_stall_test()
+    lib = ctypes.CDLL(path)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.gqa_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp]
+    lib.gqa_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                 i, i, i, i, i, i, i, i, f, vp, sz, vp]
+    lib.gqa_attn_bwd_workspace_size.argtypes = [i, i, i, i, i]
+    lib.gqa_attn_bwd_workspace_size.restype = sz
+    lib.gqa_attn_last_device_status.argtypes = [vp]
+    return lib
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("window,n_sink", [(0, 0), (200, 64)])
+def test_production_kernels_leave_through_the_abort_path(window, n_sink):
+    """A load that never lands: the forward and the backward must each end
+    (every role leaves through its bounded waits and the CTA abort flag, TMEM
+    is freed), report GQA_ERR_DEVICE_TIMEOUT, and leave the context usable."""
+    import time
+    lib = _stall_lib()
+    B, H, G, S, d, scale = 1, 4, 2, 700, 64, 0.125
+    q, k, v, do = (t.cuda() for t in make_inputs(B, H, G, S, seed=9, with_grad=True))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(lib.gqa_attn_bwd_workspace_size(B, H, G, S, d), dtype=torch.uint8,
+                     device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+    p = lambda t: t.data_ptr()
+    assert lib.gqa_attn_last_device_status(st) == gq.GQA_OK
+    t0 = time.perf_counter()
+    assert lib.gqa_attn_fwd(p(q), p(k), p(v), p(o), p(lse), B, H, G, S, d, 1, window, n_sink,
+                            scale, st) == gq.GQA_OK
+    assert lib.gqa_attn_last_device_status(st) == gq.GQA_ERR_DEVICE_TIMEOUT
+    assert lib.gqa_attn_bwd(p(q), p(k), p(v), p(o), p(do), p(lse), p(dq), p(dk), p(dv), B, H, G,
+                            S, d, 1, window, n_sink, scale, p(ws), ws.numel(),
+                            st) == gq.GQA_OK
+    assert lib.gqa_attn_last_device_status(st) == gq.GQA_ERR_DEVICE_TIMEOUT
+    assert time.perf_counter() - t0 < 10.0  # bounded waits of 100 ms, a few in sequence
+    # the context is intact: the regular library computes correct results
+    o2, lse2 = gq.fwd(q, k, v, window=window, n_sink=n_sink, scale=scale)
+    dq2, dk2, dv2 = gq.bwd(q, k, v, o2, do, lse2, window=window, n_sink=n_sink, scale=scale)
+    torch.cuda.synchronize()
+    assert gq.gqa_attn_last_device_status() == gq.GQA_OK
+    ro, _ = oracle.attn_fwd(to64(q), to64(k), to64(v), window=window, n_sink=n_sink, scale=scale)
+    rq, rk, rv = oracle.attn_bwd(to64(q), to64(k), to64(v), to64(do), window=window,
+                                 n_sink=n_sink, scale=scale)
+    check_close("O after the aborted launches", to64(o2), ro)
+    check_close("dQ after the aborted launches", to64(dq2), rq)
+    check_close("dK after the aborted launches", to64(dk2), rk)
+    check_close("dV after the aborted launches", to64(dv2), rv)
