@@ -20,7 +20,8 @@ Tensor helpers: ``fwd(q, k, v, ...)`` and ``bwd(q, k, v, o, dout, lse, ...)``.
 from __future__ import annotations
 
 from ._lib import (GQA_ERR_ALIGN, GQA_ERR_CUDA, GQA_ERR_DEVICE_TIMEOUT, GQA_ERR_HEADDIM,
-                   GQA_ERR_MASK, GQA_ERR_NULL, GQA_ERR_SCALE, GQA_ERR_SHAPE, GQA_ERR_TOO_LARGE,
+                   GQA_ERR_DEVICE_BOUNDS, GQA_ERR_MASK, GQA_ERR_NULL, GQA_ERR_SCALE,
+                   GQA_ERR_SHAPE, GQA_ERR_TOO_LARGE,
                    GQA_ERR_WORKSPACE, GQA_NOALLOC_SCRATCH_BYTES, GQA_OK, GqaError, bwd, fwd,
                    gqa_attn_bwd, gqa_attn_bwd_noalloc,
                    gqa_attn_bwd_workspace_size, gqa_attn_fwd, gqa_attn_last_device_status,
@@ -29,7 +30,7 @@ from ._lib import (GQA_ERR_ALIGN, GQA_ERR_CUDA, GQA_ERR_DEVICE_TIMEOUT, GQA_ERR_
 
 __all__ = [
     "fwd", "bwd", "gqa_attn_fwd", "gqa_attn_bwd", "gqa_attn_bwd_noalloc",
-    "gqa_attn_bwd_workspace_size", "GQA_ERR_TOO_LARGE", "GQA_NOALLOC_SCRATCH_BYTES",
+    "gqa_attn_bwd_workspace_size", "GQA_ERR_TOO_LARGE", "GQA_ERR_DEVICE_BOUNDS", "GQA_NOALLOC_SCRATCH_BYTES",
     "gqa_attn_strerror", "gqa_attn_last_error_detail", "gqa_attn_last_device_status",
     "gqa_attn_selftest_timeout", "selftest_timeout", "gqa_attn_timing_enable",
     "gqa_attn_timing_collect", "timing_buffer", "load_library", "lib_path", "GqaError",

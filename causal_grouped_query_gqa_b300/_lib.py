@@ -21,6 +21,7 @@ GQA_ERR_WORKSPACE = -7
 GQA_ERR_CUDA = -8
 GQA_ERR_DEVICE_TIMEOUT = -9
 GQA_ERR_TOO_LARGE = -10
+GQA_ERR_DEVICE_BOUNDS = -11
 GQA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 

@@ -59,14 +59,25 @@ def build_stall_test(force: bool = False, verbose: bool = False) -> str:
     return build(force=force, verbose=verbose, out=STALL_TEST_LIB, extra=STALL_TEST_FLAGS)
 
 
+# Debug build with the kernels' run-time index checks (GQA_DEVICE_CHECKS): a
+# violated check reports GQA_ERR_DEVICE_BOUNDS instead of touching memory.
+# Used only by tests/test_device_checks.py.
+CHECKED_LIB = os.path.join(PKG, "libgqa_attn_checked.so")
+
+
+def build_checked(force: bool = False, verbose: bool = False) -> str:
+    return build(force=force, verbose=verbose, out=CHECKED_LIB, extra=("-DGQA_DEVICE_CHECKS",))
+
+
 if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose", action="store_true")
-    ap.add_argument("--stall-test", action="store_true",
-                    help="also build the failure-detection test library")
+    ap.add_argument("--test-libs", action="store_true",
+                    help="also build the failure-detection and index-check test libraries")
     a = ap.parse_args()
     print(build(force=a.force, verbose=a.verbose))
-    if a.stall_test:
+    if a.test_libs:
         print(build_stall_test(force=a.force, verbose=a.verbose))
+        print(build_checked(force=a.force, verbose=a.verbose))
     sys.exit(0)

@@ -39,6 +39,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "device_checks.cuh"
 #include "error_detail.cuh"
 #include "sm100_ptx.cuh"
 #include "timing.cuh"
@@ -366,6 +367,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
       const int kvz = b * p.G + g;
+      GQA_REPORT(p.status, kb >= 0 && kb * BK < p.S && kvz < p.B * p.G && qlo <= qhi);
       mbar_arrive_expect_tx(&bars->kv_full, 2 * TILE_BYTES);
       tma_load_3d(smem + SM_K, &tm_k, &bars->kv_full, 0, kb * BK, kvz);
       tma_load_3d(smem + SM_V, &tm_v, &bars->kv_full, 0, kb * BK, kvz);
@@ -385,6 +387,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           continue;
         }
 #endif
+        GQA_REPORT(p.status, h < p.H && qb >= 0 && qb * BQ < p.S &&
+                                static_cast<size_t>(bh) * p.S_pad + (qb + 1) * BQ <=
+                                    static_cast<size_t>(p.B) * p.H * p.S_pad);
         mbar_arrive_expect_tx(&bars->qdo_full[st], 2 * TILE_BYTES + 2 * BQ * 4);
         tma_load_3d(smem + SM_Q + st * TILE_BYTES, &tm_q, &bars->qdo_full[st], 0, qb * BQ, bh);
         tma_load_3d(smem + SM_DO + st * TILE_BYTES, &tm_do, &bars->qdo_full[st], 0, qb * BQ, bh);
@@ -552,7 +557,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tmem_wait_ld();
       reg_fence(a0);
       reg_fence(a1);
-      if (j < p.S) {
+      if (j < p.S && GQA_CHECK(p.status, b < p.B && g < p.G)) {
         const float f = wg == 0 ? 1.f : p.scale;
         __nv_bfloat16 *dst = (wg == 0 ? p.dv : p.dk) +
                              ((static_cast<size_t>(b) * p.G + g) * p.S + j) * HD;
@@ -617,7 +622,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       fence_proxy_async_smem();
       named_bar_sync(1, 128);
-      if (leader) {
+      if (leader && GQA_CHECK(p.status, h < p.H && qb * BQ < p.S)) {
         const int bh = b * p.H + h;
         uint8_t *box = smem + SM_DQ;
         tma_reduce_add_3d(&tm_dq, box, 0, qb * BQ, bh);

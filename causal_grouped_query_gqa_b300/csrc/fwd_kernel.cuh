@@ -45,6 +45,7 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
+#include "device_checks.cuh"
 #include "sm100_ptx.cuh"
 #include "trace.cuh"
 
@@ -260,6 +261,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // the previous unit's Q K^T products must have read Q
         if (k > 0 && !mbar_wait(&bars->q_empty, (k - 1) & 1, ab, p.status, kTimeoutCode)) break;
         const int qrow = un.qb * BM, qz = un.b * p.H + un.h0;
+        GQA_REPORT(p.status, un.qb >= 0 && un.qb < p.n_qblocks && kr.count >= 1 &&
+                                qz + (un.two ? 1 : 0) < p.B * p.H);
         mbar_arrive_expect_tx(&bars->q_full, (un.two ? 2 : 1) * TILE_BYTES);
         tma_load_3d(smem + SM_Q, &tm_q, &bars->q_full, 0, qrow, qz);
         if (un.two) tma_load_3d(smem + SM_Q + TILE_BYTES, &tm_q, &bars->q_full, 0, qrow, qz + 1);
@@ -279,6 +282,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           // waits and the abort flag
           if (blockIdx.x == 0 && k == 0 && it == min(1, kr.count - 1)) continue;
 #endif
+          GQA_REPORT(p.status, kb >= 0 && kb * BN < p.S && kvz < p.B * p.G);
           mbar_arrive_expect_tx(&bars->kv_full[st], 2 * TILE_BYTES);
           tma_load_3d(smem + SM_K + st * TILE_BYTES, &tm_k, &bars->kv_full[st], 0, kb * BN, kvz);
           tma_load_3d(smem + SM_V + st * TILE_BYTES, &tm_v, &bars->kv_full[st], 0, kb * BN, kvz);
@@ -577,10 +581,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_before_sync();
       mbar_arrive(&bars->o_empty[t]);
       ++uo;
-      if (i < p.S) {
-        const int h = un.h0 + t;
+      const int h = un.h0 + t;
+      const size_t row = (static_cast<size_t>(un.b) * p.H + h) * p.S + i;
+      if (i < p.S && GQA_CHECK(p.status, h < p.H && row < static_cast<size_t>(p.B) * p.H * p.S)) {
         const float inv_l = 1.f / l_run;
-        const size_t row = (static_cast<size_t>(un.b) * p.H + h) * p.S + i;
         uint4 *dst = reinterpret_cast<uint4 *>(p.o + row * HD);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {

@@ -153,6 +153,7 @@ const char *gqa_attn_strerror(int status) {
     case GQA_ERR_CUDA: return "CUDA call or kernel launch failed";
     case GQA_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait";
     case GQA_ERR_TOO_LARGE: return "problem needs more scratch than gqa_attn_bwd_noalloc holds";
+    case GQA_ERR_DEVICE_BOUNDS: return "a kernel's run-time index check failed (debug build)";
     default: return "unknown status";
   }
 }

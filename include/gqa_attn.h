@@ -61,7 +61,9 @@ typedef enum {
     GQA_ERR_WORKSPACE = -7,      /* workspace smaller than gqa_attn_bwd_workspace_size() */
     GQA_ERR_CUDA = -8,           /* a CUDA runtime/driver call or a launch failed */
     GQA_ERR_DEVICE_TIMEOUT = -9, /* a kernel gave up a bounded wait (device status) */
-    GQA_ERR_TOO_LARGE = -10      /* needs more than the fixed scratch of gqa_attn_bwd_noalloc */
+    GQA_ERR_TOO_LARGE = -10,     /* needs more than the fixed scratch of gqa_attn_bwd_noalloc */
+    GQA_ERR_DEVICE_BOUNDS = -11  /* a run-time index check of a debug build failed (device status;
+                                    only libraries built with -DGQA_DEVICE_CHECKS report it) */
 } gqa_status;
 
 /*
