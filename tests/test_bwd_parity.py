@@ -64,6 +64,7 @@ def test_full_attention(S):
     (500, 600, 5),
     (1000, 128, 128),
     (777, 129, 300),
+    (300, 50, 1000),
 ])
 def test_window_sinks(S, window, n_sink):
     _run_full(1, 4, 2, S, window=window, n_sink=n_sink)

@@ -51,6 +51,7 @@ def test_full_attention(S):
     (500, 600, 5),      # window longer than the sequence: plain causal
     (1000, 128, 128),   # tile-aligned window and sinks
     (777, 129, 300),    # sinks spanning three tiles
+    (300, 50, 1000),    # more sinks than keys: every key is a sink, plain causal
 ])
 def test_window_sinks(S, window, n_sink):
     _run_full(1, 4, 2, S, window=window, n_sink=n_sink)
