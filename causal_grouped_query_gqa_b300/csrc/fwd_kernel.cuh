@@ -60,8 +60,8 @@ constexpr int TILE_BYTES = BM * HD * 2;  // 16 KB, 128-byte rows
 constexpr int NTHREADS = 384;
 // Registers per thread after the split: warps 0-3 (producer, MMA, TMEM alloc)
 // drop to kRegsControl, the two softmax warpgroups rise to kRegsSoftmax.
-constexpr int kRegsControl = 80;
-constexpr int kRegsSoftmax = 200;
+constexpr int kRegsControl = 72;
+constexpr int kRegsSoftmax = 208;
 // the launch allocation must cover the split (checked on the host)
 constexpr int kMinLaunchRegs = (128 * kRegsControl + 256 * kRegsSoftmax + NTHREADS - 1) / NTHREADS;
 constexpr uint32_t TMEM_COLS = 512;
