@@ -178,39 +178,53 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__re
   const int lane = threadIdx.x & 31;
   const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
-  const int sub = lane >> 3;  // row within the group of four
+  const int sub = lane >> 3;  // row within a group of four
   const int ch = lane & 7;    // 16-byte chunk of the row
-  for (long long r0 = warp * 4; r0 < rows_pad; r0 += nwarps * 4) {
-    const long long r = r0 + sub;
-    float acc = 0.f;
-    long long src = -1;
-    if (r < rows_pad) {
-      const long long bh = r / S_pad;
-      const int i = static_cast<int>(r - bh * S_pad);
-      if (i < S) {
-        src = bh * S + i;
-        const uint4 a = reinterpret_cast<const uint4 *>(o + src * HD)[ch];
-        const uint4 c = reinterpret_cast<const uint4 *>(dout + src * HD)[ch];
-        const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&a);
-        const __nv_bfloat162 *c2 = reinterpret_cast<const __nv_bfloat162 *>(&c);
+  // eight rows per warp and iteration, as two groups of four whose loads are
+  // all issued before either is used (more bytes in flight per warp)
+  for (long long r0 = warp * 8; r0 < rows_pad; r0 += nwarps * 8) {
+    long long src[2];
+    uint4 a[2], c[2];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 x = __bfloat1622float2(a2[e]);
-          const float2 y = __bfloat1622float2(c2[e]);
-          acc = fmaf(x.x, y.x, acc);
-          acc = fmaf(x.y, y.y, acc);
+    for (int u = 0; u < 2; ++u) {
+      const long long r = r0 + 4 * u + sub;
+      src[u] = -1;
+      a[u] = c[u] = make_uint4(0, 0, 0, 0);
+      if (r < rows_pad) {
+        const long long bh = r / S_pad;
+        const int i = static_cast<int>(r - bh * S_pad);
+        if (i < S) {
+          src[u] = bh * S + i;
+          a[u] = reinterpret_cast<const uint4 *>(o + src[u] * HD)[ch];
+          c[u] = reinterpret_cast<const uint4 *>(dout + src[u] * HD)[ch];
         }
-        float4 *z = reinterpret_cast<float4 *>(dq_acc + src * HD) + 2 * ch;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const long long r = r0 + 4 * u + sub;
+      float acc = 0.f;
+      const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&a[u]);
+      const __nv_bfloat162 *c2 = reinterpret_cast<const __nv_bfloat162 *>(&c[u]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 x = __bfloat1622float2(a2[e]);
+        const float2 y = __bfloat1622float2(c2[e]);
+        acc = fmaf(x.x, y.x, acc);
+        acc = fmaf(x.y, y.y, acc);
+      }
+      if (src[u] >= 0) {
+        float4 *z = reinterpret_cast<float4 *>(dq_acc + src[u] * HD) + 2 * ch;
         z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
         z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
-    }
-    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-    if (r < rows_pad && ch == 0) {
-      delta[r] = src >= 0 ? acc : 0.f;
-      lse2[r] = src >= 0 ? lse[src] * 1.4426950408889634f : 0.f;
+      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+      if (r < rows_pad && ch == 0) {
+        delta[r] = src[u] >= 0 ? acc : 0.f;
+        lse2[r] = src[u] >= 0 ? lse[src[u]] * 1.4426950408889634f : 0.f;
+      }
     }
   }
 }
@@ -705,7 +719,7 @@ inline int launch(const Problem &pr, const void *q, const void *k, const void *v
   }
 
   {
-    const long long warps_needed = (rows_pad + 3) / 4;
+    const long long warps_needed = (rows_pad + 7) / 8;
     long long blocks = (warps_needed * 32 + 255) / 256;
     blocks = blocks < 1 ? 1 : (blocks > 8LL * sm_count ? 8LL * sm_count : blocks);
     timing_begin(1, st);
