@@ -25,6 +25,10 @@
 //          step n into registers, so those warps overlap step n's dV, dK, dQ;
 //          P^T and dS are handed over separately (dV starts while dS is still
 //          being written) and freed separately (after dV, after dK and dQ).
+//          dS alternates between two shared-memory tiles by step, so each half
+//          of a row is stored as soon as it is computed: the tile being written
+//          was last read by the products of step n - 2, long finished, while
+//          step n - 1's dK and dQ still read the other one.
 //          dK, dV are summed over the group's heads inside the CTA
 //          (deterministic) and written once as bf16;
 //   convert dQ = bf16(scale * accumulator).
@@ -76,9 +80,10 @@ constexpr int SM_K = 0;
 constexpr int SM_V = SM_K + TILE_BYTES;
 constexpr int SM_Q = SM_V + TILE_BYTES;                 // NSTAGE tiles
 constexpr int SM_DO = SM_Q + NSTAGE * TILE_BYTES;       // NSTAGE tiles
-constexpr int SM_DS = SM_DO + NSTAGE * TILE_BYTES;      // 32 KB: dS, two 64-query halves
-constexpr int SM_DQ = SM_DS + 2 * TILE_BYTES;           // 32 KB fp32 dQ staging
-constexpr int SM_VEC = SM_DQ + 2 * TILE_BYTES;          // NSTAGE x (LSE2[128], D[128]) fp32
+constexpr int DS_BYTES = 2 * TILE_BYTES;                 // one dS tile: two 64-query halves
+constexpr int SM_DS = SM_DO + NSTAGE * TILE_BYTES;      // two dS tiles, alternating by step
+constexpr int SM_DQ = SM_DS + 2 * DS_BYTES;             // 16 KB fp32 dQ staging (32 columns)
+constexpr int SM_VEC = SM_DQ + TILE_BYTES;              // NSTAGE x (LSE2[128], D[128]) fp32
 constexpr int SM_BARS = SM_VEC + NSTAGE * 2 * BQ * 4;
 
 struct Bars {
@@ -90,7 +95,7 @@ struct Bars {
   uint64_t pt_ready;  // P^T stored in TMEM (256 P/dS threads)
   uint64_t ds_ready;  // dS stored in shared memory (256 P/dS threads)
   uint64_t pt_free;   // dV of the step finished: P^T may be overwritten (issuer B commit)
-  uint64_t ds_free;   // dK, dQ of the step finished: dS may be overwritten (issuer B commit)
+  uint64_t ds_free[2];  // dK, dQ finished with dS tile t (issuer B commit, steps t, t+2, ...)
   uint64_t dq_full;   // dQ tile ready (issuer B commit)
   uint64_t dq_free;   // dQ tile read out (128 drain threads)
   uint64_t a_done;    // every product of issuer A finished
@@ -353,7 +358,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(&bars->pt_ready, 256);
     mbar_init(&bars->ds_ready, 256);
     mbar_init(&bars->pt_free, 1);
-    mbar_init(&bars->ds_free, 1);
+    mbar_init(&bars->ds_free[0], 1);
+    mbar_init(&bars->ds_free[1], 1);
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_free, 128);
     mbar_init(&bars->a_done, 1);
@@ -452,11 +458,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint32_t do_addr = smem_u32(smem + SM_DO);
       const uint32_t ds_addr = smem_u32(smem + SM_DS);
       const uint64_t k_mn = sdesc_sw128(smem_u32(smem + SM_K), TILE_BYTES, 1024);
-      const uint64_t ds_mn = sdesc_sw128(ds_addr, TILE_BYTES, 1024);  // LBO: next 64-query half
       bool ok = true;
       for (int n = 0; n < nsteps; ++n) {
         const int st = n % NSTAGE;
         const uint64_t q_mn = sdesc_sw128(q_addr + st * TILE_BYTES, TILE_BYTES, 1024);
+        const uint32_t ds_t = ds_addr + (n & 1) * DS_BYTES;  // this step's dS tile
+        const uint64_t ds_mn = sdesc_sw128(ds_t, TILE_BYTES, 1024);  // LBO: next 64-query half
         const uint64_t do_mn = sdesc_sw128(do_addr + st * TILE_BYTES, TILE_BYTES, 1024);
         if (!mbar_wait(&bars->pt_ready, n & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
         GQA_TRACE_EVENT(1, 4, n);
@@ -472,7 +479,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // the first 16 KB half, 64-127 in the second; 32 B per 16 queries)
 #pragma unroll
         for (int ks = 0; ks < BQ / 16; ++ks) {
-          const uint64_t a = sdesc_sw128(ds_addr + (ks >> 2) * TILE_BYTES + (ks & 3) * 32, 16, 1024);
+          const uint64_t a = sdesc_sw128(ds_t + (ks >> 2) * TILE_BYTES + (ks & 3) * 32, 16, 1024);
           mma_bf16_ss(tbase + C_DK, a, q_mn + ks * 128, id_ts, (n > 0 || ks > 0));
         }
         mma_commit(&bars->qdo_empty[st]);
@@ -483,7 +490,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int ks = 0; ks < BK / 16; ++ks)  // 16 keys = 2048 B of the MN-major operands
           mma_bf16_ss(tbase + C_DQ, ds_mn + ks * 128, k_mn + ks * 128, id_dq, ks > 0);
         mma_commit(&bars->dq_full);
-        mma_commit(&bars->ds_free);
+        mma_commit(&bars->ds_free[n & 1]);
         GQA_TRACE_EVENT(1, 6, n);
       }
       mma_commit(&bars->dkv_done);
@@ -498,7 +505,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int j = kb * BK + r;              // key index
     const float sl2 = p.scale_log2;
     const uint32_t lane_off = static_cast<uint32_t>(lane_base) << 16;
-    uint8_t *ds_row = smem + SM_DS + wg * TILE_BYTES + r * 128;
+    // this thread's key row of its group's 64-query half of a dS tile; chunk c
+    // of 8 queries sits at (c ^ (r & 7)) (128-byte swizzle)
+    uint8_t *ds_row0 = smem + SM_DS + wg * TILE_BYTES + r * 128;
     bool ok = true;
     for (int n = 0; n < nsteps; ++n) {
       const int st = n % NSTAGE;
@@ -521,6 +530,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         p_ds_chunk(sr, dr, lse2, dlt, 64 * wg, masked ? visible_bits(64 * wg, i0, j, p) : 0u,
                    masked, sl2, pp0, pd0);
       }
+      // dS goes to the step's tile as soon as each half of the row is computed:
+      // the tile was last read by the dK and dQ products of step n - 2
+      uint8_t *ds_row = ds_row0 + (n & 1) * DS_BYTES;
+      if (n >= 2 && !mbar_wait_warp(&bars->ds_free[n & 1], ((n >> 1) - 1) & 1, ab, p.status, kTimeoutCode)) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8)
+        *reinterpret_cast<uint4 *>(ds_row + ((q8 ^ (r & 7)) << 4)) =
+            make_uint4(pd0[4 * q8], pd0[4 * q8 + 1], pd0[4 * q8 + 2], pd0[4 * q8 + 3]);
       {
         uint32_t sr[32], dr[32];
         tmem_ld_32x32b_x32(tbase + lane_off + C_S + 64 * wg + 32, sr);
@@ -535,6 +555,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         p_ds_chunk(sr, dr, lse2, dlt, 64 * wg + 32,
                    masked ? visible_bits(64 * wg + 32, i0, j, p) : 0u, masked, sl2, pp1, pd1);
       }
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8)
+        *reinterpret_cast<uint4 *>(ds_row + (((4 + q8) ^ (r & 7)) << 4)) =
+            make_uint4(pd1[4 * q8], pd1[4 * q8 + 1], pd1[4 * q8 + 2], pd1[4 * q8 + 3]);
       // the previous step's dV must be done with P^T
       if (n > 0) {
         if (!mbar_wait_warp(&bars->pt_free, (n - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
@@ -547,16 +571,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tmem_wait_st();
       tc_fence_before_sync();
       mbar_arrive(&bars->pt_ready);
-      // the previous step's dK and dQ must be done with dS
-      if (n > 0 && !mbar_wait_warp(&bars->ds_free, (n - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
-      // dS: half wg of the tile, key row r, chunk c of 8 queries at (c ^ (r & 7))
-#pragma unroll
-      for (int q8 = 0; q8 < 4; ++q8) {
-        *reinterpret_cast<uint4 *>(ds_row + ((q8 ^ (r & 7)) << 4)) =
-            make_uint4(pd0[4 * q8], pd0[4 * q8 + 1], pd0[4 * q8 + 2], pd0[4 * q8 + 3]);
-        *reinterpret_cast<uint4 *>(ds_row + (((4 + q8) ^ (r & 7)) << 4)) =
-            make_uint4(pd1[4 * q8], pd1[4 * q8 + 1], pd1[4 * q8 + 2], pd1[4 * q8 + 3]);
-      }
+      // the dS stores above become visible to the tensor core's operand reads
       fence_proxy_async_smem();
       if (lane == 0 && (warp == 4 || warp == 8)) GQA_TRACE_EVENT(1, warp == 4 ? 11 : 7, n);
       mbar_arrive(&bars->ds_ready);
@@ -622,28 +637,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       reg_fence(a1);
       tc_fence_before_sync();
       mbar_arrive(&bars->dq_free);
-      // the staging buffer was last read by the previous step's reduce
-      if (leader) bulk_wait_group_read<0>();
-      if (leader) GQA_TRACE_EVENT(1, 13, n);
-      named_bar_sync(1, 128);
-      // two boxes [128 rows][32 fp32], 128-byte swizzle: 16-B chunk c of row r at c ^ (r & 7)
+      // Two passes through the 16 KB staging box, 32 fp32 columns each: [128
+      // rows][32 fp32] with the 128-byte swizzle (16-B chunk c of row r at
+      // c ^ (r & 7)), then a TMA reduce-add into the fp32 dQ accumulator.
+      const bool do_reduce = GQA_CHECK(p.status, h < p.H && qb * BQ < p.S);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        *reinterpret_cast<uint4 *>(stg + ((c ^ (r & 7)) << 4)) =
-            make_uint4(a0[4 * c], a0[4 * c + 1], a0[4 * c + 2], a0[4 * c + 3]);
-        *reinterpret_cast<uint4 *>(stg + TILE_BYTES + ((c ^ (r & 7)) << 4)) =
-            make_uint4(a1[4 * c], a1[4 * c + 1], a1[4 * c + 2], a1[4 * c + 3]);
+      for (int half = 0; half < 2; ++half) {
+        const uint32_t *a = half == 0 ? a0 : a1;
+        // the staging box was last read by the previous pass's reduce
+        if (leader) bulk_wait_group_read<0>();
+        if (leader && half == 0) GQA_TRACE_EVENT(1, 13, n);
+        named_bar_sync(1, 128);
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4 *>(stg + ((c ^ (r & 7)) << 4)) =
+              make_uint4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (leader && do_reduce) {
+          tma_reduce_add_3d(&tm_dq, smem + SM_DQ, 32 * half, qb * BQ, b * p.H + h);
+          bulk_commit_group();
+        }
       }
-      fence_proxy_async_smem();
-      named_bar_sync(1, 128);
-      if (leader && GQA_CHECK(p.status, h < p.H && qb * BQ < p.S)) {
-        const int bh = b * p.H + h;
-        uint8_t *box = smem + SM_DQ;
-        tma_reduce_add_3d(&tm_dq, box, 0, qb * BQ, bh);
-        tma_reduce_add_3d(&tm_dq, box + TILE_BYTES, 32, qb * BQ, bh);
-        bulk_commit_group();
-        GQA_TRACE_EVENT(1, 14, n);
-      }
+      if (leader) GQA_TRACE_EVENT(1, 14, n);
     }
     if (leader) bulk_wait_group_all();
   }
