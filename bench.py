@@ -38,7 +38,9 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd/bwd TFLOPS (causal FLOPs) and % of B300 BF16 tensor peak"
-KERNEL_NAMES = ["gqa_fwd_kernel", "bwd_prep_kernel", "bwd_main_kernel", "bwd_dq_convert_kernel"]
+KERNEL_NAMES = ["gqa_fwd_kernel", "bwd_prep_kernel", "bwd_main_kernel", "bwd_dq_convert_kernel",
+                "fwd_knorm_kernel"]
+N_KERNELS = len(KERNEL_NAMES)
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -197,16 +199,18 @@ def run_ours(args, w, rank, world, local_rank):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws_bytes = gq.gqa_attn_bwd_workspace_size(B, H, G, S, d)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    fws_bytes = gq.gqa_attn_fwd_workspace_size(B, H, G, S, d)
+    fws = torch.empty(max(fws_bytes, 16), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step_on(ins, outs, strm):
         q_, k_, v_, do_ = ins
         o_, lse_, dq_, dk_, dv_ = outs
-        rc = gq.gqa_attn_fwd(q_, k_, v_, o_, lse_, B, H, G, S, d, w.causal, w.window, w.n_sink,
-                             w.scale, strm)
+        rc = gq.gqa_attn_fwd_ws(q_, k_, v_, o_, lse_, B, H, G, S, d, w.causal, w.window,
+                                w.n_sink, w.scale, fws, fws_bytes, strm)
         if rc != gq.GQA_OK:
-            raise gq.GqaError(rc, "gqa_attn_fwd")
+            raise gq.GqaError(rc, "gqa_attn_fwd_ws")
         if with_bwd:
             rc = gq.gqa_attn_bwd(q_, k_, v_, o_, do_, lse_, dq_, dk_, dv_, B, H, G, S, d,
                                  w.causal, w.window, w.n_sink, w.scale, ws, ws_bytes, strm)
@@ -216,7 +220,7 @@ def run_ours(args, w, rank, world, local_rank):
     def step():
         step_on((q, k, v, do), (o, lse, dq, dk, dv), stream)
 
-    launches_per_step = 1 + (3 if with_bwd else 0)
+    launches_per_step = 2 + (3 if with_bwd else 0)  # key norms + forward, prep + main + convert
     for _ in range(args.warmup):
         flush.zero_()
         step()
@@ -227,7 +231,7 @@ def run_ours(args, w, rank, world, local_rank):
     # ---- timed region: per-step events, kernel events from the library hooks
     gq.gqa_attn_timing_enable(1)
     kms = gq.timing_buffer()
-    kernel_ms = [[] for _ in range(4)]
+    kernel_ms = [[] for _ in range(N_KERNELS)]
     step_ms = []
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
@@ -240,7 +244,7 @@ def run_ours(args, w, rank, world, local_rank):
             step()
             ev[s_i][1].record(stream)
             gq.gqa_attn_timing_collect(kms)
-            for kid in range(4):
+            for kid in range(N_KERNELS):
                 if kms[kid] >= 0:
                     kernel_ms[kid].append(float(kms[kid]))
         torch.cuda.synchronize()
@@ -259,7 +263,7 @@ def run_ours(args, w, rank, world, local_rank):
 
     # ---- dominant kernel roofline
     tot = [sum(x) for x in kernel_ms]
-    dom = max(range(4), key=lambda kid: tot[kid])
+    dom = max(range(N_KERNELS), key=lambda kid: tot[kid])
     dom_avg_ms = tot[dom] / max(1, len(kernel_ms[dom]))
     dom_flops = {0: fwd_f, 2: bwd_f}.get(dom)
     if dom_flops:
@@ -278,7 +282,7 @@ def run_ours(args, w, rank, world, local_rank):
                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                     "traffic": None, "kernel": KERNEL_NAMES[dom]}
     kernels = {KERNEL_NAMES[kid]: round(tot[kid] / max(1, len(kernel_ms[kid])) * 1e3, 1)
-               for kid in range(4) if kernel_ms[kid]}
+               for kid in range(N_KERNELS) if kernel_ms[kid]}
 
     # ---- end to end through the same calls, host buffers
     e2e = run_e2e(args, dev, with_bwd, dev_in=(q, k, v, do), dev_out=(o, lse, dq, dk, dv),
@@ -296,7 +300,8 @@ def run_ours(args, w, rank, world, local_rank):
                    "l2": "flushed before every timed step (256 MB write, outside the events)",
                    "parallelism": f"replicas over ranks ({world}), no collective"},
         "pct_of_peak": round(100 * value / world / peaks["bf16_tflops"], 2),
-        "fwd_tflops": round(fwd_f / (kernels_ms_avg(kernel_ms, 0) * 1e-3) / 1e12, 2)
+        "fwd_tflops": round(fwd_f / (sum(kernels_ms_avg(kernel_ms, k) for k in (0, 4)) * 1e-3)
+                            / 1e12, 2)
         if kernel_ms[0] else None,
         "bwd_tflops": round(bwd_f / (sum(kernels_ms_avg(kernel_ms, k) for k in (1, 2, 3)) * 1e-3)
                             / 1e12, 2) if with_bwd and kernel_ms[2] else None,

@@ -8,6 +8,9 @@ library is missing or cannot be loaded, every call raises.
 
 Low-level calls (same names and argument order as the C header):
     gqa_attn_fwd(q, k, v, o, lse, B, H, G, S, d, causal, window, n_sink, scale, stream)
+    gqa_attn_fwd_ws(q, k, v, o, lse, B, H, G, S, d, causal, window, n_sink, scale,
+                    workspace, workspace_bytes, stream)   (score-bound forward)
+    gqa_attn_fwd_workspace_size(B, H, G, S, d)
     gqa_attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, G, S, d, causal, window,
                  n_sink, scale, workspace, workspace_bytes, stream)
     gqa_attn_bwd_workspace_size(B, H, G, S, d)
@@ -24,12 +27,14 @@ from ._lib import (GQA_ERR_ALIGN, GQA_ERR_CUDA, GQA_ERR_DEVICE_TIMEOUT, GQA_ERR_
                    GQA_ERR_SHAPE, GQA_ERR_TOO_LARGE,
                    GQA_ERR_WORKSPACE, GQA_NOALLOC_SCRATCH_BYTES, GQA_OK, GqaError, bwd, fwd,
                    gqa_attn_bwd, gqa_attn_bwd_noalloc,
-                   gqa_attn_bwd_workspace_size, gqa_attn_fwd, gqa_attn_last_device_status,
+                   gqa_attn_bwd_workspace_size, gqa_attn_fwd, gqa_attn_fwd_workspace_size,
+                   gqa_attn_fwd_ws, gqa_attn_last_device_status,
                    gqa_attn_last_error_detail, gqa_attn_selftest_timeout, gqa_attn_strerror, gqa_attn_timing_collect, gqa_attn_timing_enable,
                    lib_path, load_library, selftest_timeout, timing_buffer)
 
 __all__ = [
-    "fwd", "bwd", "gqa_attn_fwd", "gqa_attn_bwd", "gqa_attn_bwd_noalloc",
+    "fwd", "bwd", "gqa_attn_fwd", "gqa_attn_fwd_ws", "gqa_attn_fwd_workspace_size",
+    "gqa_attn_bwd", "gqa_attn_bwd_noalloc",
     "gqa_attn_bwd_workspace_size", "GQA_ERR_TOO_LARGE", "GQA_ERR_DEVICE_BOUNDS", "GQA_NOALLOC_SCRATCH_BYTES",
     "gqa_attn_strerror", "gqa_attn_last_error_detail", "gqa_attn_last_device_status",
     "gqa_attn_selftest_timeout", "selftest_timeout", "gqa_attn_timing_enable",

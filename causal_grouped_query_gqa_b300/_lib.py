@@ -54,6 +54,10 @@ def load_library():
         vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.gqa_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp]
         lib.gqa_attn_fwd.restype = i
+        lib.gqa_attn_fwd_ws.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp, sz, vp]
+        lib.gqa_attn_fwd_ws.restype = i
+        lib.gqa_attn_fwd_workspace_size.argtypes = [i, i, i, i, i]
+        lib.gqa_attn_fwd_workspace_size.restype = sz
         lib.gqa_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                      i, i, i, i, i, i, i, i, f, vp, sz, vp]
         lib.gqa_attn_bwd.restype = i
@@ -106,6 +110,17 @@ def gqa_attn_fwd(q, k, v, o, lse, B, H, G, S, d, causal, window, n_sink, scale, 
                                        _stream(stream))
 
 
+def gqa_attn_fwd_ws(q, k, v, o, lse, B, H, G, S, d, causal, window, n_sink, scale, workspace,
+                    workspace_bytes, stream=None):
+    return load_library().gqa_attn_fwd_ws(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, G, S, d,
+                                          int(causal), int(window), int(n_sink), float(scale),
+                                          _p(workspace), int(workspace_bytes), _stream(stream))
+
+
+def gqa_attn_fwd_workspace_size(B, H, G, S, d):
+    return load_library().gqa_attn_fwd_workspace_size(B, H, G, S, d)
+
+
 def gqa_attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, G, S, d, causal, window, n_sink,
                  scale, workspace, workspace_bytes, stream=None):
     return load_library().gqa_attn_bwd(_p(q), _p(k), _p(v), _p(o), _p(dout), _p(lse), _p(dq),
@@ -153,7 +168,7 @@ def selftest_timeout(budget_ms: int = 20, stream=None):
     return rc, [int(x) for x in el], [int(x) for x in ok]
 
 
-GQA_KERNEL_COUNT = 4  # fwd, bwd prep, bwd main, bwd dq convert
+GQA_KERNEL_COUNT = 5  # fwd, bwd prep, bwd main, bwd dq convert, fwd key norms
 
 
 def gqa_attn_timing_enable(on: bool) -> int:
@@ -185,8 +200,9 @@ def _check(t, shape, dtype, name):
 
 
 def fwd(q, k, v, *, causal=True, window=0, n_sink=0, scale=None, out=None, lse=None,
-        stream=None):
-    """o, lse = fwd(q [B,H,S,64] bf16, k/v [B,G,S,64] bf16) on the current CUDA stream."""
+        workspace=None, stream=None):
+    """o, lse = fwd(q [B,H,S,64] bf16, k/v [B,G,S,64] bf16) on the current CUDA stream
+    (gqa_attn_fwd_ws; `workspace` is allocated when not given)."""
     import torch
     B, H, S, d = q.shape
     G = k.shape[1]
@@ -196,9 +212,13 @@ def fwd(q, k, v, *, causal=True, window=0, n_sink=0, scale=None, out=None, lse=N
     scale = 1.0 / d ** 0.5 if scale is None else scale
     o = torch.empty_like(q) if out is None else out
     l = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if lse is None else lse
-    rc = gqa_attn_fwd(q, k, v, o, l, B, H, G, S, d, causal, window, n_sink, scale, stream)
+    need = gqa_attn_fwd_workspace_size(B, H, G, S, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    rc = gqa_attn_fwd_ws(q, k, v, o, l, B, H, G, S, d, causal, window, n_sink, scale, workspace,
+                         workspace.numel() * workspace.element_size(), stream)
     if rc != GQA_OK:
-        raise GqaError(rc, "gqa_attn_fwd")
+        raise GqaError(rc, "gqa_attn_fwd_ws")
     return o, l
 
 

@@ -45,6 +45,8 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
+#include <type_traits>
+
 #include "device_checks.cuh"
 #include "sm100_ptx.cuh"
 #include "trace.cuh"
@@ -69,6 +71,18 @@ constexpr uint32_t TMEM_COLS = 512;
 // (base-2 units), so P stays below 2^8 and O is rescaled only rarely; the
 // result is exact because O and l are normalised with the same running max.
 constexpr float kRescaleThreshold = 8.0f;
+// Score bound (gqa_attn_fwd_ws only): |s_ij| * scale * log2(e) <= U_i =
+// |q_i| * max_j |k_j| * scale * log2(e) (Cauchy-Schwarz), with max_j |k_j|^2 over
+// the kv head from fwd_knorm_kernel.  A warp whose rows all have U_i <=
+// kBoundMax runs the whole unit against the fixed reference m_i = U_i -
+// kFastSlack and takes no row maxima: every term 2^(s * sl2 - m_i) lies in
+// [2^(kFastSlack - 2 U_i), 2^kFastSlack], so none overflows and the largest of
+// a row stays above 2^(kFastSlack - 2 kBoundMax) = 2^-96; the result is the same
+// softmax, normalised by the same reference in O and l.
+constexpr float kFastSlack = 32.0f;
+constexpr float kBoundMax = 64.0f;
+constexpr int kKnParts = 4;  // partial maxima of |k_j|^2 per kv head: one 16-byte record
+static_assert(kKnParts == 4, "score_bound reads a record of four partial maxima");
 __device__ __forceinline__ uint32_t col_s(int t) { return static_cast<uint32_t>(t) * 128u; }
 __device__ __forceinline__ uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(t) * 64u; }
 __device__ __forceinline__ uint32_t col_p(int t) { return 384u + static_cast<uint32_t>(t) * 64u; }
@@ -79,7 +93,8 @@ constexpr int SM_V = SM_K + NSTAGE * TILE_BYTES;
 constexpr int SM_BARS = SM_V + NSTAGE * TILE_BYTES;
 
 struct Bars {
-  uint64_t q_full;     // the unit's Q tiles landed (TMA transaction bytes)
+  alignas(16) float kn[2][kKnParts];  // the unit's |k_j|^2 record (units alternate slots)
+  uint64_t q_full;     // the unit's Q tiles (and |k|^2 record) landed (TMA transaction bytes)
   uint64_t q_empty;    // every Q K^T of the unit finished: Q may be reloaded
   uint64_t kv_full[NSTAGE];   // K and V tile landed (TMA transaction bytes)
   uint64_t kv_empty[NSTAGE];  // every head's products with the tile finished (the
@@ -107,6 +122,7 @@ struct Params {
   int n_qblocks;
   int n_pairs;  // ceil(R / 2) head pairs per kv head
   int n_units;  // n_qblocks * B * G * n_pairs
+  const float *kn2;  // [B*G][kKnParts] partial maxima of |k_j|^2, or null (no score bound)
   __nv_bfloat16 *o;
   float *lse;
   int *status;
@@ -187,6 +203,31 @@ __device__ __forceinline__ Unit unit_of(int u, const Params &p) {
   return un;
 }
 
+__device__ __forceinline__ int kvz_of(const Unit &un, const Params &p) { return un.b * p.G + un.g; }
+
+// U_i of the score bound, in base-2 units: sqrt(|q_i|^2 * max_j |k_j|^2) * sl2,
+// widened by 2^-10 relative and absolute for the rounding of the norms and of
+// the MMA's fp32 sums.  qrow: row r of a Q tile in shared memory (128-byte
+// swizzle: 16-byte chunk c at c ^ (r & 7), read in that order so that the
+// eight rows r..r+7 of a load hit eight different chunks of the banks).
+__device__ __forceinline__ float score_bound(const uint8_t *qrow, int r, const float *kn, float sl2) {
+  uint64_t acc = 0ull;  // fp32 pair (0.0f bits)
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint4 w = *reinterpret_cast<const uint4 *>(qrow + ((c ^ (r & 7)) << 4));
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint64_t x = f32x2(__uint_as_float(ws[e] << 16), __uint_as_float(ws[e] & 0xffff0000u));
+      acc = fma_f32x2(x, x, acc);
+    }
+  }
+  float qa, qb;
+  f32x2_split(acc, qa, qb);
+  const float kmax2 = fmaxf(fmaxf(kn[0], kn[1]), fmaxf(kn[2], kn[3]));
+  return sqrtf((qa + qb) * kmax2) * sl2 * (1.f + 0x1p-10f) + 0x1p-10f;
+}
+
 // The k-th unit of this CTA, or -1 when none is left.  Rounds of gridDim.x
 // units alternate direction (CTA c takes unit c of even rounds and unit
 // grid - 1 - c of odd ones): unit sizes shrink along the heaviest-first list,
@@ -263,8 +304,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int qrow = un.qb * BM, qz = un.b * p.H + un.h0;
         GQA_REPORT(p.status, un.qb >= 0 && un.qb < p.n_qblocks && kr.count >= 1 &&
                                 qz + (un.two ? 1 : 0) < p.B * p.H);
-        mbar_arrive_expect_tx(&bars->q_full, (un.two ? 2 : 1) * TILE_BYTES);
+        mbar_arrive_expect_tx(&bars->q_full,
+                              (un.two ? 2 : 1) * TILE_BYTES + (p.kn2 ? kKnParts * 4 : 0));
         tma_load_3d(smem + SM_Q, &tm_q, &bars->q_full, 0, qrow, qz);
+        if (p.kn2)  // the kv head's |k|^2 record, for the softmax's score bound
+          bulk_load(&bars->kn[k & 1][0], p.kn2 + static_cast<size_t>(kvz_of(un, p)) * kKnParts,
+                    kKnParts * 4, &bars->q_full);
         if (un.two) tma_load_3d(smem + SM_Q + TILE_BYTES, &tm_q, &bars->q_full, 0, qrow, qz + 1);
         q_loads = k + 1;
         const int kvz = un.b * p.G + un.g;
@@ -428,11 +473,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
       float m_run = -CUDART_INF_F;  // running max of scaled scores, base-2 units
       float l_run = 0.f;            // running sum of 2^(s - m_run)
-      for (int it = 0; it < n; ++it, ++ts) {
+      // Score bound (kBoundMax): decided per warp before the unit's first tile.
+      // Units of one key tile keep the exact step: their Q may be reloaded as
+      // soon as their only Q K^T is done, before this read could happen.
+      bool fast = false;
+      if (p.kn2 != nullptr && n >= 2) {
+        // Q and the record landed with q_full (phase k); they stay until every
+        // Q K^T of the unit is done, and the last one (tile n - 1 >= 1) waits
+        // for this thread's release of S of tile n - 2 >= 0.
+        if (!mbar_wait(&bars->q_full, k & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        const float bound = score_bound(smem + SM_Q + t * TILE_BYTES + r * 128, r, &bars->kn[k & 1][0], sl2);
+        fast = __all_sync(0xffffffffu, bound <= kBoundMax);
+        if (fast) m_run = bound - kFastSlack;
+      }
+      // One key tile of the unit.  kFast: the warp runs against the score
+      // bound's fixed reference and takes no row maxima.  Two instantiations,
+      // chosen once per unit, so the steady-state loop carries no max code.
+      // Returns false on abort.
+      int it = 0;
+      auto tile = [&](auto fast_tag) -> bool {
+        constexpr bool kFast = decltype(fast_tag)::value;
         const int kb = kr.tile(it);
         const int step = k == 0 ? it : kTraceSteps;  // trace the first unit only
         (void)step;
-        if (!mbar_wait(&bars->s_full[t], ts & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        if (!mbar_wait(&bars->s_full[t], ts & 1, ab, p.status, kTimeoutCode)) return false;
         if (lane == 0 && (warp == 4 || warp == 8)) GQA_TRACE_EVENT(0, warp == 4 ? 6 : 10, step);
         tc_fence_after_sync();
         uint32_t s0[32], s1[32], s2[32], s3[32];
@@ -473,22 +537,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           for (int c = 0; c < BN; ++c) s[c] = ((vb[c >> 5] >> (c & 31)) & 1u) ? s[c] : -CUDART_INF_F;
         }
         // row max: 4 independent chains of 3-input max over elements 8..127,
-        // seeded with elements 0..7
-        float mx4[4];
+        // seeded with elements 0..7 (not needed against a bound's reference)
+        bool need = false;  // O and l are rescaled by alpha
+        float m_new = m_run, alpha = 1.f;
+        if constexpr (!kFast) {
+          float mx4[4];
 #pragma unroll
-        for (int a = 0; a < 4; ++a) mx4[a] = fmaxf(s[2 * a], s[2 * a + 1]);
+          for (int a = 0; a < 4; ++a) mx4[a] = fmaxf(s[2 * a], s[2 * a + 1]);
 #pragma unroll
-        for (int c = 8; c < BN; c += 8) {
+          for (int c = 8; c < BN; c += 8) {
 #pragma unroll
-          for (int a = 0; a < 4; ++a) mx4[a] = max3f(mx4[a], s[c + 2 * a], s[c + 2 * a + 1]);
+            for (int a = 0; a < 4; ++a) mx4[a] = max3f(mx4[a], s[c + 2 * a], s[c + 2 * a + 1]);
+          }
+          const float mx = fmaxf(max3f(mx4[0], mx4[1], mx4[2]), mx4[3]);
+          const float m_tile = mx * sl2;
+          // lazy rescale: keep the running max unless this tile exceeds it by > threshold
+          need = m_tile > m_run + kRescaleThreshold;
+          m_new = need ? m_tile : m_run;
         }
-        const float mx = fmaxf(max3f(mx4[0], mx4[1], mx4[2]), mx4[3]);
-        const float m_tile = mx * sl2;
-        // lazy rescale: keep the running max unless this tile exceeds it by > threshold
-        const bool need = m_tile > m_run + kRescaleThreshold;
-        const float m_new = need ? m_tile : m_run;
         const float m_use = (m_new == -CUDART_INF_F) ? 0.f : m_new;
-        const float alpha = need ? ex2_approx(m_run - m_use) : 1.f;
+        if constexpr (!kFast) alpha = need ? ex2_approx(m_run - m_use) : 1.f;
         const uint64_t negm = f32x2(-m_use, -m_use);
         if (lane == 0 && warp == 4) GQA_TRACE_EVENT(0, 16, step);
         // Ping-pong: the two heads take turns on the exp2 section (MUFU-bound), so
@@ -497,7 +565,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (un.two) {
           const bool wait_turn = (t == 1) || tt > 0;
           const uint32_t par = t == 0 ? ((tt - 1) & 1) : (tt & 1);
-          if (wait_turn && !mbar_wait(&bars->turn[t], par, ab, p.status, kTimeoutCode)) { ok = false; break; }
+          if (wait_turn && !mbar_wait(&bars->turn[t], par, ab, p.status, kTimeoutCode)) return false;
         }
         if (lane == 0 && warp == 4) GQA_TRACE_EVENT(0, 17, step);
         uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};  // four chains of fp32 pairs (0.0f bits)
@@ -525,9 +593,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // and O_t rescaled.  (Before a unit's first tile the previous unit's
         // epilogue already waited for all of its products.)
         if (it > 0) {
-          if (!mbar_wait(&bars->o_done[t], (ts - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+          if (!mbar_wait(&bars->o_done[t], (ts - 1) & 1, ab, p.status, kTimeoutCode)) return false;
           tc_fence_after_sync();
-          if (__any_sync(0xffffffffu, need)) {
+          if (!kFast && __any_sync(0xffffffffu, need)) {
             uint32_t o0[32], o1[32];
             tmem_ld_32x32b_x32(t_o + 0, o0);
             tmem_ld_32x32b_x32(t_o + 32, o1);
@@ -565,6 +633,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_arrive(&bars->p_full[t]);
         l_run = l_run * alpha + sum;
         m_run = m_new;
+        return true;
+      };
+      if (fast) {
+        for (; ok && it < n; ++it, ++ts) ok = tile(std::true_type{});
+      } else {
+        for (; ok && it < n; ++it, ++ts) ok = tile(std::false_type{});
       }
       if (!ok) break;
       // ---- epilogue of the unit: O_t / l -> bf16, LSE
@@ -617,6 +691,52 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (warp == 2) {
     tc_fence_after_sync();
     tmem_dealloc(tbase, TMEM_COLS);
+  }
+}
+
+// Pre-pass of the score bound: for each kv head bg = b * G + g,
+// kn2[bg * kKnParts + part] = max |k_j|^2 over the keys of slice `part` of
+// [0, S) (fp32 sums of the squared bf16 elements; 0 for an empty slice).  One
+// CTA per (kv head, slice); 8 lanes per key row (16 bytes each), four rows per
+// warp and step.  fmaxf drops NaN rows (their scores are NaN whatever the
+// reference); an infinite row gives an infinite bound, hence the exact step.
+constexpr int kKnormThreads = 256;
+__global__ void __launch_bounds__(kKnormThreads)
+    fwd_knorm_kernel(const __nv_bfloat16 *k, int S, float *kn2) {
+  const int bg = blockIdx.x / kKnParts, part = blockIdx.x % kKnParts;
+  const int per = (S + kKnParts - 1) / kKnParts;
+  const int r0 = part * per, r1 = min(S, r0 + per);
+  const uint4 *rows = reinterpret_cast<const uint4 *>(k + static_cast<size_t>(bg) * S * HD);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float m = 0.f;
+  // the loop bound is uniform in the warp, so every lane reaches the shuffles
+  for (int rb = r0 + 4 * warp; rb < r1; rb += 4 * (kKnormThreads / 32)) {
+    const int row = rb + (lane >> 3);
+    float sq = 0.f;
+    if (row < r1) {
+      const uint4 w = __ldg(rows + static_cast<size_t>(row) * (HD / 8) + (lane & 7));
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float lo = __uint_as_float(ws[e] << 16), hi = __uint_as_float(ws[e] & 0xffff0000u);
+        sq = fmaf(lo, lo, fmaf(hi, hi, sq));
+      }
+    }
+    sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+    sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+    sq += __shfl_xor_sync(0xffffffffu, sq, 4);
+    m = fmaxf(m, sq);
+  }
+#pragma unroll
+  for (int o = 8; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __shared__ float wmax[kKnormThreads / 32];
+  if (lane == 0) wmax[warp] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float b = wmax[0];
+#pragma unroll
+    for (int w = 1; w < kKnormThreads / 32; ++w) b = fmaxf(b, wmax[w]);
+    kn2[blockIdx.x] = b;
   }
 }
 

@@ -158,16 +158,16 @@ const char *gqa_attn_strerror(int status) {
   }
 }
 
-int gqa_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
-                 int G, int S, int d, int causal, int window, int n_sink, float scale,
-                 void *stream) {
-  int rc = check_common(B, H, G, S, d, causal, window, n_sink, scale);
-  if (rc != GQA_OK) return rc;
-  if (!q || !k || !v || !o || !lse) return GQA_ERR_NULL;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
-    return GQA_ERR_ALIGN;
+namespace {
+
+// The forward launch shared by both entry points; kn2 (the score-bound record
+// that fwd_knorm_kernel writes first, on the same stream) may be null.
+int launch_forward(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                   int G, int S, int causal, int window, int n_sink, float scale, float *kn2,
+                   cudaStream_t st) {
   DeviceState *ds = nullptr;
-  if ((rc = device_state(&ds)) != GQA_OK) return rc;
+  int rc = device_state(&ds);
+  if (rc != GQA_OK) return rc;
 
   using namespace gqa::fwd;
   CUtensorMap tq, tk, tv;
@@ -188,6 +188,7 @@ int gqa_attn_fwd(const void *q, const void *k, const void *v, void *o, float *ls
   p.scale_log2 = scale * 1.4426950408889634f;
   p.n_qblocks = (S + BM - 1) / BM;
   p.n_pairs = (p.R + 1) / 2;
+  p.kn2 = kn2;
   p.o = static_cast<__nv_bfloat16 *>(o);
   p.lse = lse;
   p.status = ds->status;
@@ -197,12 +198,54 @@ int gqa_attn_fwd(const void *q, const void *k, const void *v, void *o, float *ls
   // persistent grid: one CTA per SM (the kernel's shared memory and TMEM allow one)
   const int grid = static_cast<int>(units < ds->sm_count ? units : ds->sm_count);
 
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (kn2) {
+    const long long blocks = static_cast<long long>(B) * G * kKnParts;
+    if (blocks > 0x7fffffffLL) return GQA_ERR_SHAPE;
+    gqa::timing_begin(GQA_KERNEL_FWD_KNORM, st);
+    fwd_knorm_kernel<<<static_cast<unsigned>(blocks), kKnormThreads, 0, st>>>(
+        static_cast<const __nv_bfloat16 *>(k), S, kn2);
+    gqa::timing_end(GQA_KERNEL_FWD_KNORM, st);
+    if (gqa::cuda_failed(cudaGetLastError(), "launch of the forward's key-norm kernel"))
+      return GQA_ERR_CUDA;
+  }
   gqa::timing_begin(GQA_KERNEL_FWD, st);
   gqa_fwd_kernel<<<static_cast<unsigned>(grid), NTHREADS, SMEM_BYTES, st>>>(tq, tk, tv, p);
   gqa::timing_end(GQA_KERNEL_FWD, st);
   return gqa::cuda_failed(cudaGetLastError(), "launch of the forward kernel") ? GQA_ERR_CUDA
                                                                                : GQA_OK;
+}
+
+}  // namespace
+
+int gqa_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                 int G, int S, int d, int causal, int window, int n_sink, float scale,
+                 void *stream) {
+  int rc = check_common(B, H, G, S, d, causal, window, n_sink, scale);
+  if (rc != GQA_OK) return rc;
+  if (!q || !k || !v || !o || !lse) return GQA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return GQA_ERR_ALIGN;
+  return launch_forward(q, k, v, o, lse, B, H, G, S, causal, window, n_sink, scale, nullptr,
+                        static_cast<cudaStream_t>(stream));
+}
+
+size_t gqa_attn_fwd_workspace_size(int B, int H, int G, int S, int d) {
+  if (check_common(B, H, G, S, d, 1, 0, 0, 1.f) != GQA_OK) return 0;
+  return static_cast<size_t>(B) * G * gqa::fwd::kKnParts * sizeof(float);
+}
+
+int gqa_attn_fwd_ws(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                    int G, int S, int d, int causal, int window, int n_sink, float scale,
+                    void *workspace, size_t workspace_bytes, void *stream) {
+  int rc = check_common(B, H, G, S, d, causal, window, n_sink, scale);
+  if (rc != GQA_OK) return rc;
+  if (!q || !k || !v || !o || !lse || !workspace) return GQA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(workspace))
+    return GQA_ERR_ALIGN;
+  if (workspace_bytes < gqa_attn_fwd_workspace_size(B, H, G, S, d)) return GQA_ERR_WORKSPACE;
+  return launch_forward(q, k, v, o, lse, B, H, G, S, causal, window, n_sink, scale,
+                        static_cast<float *>(workspace), static_cast<cudaStream_t>(stream));
 }
 
 size_t gqa_attn_bwd_workspace_size(int B, int H, int G, int S, int d) {

@@ -7,7 +7,7 @@
 
 namespace gqa {
 
-constexpr int kNumKernelIds = 4;  // fwd, bwd prep, bwd main, bwd dq convert
+constexpr int kNumKernelIds = 5;  // fwd, bwd prep, bwd main, bwd dq convert, fwd key norms
 
 struct TimingState {
   bool on = false;

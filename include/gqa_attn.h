@@ -80,6 +80,33 @@ GQA_API int gqa_attn_fwd(const void *q, const void *k, const void *v, void *o, f
                  int causal, int window, int n_sink, float scale, void *stream);
 
 /*
+ * Bytes of scratch that gqa_attn_fwd_ws needs: B * G records of 4 fp32 partial
+ * maxima of |k_j|^2 (16 bytes per kv head).  Returns 0 for invalid sizes.
+ */
+GQA_API size_t gqa_attn_fwd_workspace_size(int B, int H, int G, int S, int d);
+
+/*
+ * Forward with a score bound: the result contract of gqa_attn_fwd (the same
+ * definition in the same precision), in two launches on `stream`.  A first
+ * kernel writes into `workspace` the largest squared norm of each kv head's key
+ * rows.  Every scaled score of query row i is at most
+ * U_i = |q_i| * max_j |k_j| * scale * log2(e) in magnitude (Cauchy-Schwarz, base-2
+ * units); a warp whose 32 rows all have U_i <= 64 computes its whole unit of key
+ * tiles against the fixed reference U_i - 32 instead of a running row maximum
+ * (every term 2^(s - reference) then lies in [2^-96, 2^32]), and rows with
+ * larger bounds keep the online maximum of "SnapKitty Transformer 8B",
+ * section "FlashAttention Inference".  The bound is this library's.
+ * workspace: device memory of at least gqa_attn_fwd_workspace_size() bytes,
+ * 16-byte aligned, owned by the caller and not used by any other call running
+ * at the same time.  Errors: as gqa_attn_fwd, plus GQA_ERR_NULL for a null
+ * workspace and GQA_ERR_WORKSPACE for a short one.
+ */
+GQA_API int gqa_attn_fwd_ws(const void *q, const void *k, const void *v, void *o, float *lse,
+                    int B, int H, int G, int S, int d,
+                    int causal, int window, int n_sink, float scale,
+                    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Bytes of scratch that gqa_attn_bwd needs for these sizes: an fp32 dq
  * accumulator [B][H][S][d], then two fp32 row arrays [B][H][S_pad] with
  * S_pad = S rounded up to a multiple of 128: lse * log2(e) and the row term
@@ -190,7 +217,8 @@ typedef enum {
     GQA_KERNEL_BWD_PREP = 1,  /* backward: D = rowsum(dout * o), dq accumulator cleared */
     GQA_KERNEL_BWD_MAIN = 2,  /* backward: dk, dv and the dq accumulation */
     GQA_KERNEL_BWD_DQ = 3,    /* backward: dq accumulator -> bf16 dq */
-    GQA_KERNEL_COUNT = 4
+    GQA_KERNEL_FWD_KNORM = 4, /* gqa_attn_fwd_ws: key-norm maxima for the score bound */
+    GQA_KERNEL_COUNT = 5
 } gqa_kernel_id;
 
 GQA_API int gqa_attn_timing_enable(int on);

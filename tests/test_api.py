@@ -30,7 +30,8 @@ def _declared_symbols():
 
 def test_library_exports_every_declared_symbol(lib):
     names = _declared_symbols()
-    assert {"gqa_attn_fwd", "gqa_attn_bwd", "gqa_attn_bwd_workspace_size",
+    assert {"gqa_attn_fwd", "gqa_attn_fwd_ws", "gqa_attn_fwd_workspace_size",
+            "gqa_attn_bwd", "gqa_attn_bwd_workspace_size",
             "gqa_attn_strerror", "gqa_attn_last_device_status"} <= names
     raw = ctypes.CDLL(gq.lib_path())
     for n in sorted(names):
@@ -52,6 +53,10 @@ def test_workspace_size(lib):
     assert gq.gqa_attn_bwd_workspace_size(B, H, G, S, 128) == 0
     assert gq.gqa_attn_bwd_workspace_size(1, 3, 2, 10, 64) == 0
     assert gq.gqa_attn_bwd_workspace_size(0, 4, 2, 10, 64) == 0
+    # forward: one 16-byte record (4 fp32 partial maxima of |k|^2) per kv head
+    assert gq.gqa_attn_fwd_workspace_size(B, H, G, S, 64) == B * G * 16
+    assert gq.gqa_attn_fwd_workspace_size(1, 3, 2, 10, 64) == 0
+    assert gq.gqa_attn_fwd_workspace_size(B, H, G, S, 128) == 0
 
 
 FAKE = 0x10000  # a 16-byte-aligned non-null address that is never dereferenced
@@ -66,6 +71,15 @@ def _fwd(**kw):
                            a["stream"])
 
 
+def _fwd_ws(**kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=4, G=2, S=128, d=64,
+             causal=1, window=0, n_sink=0, scale=0.125, ws=FAKE, wsb=1 << 20, stream=0)
+    a.update(kw)
+    return gq.gqa_attn_fwd_ws(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["G"],
+                              a["S"], a["d"], a["causal"], a["window"], a["n_sink"], a["scale"],
+                              a["ws"], a["wsb"], a["stream"])
+
+
 def _bwd(**kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, dout=FAKE, lse=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
              B=1, H=4, G=2, S=128, d=64, causal=1, window=0, n_sink=0, scale=0.125,
@@ -76,7 +90,7 @@ def _bwd(**kw):
                            a["window"], a["n_sink"], a["scale"], a["ws"], a["wsb"], a["stream"])
 
 
-@pytest.mark.parametrize("call", [_fwd, _bwd])
+@pytest.mark.parametrize("call", [_fwd, _fwd_ws, _bwd])
 def test_argument_errors(lib, call):
     assert call(B=0) == gq.GQA_ERR_SHAPE
     assert call(S=0) == gq.GQA_ERR_SHAPE
@@ -99,6 +113,13 @@ def test_argument_errors(lib, call):
 def test_fwd_specific_errors(lib):
     assert _fwd(lse=None) == gq.GQA_ERR_NULL
     assert _fwd(o=FAKE + 4) == gq.GQA_ERR_ALIGN
+
+
+def test_fwd_ws_specific_errors(lib):
+    assert _fwd_ws(ws=None) == gq.GQA_ERR_NULL
+    assert _fwd_ws(ws=FAKE + 4) == gq.GQA_ERR_ALIGN
+    assert _fwd_ws(wsb=1 * 2 * 16 - 1) == gq.GQA_ERR_WORKSPACE
+    assert _fwd_ws(lse=None) == gq.GQA_ERR_NULL
 
 
 def test_bwd_specific_errors(lib):

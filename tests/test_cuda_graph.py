@@ -13,8 +13,8 @@ from causal_grouped_query_gqa_b300.inputs import make_inputs
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("noalloc", [False, True])
-def test_graph_replay_matches_eager(noalloc):
+@pytest.mark.parametrize("noalloc,fwd_ws", [(False, False), (True, False), (False, True)])
+def test_graph_replay_matches_eager(noalloc, fwd_ws):
     B, H, G, S, W, NS, d, scale = 1, 8, 2, 1000, 300, 64, 64, 0.125
     q, k, v, do = (t.cuda() for t in make_inputs(B, H, G, S, seed=21, with_grad=True))
     o = torch.empty_like(q)
@@ -22,10 +22,17 @@ def test_graph_replay_matches_eager(noalloc):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = torch.empty(gq.gqa_attn_bwd_workspace_size(B, H, G, S, d), dtype=torch.uint8,
                      device="cuda")
+    fws = torch.empty(gq.gqa_attn_fwd_workspace_size(B, H, G, S, d), dtype=torch.uint8,
+                      device="cuda")
+
+    def forward(q_, k_, v_, o_, lse_, stream):
+        if fwd_ws:  # key-norm pre-pass + score-bound forward
+            return gq.gqa_attn_fwd_ws(q_, k_, v_, o_, lse_, B, H, G, S, d, 1, W, NS, scale, fws,
+                                      fws.numel(), stream)
+        return gq.gqa_attn_fwd(q_, k_, v_, o_, lse_, B, H, G, S, d, 1, W, NS, scale, stream)
 
     def step(stream):
-        assert gq.gqa_attn_fwd(q, k, v, o, lse, B, H, G, S, d, 1, W, NS, scale,
-                               stream) == gq.GQA_OK
+        assert forward(q, k, v, o, lse, stream) == gq.GQA_OK
         if noalloc:
             rc = gq.gqa_attn_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, B, H, G, S, d, 1, W,
                                          NS, scale, stream)
@@ -49,7 +56,8 @@ def test_graph_replay_matches_eager(noalloc):
         torch.cuda.synchronize()
         assert gq.gqa_attn_last_device_status() == gq.GQA_OK
         got = [t.clone() for t in (o, lse, dq, dk, dv)]
-        ro, rl = gq.fwd(q, k, v, window=W, n_sink=NS, scale=scale)
+        ro, rl = torch.empty_like(o), torch.empty_like(lse)
+        assert forward(q, k, v, ro, rl, None) == gq.GQA_OK
         rq, rk, rv = gq.bwd(q, k, v, ro, do, rl, window=W, n_sink=NS, scale=scale)
         torch.cuda.synchronize()
         assert torch.equal(got[0], ro) and torch.equal(got[1], rl)

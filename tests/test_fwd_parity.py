@@ -138,3 +138,104 @@ def test_repeat_is_deterministic():
     o2, l2 = gq.fwd(q, k, v, window=300, n_sink=17)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+# ---------------------------------------------------------------- score bound
+# gq.fwd runs gqa_attn_fwd_ws: a key-norm pre-pass, then the forward kernel in
+# which a warp whose rows' score bounds U_i = |q_i| max_j |k_j| scale log2(e) are
+# all <= 64 runs its unit against the fixed reference U_i - 32 without row
+# maxima.  The tests above therefore cover that path on their inputs; these pin
+# the pre-pass, the plain entry point and the warps that keep the exact step.
+
+def _oracle_check(q, k, v, o, lse, **mask):
+    ro, rl = oracle.attn_fwd(to64(q), to64(k), to64(v), **mask)
+    check_close("O", to64(o), ro)
+    check_close("LSE", to64(lse), rl, max_abs=LSE_ABS, mean_abs=None, bf16_out=False)
+
+
+def test_key_norm_prepass_record():
+    """The workspace holds, per kv head, 4 partial maxima: each the largest
+    |k_j|^2 of its slice of ceil(S / 4) keys (float64 reference from the same
+    bf16 keys)."""
+    B, H, G, S = 2, 8, 4, 777
+    q, k, v = make_inputs(B, H, G, S, seed=5)
+    ws = torch.zeros(gq.gqa_attn_fwd_workspace_size(B, H, G, S, 64), dtype=torch.uint8,
+                     device="cuda")
+    gq.fwd(q.cuda(), k.cuda(), v.cuda(), workspace=ws)
+    torch.cuda.synchronize()
+    rec = ws.view(torch.float32).view(B * G, 4).cpu().numpy().astype(np.float64)
+    ref = (to64(k) ** 2).sum(-1).reshape(B * G, S)
+    per = -(-S // 4)
+    parts = np.array([[ref[bg, p * per:(p + 1) * per].max() for p in range(4)]
+                      for bg in range(B * G)])
+    np.testing.assert_allclose(rec, parts, rtol=1e-5)
+
+
+@pytest.mark.parametrize("window,n_sink", [(0, 0), (200, 33)])
+def test_plain_entry_point(window, n_sink):
+    """gqa_attn_fwd (one launch, the online maximum everywhere) against the
+    oracle and against the score-bound entry point."""
+    B, H, G, S = 2, 4, 2, 700
+    q, k, v = [t.cuda() for t in make_inputs(B, H, G, S, seed=7)]
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device="cuda")
+    assert gq.gqa_attn_fwd(q, k, v, o, lse, B, H, G, S, 64, 1, window, n_sink, 0.125) == gq.GQA_OK
+    o2, l2 = gq.fwd(q, k, v, window=window, n_sink=n_sink)
+    torch.cuda.synchronize()
+    assert gq.gqa_attn_last_device_status() == gq.GQA_OK
+    _oracle_check(q, k, v, o, lse, window=window, n_sink=n_sink)
+    check_close("O(ws vs plain)", to64(o2), to64(o))
+    check_close("LSE(ws vs plain)", to64(l2), to64(lse), max_abs=LSE_ABS, mean_abs=None,
+                bf16_out=False)
+
+
+def test_score_bound_mixed_warps():
+    """Rows 0..31 of every 128-row block have 8x larger queries (bound > 64):
+    those warps keep the exact step while the other warps of the same heads run
+    against the bound's reference."""
+    B, H, G, S = 1, 4, 2, 1100
+    q, k, v = make_inputs(B, H, G, S, seed=11)
+    q[:, :, torch.arange(S) % 128 < 32] *= 8  # exact in bf16
+    o, lse = gq.fwd(q.cuda(), k.cuda(), v.cuda())
+    torch.cuda.synchronize()
+    assert gq.gqa_attn_last_device_status() == gq.GQA_OK
+    _oracle_check(q, k, v, o, lse)
+
+
+@pytest.mark.parametrize("window,n_sink", [(0, 0), (300, 70)])
+def test_score_bound_loose_everywhere(window, n_sink):
+    """One key per kv head with 8x the norm makes every row's bound exceed 64:
+    the whole forward keeps the exact step (large scores, peaked rows)."""
+    B, H, G, S = 1, 4, 2, 900
+    q, k, v = make_inputs(B, H, G, S, seed=13)
+    k[:, :, S // 3] *= 8  # exact in bf16
+    o, lse = gq.fwd(q.cuda(), k.cuda(), v.cuda(), window=window, n_sink=n_sink)
+    torch.cuda.synchronize()
+    assert gq.gqa_attn_last_device_status() == gq.GQA_OK
+    _oracle_check(q, k, v, o, lse, window=window, n_sink=n_sink)
+
+
+def test_score_bound_growing_keys():
+    """Key norms growing 1x..4x along the sequence: bounds near the 64 limit
+    (some warps on each side) and row maxima that keep rising after the first
+    tile, which the fixed reference must absorb."""
+    B, H, G, S = 1, 2, 1, 1024
+    q, k, v = make_inputs(B, H, G, S, seed=17)
+    ramp = 1.0 + 3.0 * torch.arange(S, dtype=torch.float32) / S
+    k = (k.float() * ramp[None, None, :, None]).to(torch.bfloat16)
+    o, lse = gq.fwd(q.cuda(), k.cuda(), v.cuda())
+    torch.cuda.synchronize()
+    assert gq.gqa_attn_last_device_status() == gq.GQA_OK
+    _oracle_check(q, k, v, o, lse)
+
+
+def test_score_bound_tiny_queries():
+    """Queries near zero: the bound is tiny, the reference about -32, and every
+    term close to 2^32 (uniform weights); O is the mean of the visible values."""
+    B, H, G, S = 1, 2, 1, 600
+    q, k, v = make_inputs(B, H, G, S, seed=19)
+    q = (q.float() * 2.0 ** -20).to(torch.bfloat16)
+    o, lse = gq.fwd(q.cuda(), k.cuda(), v.cuda())
+    torch.cuda.synchronize()
+    assert gq.gqa_attn_last_device_status() == gq.GQA_OK
+    _oracle_check(q, k, v, o, lse)
