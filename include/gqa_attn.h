@@ -142,10 +142,9 @@ GQA_API int gqa_attn_bwd(const void *q, const void *k, const void *v, const void
  * the library keeps in device memory; every GPU that loads the library holds
  * that array until the process exits.
  * It is meant for callers that cannot call cudaMalloc (or any allocator) when
- * they run the backward: code whose stream is being captured into a CUDA graph,
- * where a fresh allocation cannot be recorded; plug-ins that run inside a host
- * framework that owns all device memory and hands them no scratch; real-time or
- * latency-critical paths that must never enter the allocator.  The pages have
+ * they run the backward: plug-ins that run inside a host framework that owns all
+ * device memory and hands them no scratch; real-time or latency-critical paths
+ * that must never enter the allocator.  The pages have
  * no counterpart of this call.
  *   - A problem whose scratch (gqa_attn_bwd_workspace_size) exceeds
  *     GQA_NOALLOC_SCRATCH_BYTES is rejected with GQA_ERR_TOO_LARGE before

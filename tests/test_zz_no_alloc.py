@@ -1,8 +1,8 @@
 """gqa_attn_bwd_noalloc: the backward for callers that cannot allocate.
 
 Some callers cannot call cudaMalloc at the moment they run the backward (a
-stream being captured into a CUDA graph, a plug-in inside a framework that owns
-all device memory, a latency-critical path that must not enter the allocator).
+plug-in inside a framework that owns all device memory and hands it no scratch,
+a latency-critical path that must not enter the allocator).
 For them the library offers one entry point that uses a fixed scratch array the
 library keeps in device memory instead of a caller-provided workspace.  These
 tests check, through the C ABI, that it gives the same results as the regular
