@@ -176,69 +176,83 @@ class ClockSampler:
 
 # --------------------------------------------------------------- our arm ---
 
-def run_ours(args, w, rank, world, local_rank):
-    import torch
-    import causal_grouped_query_gqa_b300 as gq
-    from causal_grouped_query_gqa_b300.inputs import make_inputs
+class Problem:
+    """Device tensors of one workload and the calls of one step (through the C ABI)."""
 
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py: no CUDA device (the library has no CPU path)")
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    gq.load_library()
-    with_bwd = args.step == "fwd+bwd" or (
-        args.step == "auto" and (w.backward or args.workload == DEFAULT_WORKLOAD))
-    B, H, G, S, d = w.B, w.H, w.G, w.S, w.d
-    kw = dict(causal=w.causal, window=w.window, n_sink=w.n_sink, scale=w.scale)
+    def __init__(self, w, dev, seed, with_bwd):
+        import torch
+        import causal_grouped_query_gqa_b300 as gq
+        from causal_grouped_query_gqa_b300.inputs import make_inputs
+        self.w, self.dev, self.with_bwd = w, dev, with_bwd
+        B, H, G, S, d = w.B, w.H, w.G, w.S, w.d
+        self.host = make_inputs(B, H, G, S, seed=seed, with_grad=True)
+        self.ins = tuple(t.to(dev) for t in self.host)
+        q = self.ins[0]
+        self.outs = (torch.empty_like(q), torch.empty((B, H, S), dtype=torch.float32, device=dev),
+                     torch.empty_like(q), torch.empty_like(self.ins[1]),
+                     torch.empty_like(self.ins[2]))
+        self.ws_bytes = gq.gqa_attn_bwd_workspace_size(B, H, G, S, d)
+        self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=dev)
+        self.fws_bytes = gq.gqa_attn_fwd_workspace_size(B, H, G, S, d)
+        self.fws = torch.empty(max(self.fws_bytes, 16), dtype=torch.uint8, device=dev)
+        # the forward entry point the library's own fwd() picks for this size
+        fwd_f, _ = step_flops(w, False)
+        self.score_bound = fwd_f >= gq.SCORE_BOUND_MIN_FLOPS
 
-    # each rank owns its own shard of independent problems (different seeds)
-    q_h, k_h, v_h, do_h = make_inputs(B, H, G, S, seed=rank, with_grad=True)
-    q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
-    o = torch.empty_like(q)
-    lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws_bytes = gq.gqa_attn_bwd_workspace_size(B, H, G, S, d)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
-    fws_bytes = gq.gqa_attn_fwd_workspace_size(B, H, G, S, d)
-    fws = torch.empty(max(fws_bytes, 16), dtype=torch.uint8, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-
-    def step_on(ins, outs, strm):
+    def step_on(self, ins, outs, strm, score_bound=None):
+        import causal_grouped_query_gqa_b300 as gq
+        w = self.w
+        B, H, G, S, d = w.B, w.H, w.G, w.S, w.d
         q_, k_, v_, do_ = ins
         o_, lse_, dq_, dk_, dv_ = outs
-        rc = gq.gqa_attn_fwd_ws(q_, k_, v_, o_, lse_, B, H, G, S, d, w.causal, w.window,
-                                w.n_sink, w.scale, fws, fws_bytes, strm)
+        bound = self.score_bound if score_bound is None else score_bound
+        if bound:
+            rc = gq.gqa_attn_fwd_ws(q_, k_, v_, o_, lse_, B, H, G, S, d, w.causal, w.window,
+                                    w.n_sink, w.scale, self.fws, self.fws_bytes, strm)
+        else:
+            rc = gq.gqa_attn_fwd(q_, k_, v_, o_, lse_, B, H, G, S, d, w.causal, w.window,
+                                 w.n_sink, w.scale, strm)
         if rc != gq.GQA_OK:
-            raise gq.GqaError(rc, "gqa_attn_fwd_ws")
-        if with_bwd:
+            raise gq.GqaError(rc, "forward")
+        if self.with_bwd:
             rc = gq.gqa_attn_bwd(q_, k_, v_, o_, do_, lse_, dq_, dk_, dv_, B, H, G, S, d,
-                                 w.causal, w.window, w.n_sink, w.scale, ws, ws_bytes, strm)
+                                 w.causal, w.window, w.n_sink, w.scale, self.ws, self.ws_bytes,
+                                 strm)
             if rc != gq.GQA_OK:
                 raise gq.GqaError(rc, "gqa_attn_bwd")
 
-    def step():
-        step_on((q, k, v, do), (o, lse, dq, dk, dv), stream)
+    def launches_per_step(self, score_bound=None):
+        bound = self.score_bound if score_bound is None else score_bound
+        return (2 if bound else 1) + (3 if self.with_bwd else 0)
 
-    launches_per_step = 2 + (3 if with_bwd else 0)  # key norms + forward, prep + main + convert
-    for _ in range(args.warmup):
+
+def timed_steps(pb, steps, warmup, flush, stream, world, score_bound=None, clocks=False):
+    """Times `steps` steps of `pb` with CUDA events on `stream`, L2 flushed before
+    each step outside the events.  Returns (total ms, per-kernel ms lists, clocks)."""
+    import torch
+    import causal_grouped_query_gqa_b300 as gq
+
+    def step():
+        pb.step_on(pb.ins, pb.outs, stream, score_bound)
+
+    for _ in range(warmup):
         flush.zero_()
         step()
     torch.cuda.synchronize()
     if gq.gqa_attn_last_device_status() != gq.GQA_OK:
         raise SystemExit("device status error during warm-up")
-
-    # ---- timed region: per-step events, kernel events from the library hooks
     gq.gqa_attn_timing_enable(1)
     kms = gq.timing_buffer()
     kernel_ms = [[] for _ in range(N_KERNELS)]
-    step_ms = []
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+          for _ in range(steps)]
     _barrier(world)
     torch.cuda.synchronize()
-    with ClockSampler(local_rank) as clocks:
-        for s_i in range(args.steps):
+    sampler = ClockSampler(torch.cuda.current_device()) if clocks else None
+    if sampler:
+        sampler.__enter__()
+    try:
+        for s_i in range(steps):
             flush.zero_()
             ev[s_i][0].record(stream)
             step()
@@ -248,70 +262,174 @@ def run_ours(args, w, rank, world, local_rank):
                 if kms[kid] >= 0:
                     kernel_ms[kid].append(float(kms[kid]))
         torch.cuda.synchronize()
+    finally:
+        if sampler:
+            sampler.__exit__(None, None, None)
     gq.gqa_attn_timing_enable(0)
     _barrier(world)
-    step_ms = [a.elapsed_time(b) for a, b in ev]
     if gq.gqa_attn_last_device_status() != gq.GQA_OK:
         raise SystemExit("device status error in the timed region")
-    local_total_ms = sum(step_ms)
-    total_ms = _max_over_ranks(local_total_ms, world)
+    total = sum(a.elapsed_time(b) for a, b in ev)
+    return total, kernel_ms, (sampler.summary() if sampler else None)
 
-    fwd_f, bwd_f = step_flops(w, with_bwd)
-    flops_step = fwd_f + bwd_f
-    value = job_throughput(flops_step, args.steps, total_ms, world)
-    peaks = measured_peaks()
 
-    # ---- dominant kernel roofline
+def tensor_roofline(kernel, flops, ms, peaks, workload):
+    achieved = flops / (ms * 1e-3) / 1e12
+    return {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+            "traffic": recorded_traffic(kernel, workload), "kernel": kernel,
+            "peak_source": f"{peaks['source']} burst bf16 (MEASURED_PEAKS.json)",
+            "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4)}
+
+
+def summarize(w, pb, kernel_ms, total_ms, steps, world, peaks, workload):
+    fwd_f, bwd_f = step_flops(w, pb.with_bwd)
+    avg = {kid: kernels_ms_avg(kernel_ms, kid) for kid in range(N_KERNELS)}
+    fwd_ms = avg[0] + avg[4]
+    bwd_ms = avg[1] + avg[2] + avg[3]
     tot = [sum(x) for x in kernel_ms]
     dom = max(range(N_KERNELS), key=lambda kid: tot[kid])
-    dom_avg_ms = tot[dom] / max(1, len(kernel_ms[dom]))
     dom_flops = {0: fwd_f, 2: bwd_f}.get(dom)
     if dom_flops:
-        achieved = dom_flops / (dom_avg_ms * 1e-3) / 1e12
-        roofline = {"bound": "tensor", "achieved": round(achieved, 2),
-                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                    "frac": round(achieved / peaks["bf16_tflops"], 4),
-                    "traffic": recorded_traffic(KERNEL_NAMES[dom], args.workload),
-                    "kernel": KERNEL_NAMES[dom],
-                    "peak_source": f"{peaks['source']} burst bf16 (MEASURED_PEAKS.json)",
-                    "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4)}
+        roofline = tensor_roofline(KERNEL_NAMES[dom], dom_flops, avg[dom], peaks, workload)
     else:
         nbytes = bwd_bytes(w)
-        achieved = nbytes / (dom_avg_ms * 1e-3) / 1e9
+        achieved = nbytes / (avg[dom] * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                     "traffic": None, "kernel": KERNEL_NAMES[dom]}
-    kernels = {KERNEL_NAMES[kid]: round(tot[kid] / max(1, len(kernel_ms[kid])) * 1e3, 1)
-               for kid in range(N_KERNELS) if kernel_ms[kid]}
+    out = {
+        "value": round(job_throughput(fwd_f + bwd_f, steps, total_ms, world), 2),
+        "ms_per_step": round(total_ms / steps, 4),
+        "fwd_tflops": round(fwd_f / (fwd_ms * 1e-3) / 1e12, 2) if fwd_ms > 0 else None,
+        "bwd_tflops": round(bwd_f / (bwd_ms * 1e-3) / 1e12, 2) if pb.with_bwd and bwd_ms > 0
+        else None,
+        "fwd_score_bound": pb.score_bound,
+        "kernel_us": {KERNEL_NAMES[kid]: round(avg[kid] * 1e3, 1)
+                      for kid in range(N_KERNELS) if kernel_ms[kid]},
+        "roofline": roofline,
+    }
+    if avg[0] > 0:
+        fb = fwd_bytes(w)
+        gbs = fb / (avg[0] * 1e-3) / 1e9
+        out["fwd_hbm"] = {"achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                          "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": fb,
+                          "kernel": "gqa_fwd_kernel"}
+    for kid, nbytes in ((4, knorm_bytes(w)), (1, prep_bytes(w)), (3, convert_bytes(w))):
+        if avg[kid] > 0:
+            gbs = nbytes / (avg[kid] * 1e-3) / 1e9
+            out.setdefault("hbm_kernels", {})[KERNEL_NAMES[kid]] = {
+                "achieved": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
+                "algorithmic_bytes": nbytes, "unit": "GB/s"}
+    return out
+
+
+def run_ours(args, w, rank, world, local_rank):
+    import torch
+    import causal_grouped_query_gqa_b300 as gq
+    from causal_grouped_query_gqa_b300.inputs import WORKLOADS
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the library has no CPU path)")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    gq.load_library()
+    with_bwd = args.step == "fwd+bwd" or (
+        args.step == "auto" and (w.backward or args.workload == DEFAULT_WORKLOAD))
+    # each rank owns its own shard of independent problems (different seeds)
+    pb = Problem(w, dev, seed=rank, with_bwd=with_bwd)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    peaks = measured_peaks()
+
+    total_ms, kernel_ms, clocks = timed_steps(pb, args.steps, args.warmup, flush, stream, world,
+                                              clocks=True)
+    total_ms = _max_over_ranks(total_ms, world)
+    main = summarize(w, pb, kernel_ms, total_ms, args.steps, world, peaks, args.workload)
+
+    # the plain forward (gqa_attn_fwd: the online maximum on every tile, any input)
+    fwd_only = Problem.__new__(Problem)
+    fwd_only.__dict__.update(pb.__dict__)
+    fwd_only.with_bwd = False
+    p_ms, p_kernel, _ = timed_steps(fwd_only, args.steps, args.warmup, flush, stream, world,
+                                    score_bound=False)
+    fwd_f, bwd_f = step_flops(w, with_bwd)
+    plain_ms = kernels_ms_avg(p_kernel, 0)
+    fwd_plain = {"tflops": round(fwd_f / (plain_ms * 1e-3) / 1e12, 2),
+                 "kernel_us": round(plain_ms * 1e3, 1),
+                 "frac": round(fwd_f / (plain_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+                 "entry": "gqa_attn_fwd"}
 
     # ---- end to end through the same calls, host buffers
-    e2e = run_e2e(args, dev, with_bwd, dev_in=(q, k, v, do), dev_out=(o, lse, dq, dk, dv),
-                  host=(q_h, k_h, v_h, do_h), step_on=step_on, world=world, flops_step=flops_step)
+    e2e = run_e2e(args, dev, pb, world=world, flops_step=fwd_f + bwd_f)
 
     out = {
-        "metric": METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world,
+        "metric": METRIC, "value": main["value"], "unit": "TFLOPS", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+        "ms_per_step": main["ms_per_step"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (bf16 iid N(0,1), torch CPU generator, seed = rank)",
-        "config": {"workload": args.workload, "B": B, "H": H, "G": G, "S": S, "d": d,
+        "config": {"workload": args.workload, "B": w.B, "H": w.H, "G": w.G, "S": w.S, "d": w.d,
                    "causal": w.causal, "window": w.window, "n_sink": w.n_sink,
                    "step": "fwd+bwd" if with_bwd else "fwd",
                    "l2": "flushed before every timed step (256 MB write, outside the events)",
                    "parallelism": f"replicas over ranks ({world}), no collective"},
-        "pct_of_peak": round(100 * value / world / peaks["bf16_tflops"], 2),
-        "fwd_tflops": round(fwd_f / (sum(kernels_ms_avg(kernel_ms, k) for k in (0, 4)) * 1e-3)
-                            / 1e12, 2)
-        if kernel_ms[0] else None,
-        "bwd_tflops": round(bwd_f / (sum(kernels_ms_avg(kernel_ms, k) for k in (1, 2, 3)) * 1e-3)
-                            / 1e12, 2) if with_bwd and kernel_ms[2] else None,
-        "kernel_us": kernels,
-        "roofline": roofline,
+        "pct_of_peak": round(100 * main["value"] / world / peaks["bf16_tflops"], 2),
+        "fwd_tflops": main["fwd_tflops"], "bwd_tflops": main["bwd_tflops"],
+        "fwd_score_bound": main["fwd_score_bound"],
+        "fwd_plain_tflops": fwd_plain["tflops"], "fwd_plain": fwd_plain,
+        "kernel_us": main["kernel_us"],
+        "roofline": main["roofline"],
+        "hbm_kernels": main.get("hbm_kernels"),
         "e2e": e2e,
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clocks.summary(),
+        "gpu_launches": pb.launches_per_step() * args.steps,
+        "clocks": clocks,
     }
+
+    # ---- the other stated workloads, a few steps each (rank 0, after the timed region)
+    if rank == 0 and not args.no_extra and args.workload == DEFAULT_WORKLOAD:
+        extras = {}
+        for name, step in EXTRA_WORKLOADS:
+            ew = WORKLOADS[name]
+            epb = Problem(ew, dev, seed=0, with_bwd=(step == "fwd+bwd"))
+            e_steps = max(3, min(args.steps, 10))
+            e_ms, e_kernel, e_clk = timed_steps(epb, e_steps, 3, flush, stream, 1, clocks=True)
+            res = summarize(ew, epb, e_kernel, e_ms, e_steps, 1, peaks, name)
+            res.update({"step": step, "steps": e_steps, "clocks": e_clk,
+                        "config": {"B": ew.B, "H": ew.H, "G": ew.G, "S": ew.S,
+                                   "window": ew.window, "n_sink": ew.n_sink}})
+            extras[name] = res
+            del epb
+            torch.cuda.empty_cache()
+        out["extra_workloads"] = extras
     return out
+
+
+# The stated workloads besides the default one, measured in the same run
+# (the default line's value is unaffected).
+EXTRA_WORKLOADS = [
+    ("gqa_b2_h32_g8_s2048", "fwd"),
+    ("window_b1_h128_g16_s32768_w4096_sink128", "fwd"),
+    ("bwd_b4_h32_g8_s4096", "fwd+bwd"),
+]
+
+
+def knorm_bytes(w):
+    """Key-norm pre-pass: reads K, writes one 128-byte record per kv head."""
+    return 2 * w.d * w.S * w.B * w.G + 128 * w.B * w.G
+
+
+def prep_bytes(w):
+    """Backward prep: reads O, dO (bf16) and LSE, writes D and LSE2 (fp32) and
+    clears the fp32 dQ accumulator."""
+    rows = w.B * w.H * w.S
+    return 2 * 2 * w.d * rows + 4 * rows + 8 * rows + 4 * w.d * rows
+
+
+def convert_bytes(w):
+    """dQ convert: reads the fp32 accumulator, writes bf16 dQ."""
+    rows = w.B * w.H * w.S
+    return 6 * w.d * rows
 
 
 def kernels_ms_avg(kernel_ms, kid):
@@ -319,13 +437,15 @@ def kernels_ms_avg(kernel_ms, kid):
     return sum(x) / len(x) if x else 0.0
 
 
-def run_e2e(args, dev, with_bwd, dev_in, dev_out, host, step_on, world, flops_step):
+def run_e2e(args, dev, pb, world, flops_step):
     """Same step with the inputs copied from pinned host memory and every output
     copied back, all inside the timed region.  Copies and compute run on three
     streams (upload, compute, download) over two sets of device tensors, so the
     upload of step i+1 and the download of step i-1 overlap the compute of
     step i, as a training or serving loop would arrange them."""
     import torch
+    with_bwd = pb.with_bwd
+    dev_in, dev_out, host = pb.ins, pb.outs, pb.host
     n_in = 4 if with_bwd else 3
     n_out = 5 if with_bwd else 2
     sets = [(list(dev_in), list(dev_out)),
@@ -348,7 +468,7 @@ def run_e2e(args, dev, with_bwd, dev_in, dev_out, host, step_on, world, flops_st
             in_ready[b].record(s_up)
         s_cmp.wait_event(in_ready[b])
         s_cmp.wait_event(out_done[b])  # step i-2's outputs of this set are downloaded
-        step_on(d_in, d_out, s_cmp)
+        pb.step_on(d_in, d_out, s_cmp)
         cmp_done[b].record(s_cmp)
         with torch.cuda.stream(s_down):
             s_down.wait_event(cmp_done[b])
@@ -505,6 +625,8 @@ def main(argv=None):
                          "workloads stated with a backward, else fwd")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip timing the oracle (profiling runs only)")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the other stated workloads (profiling runs only)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

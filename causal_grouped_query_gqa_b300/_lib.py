@@ -199,10 +199,32 @@ def _check(t, shape, dtype, name):
     return torch
 
 
+def visible_pairs(S: int, causal=True, window=0, n_sink=0) -> int:
+    """Visible (query, key) pairs of one head under the mask (closed form)."""
+    if not causal:
+        return S * S
+    if window <= 0 or window >= S:
+        return S * (S + 1) // 2
+    in_window = window * (window + 1) // 2 + (S - window) * window
+    older = S - window  # rows with keys before their window: 1 .. S - window such keys
+    ns = min(max(n_sink, 0), older)
+    sinks = ns * (ns + 1) // 2 + (older - ns) * ns
+    return in_window + sinks
+
+
+# Smallest forward, in causal FLOPs, for which the score bound is taken by
+# default: below it the key-norm pre-pass costs about what the bound saves.
+SCORE_BOUND_MIN_FLOPS = 1 << 36
+
+
 def fwd(q, k, v, *, causal=True, window=0, n_sink=0, scale=None, out=None, lse=None,
-        workspace=None, stream=None):
-    """o, lse = fwd(q [B,H,S,64] bf16, k/v [B,G,S,64] bf16) on the current CUDA stream
-    (gqa_attn_fwd_ws; `workspace` is allocated when not given)."""
+        workspace=None, score_bound=None, stream=None):
+    """o, lse = fwd(q [B,H,S,64] bf16, k/v [B,G,S,64] bf16) on the current CUDA stream.
+
+    score_bound: True runs gqa_attn_fwd_ws (key-norm pre-pass, then the forward
+    with the score bound; `workspace` is allocated when not given), False runs
+    gqa_attn_fwd; None takes the bound when the forward has at least
+    SCORE_BOUND_MIN_FLOPS causal FLOPs.  Both give the same result contract."""
     import torch
     B, H, S, d = q.shape
     G = k.shape[1]
@@ -212,6 +234,14 @@ def fwd(q, k, v, *, causal=True, window=0, n_sink=0, scale=None, out=None, lse=N
     scale = 1.0 / d ** 0.5 if scale is None else scale
     o = torch.empty_like(q) if out is None else out
     l = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if lse is None else lse
+    if score_bound is None:
+        flops = 4 * d * B * H * visible_pairs(S, causal, window, n_sink)
+        score_bound = flops >= SCORE_BOUND_MIN_FLOPS
+    if not score_bound:
+        rc = gqa_attn_fwd(q, k, v, o, l, B, H, G, S, d, causal, window, n_sink, scale, stream)
+        if rc != GQA_OK:
+            raise GqaError(rc, "gqa_attn_fwd")
+        return o, l
     need = gqa_attn_fwd_workspace_size(B, H, G, S, d)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)

@@ -69,15 +69,26 @@ def build_checked(force: bool = False, verbose: bool = False) -> str:
     return build(force=force, verbose=verbose, out=CHECKED_LIB, extra=("-DGQA_DEVICE_CHECKS",))
 
 
+# Test build whose backward writes dq, dk and dv as fp32 (GQA_FP32_GRAD_OUT):
+# the gradients before the final bf16 rounding, for the tolerance tests of
+# tests/test_grad_precision.py.  Never loaded by the package.
+FP32_GRAD_LIB = os.path.join(PKG, "libgqa_attn_fp32grad.so")
+
+
+def build_fp32_grad(force: bool = False, verbose: bool = False) -> str:
+    return build(force=force, verbose=verbose, out=FP32_GRAD_LIB, extra=("-DGQA_FP32_GRAD_OUT",))
+
+
 if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose", action="store_true")
     ap.add_argument("--test-libs", action="store_true",
-                    help="also build the failure-detection and index-check test libraries")
+                    help="also build the failure-detection, index-check and fp32-gradient test libraries")
     a = ap.parse_args()
     print(build(force=a.force, verbose=a.verbose))
     if a.test_libs:
         print(build_stall_test(force=a.force, verbose=a.verbose))
         print(build_checked(force=a.force, verbose=a.verbose))
+        print(build_fp32_grad(force=a.force, verbose=a.verbose))
     sys.exit(0)

@@ -113,6 +113,34 @@ struct Problem {
   float scale;
 };
 
+// Element type of the dq, dk and dv outputs.  A test build of the library
+// (-DGQA_FP32_GRAD_OUT) writes them as fp32, straight from the fp32
+// accumulators, so that tests can measure the error of the gradients before
+// the final bf16 rounding; release builds write bf16.
+#ifdef GQA_FP32_GRAD_OUT
+using GradOut = float;
+#else
+using GradOut = __nv_bfloat16;
+#endif
+
+// Stores 8 consecutive gradient elements a[0..7] * f at dst.
+__device__ __forceinline__ void store_grad8(GradOut *dst, const uint32_t *a, float f) {
+#ifdef GQA_FP32_GRAD_OUT
+  float4 *d = reinterpret_cast<float4 *>(dst);
+  d[0] = make_float4(__uint_as_float(a[0]) * f, __uint_as_float(a[1]) * f,
+                     __uint_as_float(a[2]) * f, __uint_as_float(a[3]) * f);
+  d[1] = make_float4(__uint_as_float(a[4]) * f, __uint_as_float(a[5]) * f,
+                     __uint_as_float(a[6]) * f, __uint_as_float(a[7]) * f);
+#else
+  uint4 w;
+  w.x = pack_bf16x2(__uint_as_float(a[0]) * f, __uint_as_float(a[1]) * f);
+  w.y = pack_bf16x2(__uint_as_float(a[2]) * f, __uint_as_float(a[3]) * f);
+  w.z = pack_bf16x2(__uint_as_float(a[4]) * f, __uint_as_float(a[5]) * f);
+  w.w = pack_bf16x2(__uint_as_float(a[6]) * f, __uint_as_float(a[7]) * f);
+  *reinterpret_cast<uint4 *>(dst) = w;
+#endif
+}
+
 struct MainParams {
   int B, H, G, S, R, S_pad;
   int causal, window, n_sink;
@@ -121,8 +149,8 @@ struct MainParams {
   int n_ktiles;
   const float *lse2;  // [B*H][S_pad]
   const float *delta; // [B*H][S_pad]
-  __nv_bfloat16 *dk;
-  __nv_bfloat16 *dv;
+  GradOut *dk;
+  GradOut *dv;
   int *status;
 };
 
@@ -238,19 +266,15 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__re
 
 // dq = bf16(scale * dq_acc), eight elements per thread and pass.
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float *__restrict__ dq_acc,
-                                                             __nv_bfloat16 *__restrict__ dq,
+                                                             GradOut *__restrict__ dq,
                                                              long long n8, float scale) {
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < n8;
        e += stride) {
-    const float4 a = reinterpret_cast<const float4 *>(dq_acc)[2 * e];
-    const float4 b = reinterpret_cast<const float4 *>(dq_acc)[2 * e + 1];
-    uint4 w;
-    w.x = pack_bf16x2(a.x * scale, a.y * scale);
-    w.y = pack_bf16x2(a.z * scale, a.w * scale);
-    w.z = pack_bf16x2(b.x * scale, b.y * scale);
-    w.w = pack_bf16x2(b.z * scale, b.w * scale);
-    reinterpret_cast<uint4 *>(dq)[e] = w;
+    const uint4 a = reinterpret_cast<const uint4 *>(dq_acc)[2 * e];
+    const uint4 b = reinterpret_cast<const uint4 *>(dq_acc)[2 * e + 1];
+    const uint32_t v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    store_grad8(dq + 8 * e, v, scale);
   }
 }
 
@@ -588,27 +612,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       reg_fence(a1);
       if (j < p.S && GQA_CHECK(p.status, b < p.B && g < p.G)) {
         const float f = wg == 0 ? 1.f : p.scale;
-        __nv_bfloat16 *dst = (wg == 0 ? p.dv : p.dk) +
-                             ((static_cast<size_t>(b) * p.G + g) * p.S + j) * HD;
-        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+        GradOut *dst = (wg == 0 ? p.dv : p.dk) + ((static_cast<size_t>(b) * p.G + g) * p.S + j) * HD;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(a0[8 * c + 0]) * f, __uint_as_float(a0[8 * c + 1]) * f);
-          w.y = pack_bf16x2(__uint_as_float(a0[8 * c + 2]) * f, __uint_as_float(a0[8 * c + 3]) * f);
-          w.z = pack_bf16x2(__uint_as_float(a0[8 * c + 4]) * f, __uint_as_float(a0[8 * c + 5]) * f);
-          w.w = pack_bf16x2(__uint_as_float(a0[8 * c + 6]) * f, __uint_as_float(a0[8 * c + 7]) * f);
-          d4[c] = w;
-        }
+        for (int c = 0; c < 4; ++c) store_grad8(dst + 8 * c, a0 + 8 * c, f);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(a1[8 * c + 0]) * f, __uint_as_float(a1[8 * c + 1]) * f);
-          w.y = pack_bf16x2(__uint_as_float(a1[8 * c + 2]) * f, __uint_as_float(a1[8 * c + 3]) * f);
-          w.z = pack_bf16x2(__uint_as_float(a1[8 * c + 4]) * f, __uint_as_float(a1[8 * c + 5]) * f);
-          w.w = pack_bf16x2(__uint_as_float(a1[8 * c + 6]) * f, __uint_as_float(a1[8 * c + 7]) * f);
-          d4[4 + c] = w;
-        }
+        for (int c = 0; c < 4; ++c) store_grad8(dst + 32 + 8 * c, a1 + 8 * c, f);
       }
     }
   } else {
@@ -713,6 +721,9 @@ inline int launch(const Problem &pr, const void *q, const void *k, const void *v
                   cudaStream_t st) {
   const int B = pr.B, H = pr.H, G = pr.G, S = pr.S;
   const int S_pad = round_up(S, BQ);
+  // every size check comes before the first launch
+  const long long units = static_cast<long long>((S + BK - 1) / BK) * B * G;
+  if (units > 0x7fffffffLL) return -2;
   const long long rows = static_cast<long long>(B) * H * S;
   const long long rows_pad = static_cast<long long>(B) * H * S_pad;
   float *dq_acc = static_cast<float *>(ws);
@@ -761,11 +772,9 @@ inline int launch(const Problem &pr, const void *q, const void *k, const void *v
     p.n_ktiles = (S + BK - 1) / BK;
     p.lse2 = lse2;
     p.delta = delta;
-    p.dk = static_cast<__nv_bfloat16 *>(dk);
-    p.dv = static_cast<__nv_bfloat16 *>(dv);
+    p.dk = static_cast<GradOut *>(dk);
+    p.dv = static_cast<GradOut *>(dv);
     p.status = status;
-    const long long units = static_cast<long long>(p.n_ktiles) * B * G;
-    if (units > 0x7fffffffLL) return -2;
     timing_begin(2, st);
     bwd_main_kernel<<<static_cast<unsigned>(units), NTHREADS, SMEM_BYTES, st>>>(tq, tk, tv, tdo,
                                                                                tdq, p);
@@ -778,7 +787,7 @@ inline int launch(const Problem &pr, const void *q, const void *k, const void *v
     blocks = blocks < 1 ? 1 : (blocks > 8LL * sm_count ? 8LL * sm_count : blocks);
     timing_begin(3, st);
     bwd_dq_convert_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-        dq_acc, static_cast<__nv_bfloat16 *>(dq), n8, pr.scale);
+        dq_acc, static_cast<GradOut *>(dq), n8, pr.scale);
     timing_end(3, st);
     if (cuda_failed(cudaGetLastError(), "launch of the dQ convert kernel")) return -8;
   }

@@ -81,8 +81,10 @@ constexpr float kRescaleThreshold = 8.0f;
 // softmax, normalised by the same reference in O and l.
 constexpr float kFastSlack = 32.0f;
 constexpr float kBoundMax = 64.0f;
-constexpr int kKnParts = 4;  // partial maxima of |k_j|^2 per kv head: one 16-byte record
-static_assert(kKnParts == 4, "score_bound reads a record of four partial maxima");
+// partial maxima of |k_j|^2 per kv head: one 128-byte record (many CTAs per kv
+// head keep the pre-pass's loads spread over every SM)
+constexpr int kKnParts = 32;
+static_assert(kKnParts % 4 == 0, "score_bound reads the record as float4");
 __device__ __forceinline__ uint32_t col_s(int t) { return static_cast<uint32_t>(t) * 128u; }
 __device__ __forceinline__ uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(t) * 64u; }
 __device__ __forceinline__ uint32_t col_p(int t) { return 384u + static_cast<uint32_t>(t) * 64u; }
@@ -224,7 +226,13 @@ __device__ __forceinline__ float score_bound(const uint8_t *qrow, int r, const f
   }
   float qa, qb;
   f32x2_split(acc, qa, qb);
-  const float kmax2 = fmaxf(fmaxf(kn[0], kn[1]), fmaxf(kn[2], kn[3]));
+  float4 m4 = reinterpret_cast<const float4 *>(kn)[0];
+#pragma unroll
+  for (int c = 1; c < kKnParts / 4; ++c) {
+    const float4 x = reinterpret_cast<const float4 *>(kn)[c];
+    m4 = make_float4(fmaxf(m4.x, x.x), fmaxf(m4.y, x.y), fmaxf(m4.z, x.z), fmaxf(m4.w, x.w));
+  }
+  const float kmax2 = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w));
   return sqrtf((qa + qb) * kmax2) * sl2 * (1.f + 0x1p-10f) + 0x1p-10f;
 }
 
@@ -697,35 +705,45 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // Pre-pass of the score bound: for each kv head bg = b * G + g,
 // kn2[bg * kKnParts + part] = max |k_j|^2 over the keys of slice `part` of
 // [0, S) (fp32 sums of the squared bf16 elements; 0 for an empty slice).  One
-// CTA per (kv head, slice); 8 lanes per key row (16 bytes each), four rows per
-// warp and step.  fmaxf drops NaN rows (their scores are NaN whatever the
-// reference); an infinite row gives an infinite bound, hence the exact step.
+// CTA per (kv head, slice); 8 lanes per key row (16 bytes each), 32 rows per
+// pass of the CTA, and kKnormUnroll passes' loads issued before any is used,
+// so each thread keeps several 16-byte loads in flight.  fmaxf drops NaN rows
+// (their scores are NaN whatever the reference); an infinite row gives an
+// infinite bound, hence the exact step.
 constexpr int kKnormThreads = 256;
+constexpr int kKnormUnroll = 4;
 __global__ void __launch_bounds__(kKnormThreads)
-    fwd_knorm_kernel(const __nv_bfloat16 *k, int S, float *kn2) {
+    fwd_knorm_kernel(const __nv_bfloat16 *__restrict__ k, int S, float *__restrict__ kn2) {
+  constexpr int kRowsPerPass = kKnormThreads / 8;
   const int bg = blockIdx.x / kKnParts, part = blockIdx.x % kKnParts;
   const int per = (S + kKnParts - 1) / kKnParts;
-  const int r0 = part * per, r1 = min(S, r0 + per);
+  const int r0 = min(S, part * per), r1 = min(S, r0 + per);
   const uint4 *rows = reinterpret_cast<const uint4 *>(k + static_cast<size_t>(bg) * S * HD);
+  const int sub = threadIdx.x >> 3, ch = threadIdx.x & 7;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float m = 0.f;
-  // the loop bound is uniform in the warp, so every lane reaches the shuffles
-  for (int rb = r0 + 4 * warp; rb < r1; rb += 4 * (kKnormThreads / 32)) {
-    const int row = rb + (lane >> 3);
-    float sq = 0.f;
-    if (row < r1) {
-      const uint4 w = __ldg(rows + static_cast<size_t>(row) * (HD / 8) + (lane & 7));
-      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+  // the loop bound is uniform in the block, so every lane reaches the shuffles
+  for (int rb = r0; rb < r1; rb += kRowsPerPass * kKnormUnroll) {
+    uint4 w[kKnormUnroll];
+#pragma unroll
+    for (int u = 0; u < kKnormUnroll; ++u) {
+      const int row = rb + kRowsPerPass * u + sub;
+      w[u] = row < r1 ? __ldg(rows + static_cast<size_t>(row) * (HD / 8) + ch) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kKnormUnroll; ++u) {
+      const uint32_t ws[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+      float sq = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float lo = __uint_as_float(ws[e] << 16), hi = __uint_as_float(ws[e] & 0xffff0000u);
         sq = fmaf(lo, lo, fmaf(hi, hi, sq));
       }
+      sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+      sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+      sq += __shfl_xor_sync(0xffffffffu, sq, 4);
+      m = fmaxf(m, sq);
     }
-    sq += __shfl_xor_sync(0xffffffffu, sq, 1);
-    sq += __shfl_xor_sync(0xffffffffu, sq, 2);
-    sq += __shfl_xor_sync(0xffffffffu, sq, 4);
-    m = fmaxf(m, sq);
   }
 #pragma unroll
   for (int o = 8; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -735,7 +753,7 @@ __global__ void __launch_bounds__(kKnormThreads)
   if (threadIdx.x == 0) {
     float b = wmax[0];
 #pragma unroll
-    for (int w = 1; w < kKnormThreads / 32; ++w) b = fmaxf(b, wmax[w]);
+    for (int x = 1; x < kKnormThreads / 32; ++x) b = fmaxf(b, wmax[x]);
     kn2[blockIdx.x] = b;
   }
 }

@@ -80,8 +80,8 @@ GQA_API int gqa_attn_fwd(const void *q, const void *k, const void *v, void *o, f
                  int causal, int window, int n_sink, float scale, void *stream);
 
 /*
- * Bytes of scratch that gqa_attn_fwd_ws needs: B * G records of 4 fp32 partial
- * maxima of |k_j|^2 (16 bytes per kv head).  Returns 0 for invalid sizes.
+ * Bytes of scratch that gqa_attn_fwd_ws needs: B * G records of 32 fp32 partial
+ * maxima of |k_j|^2 (128 bytes per kv head).  Returns 0 for invalid sizes.
  */
 GQA_API size_t gqa_attn_fwd_workspace_size(int B, int H, int G, int S, int d);
 
@@ -89,13 +89,18 @@ GQA_API size_t gqa_attn_fwd_workspace_size(int B, int H, int G, int S, int d);
  * Forward with a score bound: the result contract of gqa_attn_fwd (the same
  * definition in the same precision), in two launches on `stream`.  A first
  * kernel writes into `workspace` the largest squared norm of each kv head's key
- * rows.  Every scaled score of query row i is at most
- * U_i = |q_i| * max_j |k_j| * scale * log2(e) in magnitude (Cauchy-Schwarz, base-2
- * units); a warp whose 32 rows all have U_i <= 64 computes its whole unit of key
- * tiles against the fixed reference U_i - 32 instead of a running row maximum
- * (every term 2^(s - reference) then lies in [2^-96, 2^32]), and rows with
- * larger bounds keep the online maximum of "SnapKitty Transformer 8B",
- * section "FlashAttention Inference".  The bound is this library's.
+ * rows (32 partial maxima per kv head).  Every scaled score of query row i is
+ * at most U_i = |q_i| * max_j |k_j| * scale * log2(e) in magnitude
+ * (Cauchy-Schwarz, base-2 units); a warp whose 32 rows all have U_i <= 64
+ * computes its whole unit of key tiles against the fixed reference U_i - 32
+ * instead of a running row maximum (every term 2^(s - reference) then lies in
+ * [2^-96, 2^32]), and rows with larger bounds keep the online maximum of
+ * "SnapKitty Transformer 8B", section "FlashAttention Inference".  The bound is
+ * this library's.
+ * Input range: the fp32 sums of O then hold up to S * 2^32 * max|v|, so the
+ * result equals gqa_attn_fwd's while max|v| < 2^(95 - log2 S) (2^77 at
+ * S = 204800); gqa_attn_fwd keeps terms below 2^8 and allows max|v| up to
+ * 2^(119 - log2 S).  Use gqa_attn_fwd for values beyond the first limit.
  * workspace: device memory of at least gqa_attn_fwd_workspace_size() bytes,
  * 16-byte aligned, owned by the caller and not used by any other call running
  * at the same time.  Errors: as gqa_attn_fwd, plus GQA_ERR_NULL for a null

@@ -53,8 +53,8 @@ def test_workspace_size(lib):
     assert gq.gqa_attn_bwd_workspace_size(B, H, G, S, 128) == 0
     assert gq.gqa_attn_bwd_workspace_size(1, 3, 2, 10, 64) == 0
     assert gq.gqa_attn_bwd_workspace_size(0, 4, 2, 10, 64) == 0
-    # forward: one 16-byte record (4 fp32 partial maxima of |k|^2) per kv head
-    assert gq.gqa_attn_fwd_workspace_size(B, H, G, S, 64) == B * G * 16
+    # forward: one 128-byte record (32 fp32 partial maxima of |k|^2) per kv head
+    assert gq.gqa_attn_fwd_workspace_size(B, H, G, S, 64) == B * G * 128
     assert gq.gqa_attn_fwd_workspace_size(1, 3, 2, 10, 64) == 0
     assert gq.gqa_attn_fwd_workspace_size(B, H, G, S, 128) == 0
 

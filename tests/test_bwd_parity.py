@@ -109,6 +109,24 @@ def test_bwd_workload_sampled_groups():
         check_close(f"dQ[b{b},g{g}]", to64(dq[b, g * R:(g + 1) * R]), rq)
 
 
+def test_wide_workload_bwd_groups():
+    """B1 H128 G16 S8192: the backward of the benchmark's default step, checked
+    on the first and last kv groups whole (dQ of their 8 heads, dK, dV)."""
+    w = WORKLOADS["wide_b1_h128_g16_s8192"]
+    q, k, v, do = make_inputs(w.B, w.H, w.G, w.S, seed=0, with_grad=True)
+    dq, dk, dv = _gpu_fwd_bwd(q, k, v, do)
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t).all()
+    R = w.H // w.G
+    for g in (0, w.G - 1):
+        heads = slice(g * R, (g + 1) * R)
+        rq, rk, rv = oracle.attn_bwd_group(to64(q[:, heads]), to64(k[:, g:g + 1]),
+                                           to64(v[:, g:g + 1]), to64(do[:, heads]), 0, 0)
+        check_close(f"dK[g{g}]", to64(dk[0, g]), rk)
+        check_close(f"dV[g{g}]", to64(dv[0, g]), rv)
+        check_close(f"dQ[g{g}]", to64(dq[0, heads]), rq)
+
+
 def test_window_bwd_long_context_sampled():
     """Window + sink backward at S = 32768 (one kv group of the window workload's
     shape with fewer heads), checked on the whole group."""

@@ -11,10 +11,11 @@ from parity_util import LSE_ABS, check_close, sample_rows, to64
 pytestmark = pytest.mark.gpu
 
 
-def _run_full(B, H, G, S, causal=True, window=0, n_sink=0, seed=0, scale=None):
+def _run_full(B, H, G, S, causal=True, window=0, n_sink=0, seed=0, scale=None,
+              score_bound=None):
     q, k, v = make_inputs(B, H, G, S, seed=seed)
     o, lse = gq.fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, window=window, n_sink=n_sink,
-                    scale=scale)
+                    scale=scale, score_bound=score_bound)
     torch.cuda.synchronize()
     assert gq.gqa_attn_last_device_status() == gq.GQA_OK
     ro, rl = oracle.attn_fwd(to64(q), to64(k), to64(v), causal=causal, window=window,
@@ -34,8 +35,9 @@ def _run_full(B, H, G, S, causal=True, window=0, n_sink=0, seed=0, scale=None):
     (1, 2, 2, 384),      # H == G (plain multi-head)
     (1, 8, 1, 520),      # R = 8, multi-query
 ])
-def test_causal(B, H, G, S):
-    _run_full(B, H, G, S)
+@pytest.mark.parametrize("score_bound", [False, True], ids=["plain", "bound"])
+def test_causal(B, H, G, S, score_bound):
+    _run_full(B, H, G, S, score_bound=score_bound)
 
 
 @pytest.mark.parametrize("S", [64, 200, 513])
@@ -53,12 +55,14 @@ def test_full_attention(S):
     (777, 129, 300),    # sinks spanning three tiles
     (300, 50, 1000),    # more sinks than keys: every key is a sink, plain causal
 ])
-def test_window_sinks(S, window, n_sink):
-    _run_full(1, 4, 2, S, window=window, n_sink=n_sink)
+@pytest.mark.parametrize("score_bound", [False, True], ids=["plain", "bound"])
+def test_window_sinks(S, window, n_sink, score_bound):
+    _run_full(1, 4, 2, S, window=window, n_sink=n_sink, score_bound=score_bound)
 
 
-def test_scale_not_default():
-    _run_full(1, 4, 2, 300, scale=0.37)
+@pytest.mark.parametrize("score_bound", [False, True], ids=["plain", "bound"])
+def test_scale_not_default(score_bound):
+    _run_full(1, 4, 2, 300, scale=0.37, score_bound=score_bound)
 
 
 @pytest.mark.parametrize("B,H,G,S,window,n_sink", [
@@ -67,10 +71,11 @@ def test_scale_not_default():
     (2, 12, 4, 1536, 300, 70),   # the same with a window and sinks (192 units)
     (3, 16, 2, 1100, 0, 0),      # R = 8, ragged tail, 216 units
 ])
-def test_persistent_grid_many_units(B, H, G, S, window, n_sink):
+@pytest.mark.parametrize("score_bound", [False, True], ids=["plain", "bound"])
+def test_persistent_grid_many_units(B, H, G, S, window, n_sink, score_bound):
     """More work units than SMs, so every CTA carries its barrier phases, Q
     buffers and O accumulators from one unit to the next."""
-    _run_full(B, H, G, S, window=window, n_sink=n_sink)
+    _run_full(B, H, G, S, window=window, n_sink=n_sink, score_bound=score_bound)
 
 
 def test_gqa_workload_full():
@@ -78,12 +83,13 @@ def test_gqa_workload_full():
     _run_full(w.B, w.H, w.G, w.S)
 
 
-def _run_sampled(w, n_rows=48, extra=()):
-    """Full-size launch (the benchmark's), checked on sampled rows plus
+def _run_sampled(w, n_rows=48, extra=(), groups=(), score_bound=None):
+    """Full-size launch (the benchmark's), checked on whole kv groups (every
+    row of their R query heads), on sampled rows of the other heads, and on
     properties that hold at any size."""
     q, k, v = make_inputs(w.B, w.H, w.G, w.S, seed=0)
     o, lse = gq.fwd(q.cuda(), k.cuda(), v.cuda(), causal=w.causal, window=w.window,
-                    n_sink=w.n_sink, scale=w.scale)
+                    n_sink=w.n_sink, scale=w.scale, score_bound=score_bound)
     torch.cuda.synchronize()
     assert gq.gqa_attn_last_device_status() == gq.GQA_OK
     assert torch.isfinite(o).all() and torch.isfinite(lse).all()
@@ -91,6 +97,14 @@ def _run_sampled(w, n_rows=48, extra=()):
     R = w.H // w.G
     v_rep = v.cuda().repeat_interleave(R, dim=1)
     assert torch.equal(o[:, :, 0], v_rep[:, :, 0])
+    mask = dict(causal=w.causal, window=w.window, n_sink=w.n_sink, scale=w.scale)
+    for b, g in groups:
+        heads = slice(g * R, (g + 1) * R)
+        ro, rl = oracle.attn_fwd(to64(q[b:b + 1, heads]), to64(k[b:b + 1, g:g + 1]),
+                                 to64(v[b:b + 1, g:g + 1]), **mask)
+        check_close(f"O[b{b},g{g}]", to64(o[b:b + 1, heads]), ro)
+        check_close(f"LSE[b{b},g{g}]", to64(lse[b:b + 1, heads]), rl, max_abs=LSE_ABS,
+                    mean_abs=None, bf16_out=False)
     rows = sample_rows(w.B, w.H, w.S, n_rows, extra=[(0, w.H - 1, w.S - 1), *extra])
     got_o = np.stack([to64(o[b, h, i]) for b, h, i in rows])
     got_l = np.array([float(lse[b, h, i]) for b, h, i in rows])
@@ -104,9 +118,7 @@ def _run_sampled(w, n_rows=48, extra=()):
         qs = to64(q[b:b + 1, h:h + 1])
         ks = to64(k[b:b + 1, g:g + 1])
         vs = to64(v[b:b + 1, g:g + 1])
-        ro, rl = oracle.attn_fwd_rows(qs, ks, vs, [(0, 0, i) for _, i in items],
-                                      causal=w.causal, window=w.window, n_sink=w.n_sink,
-                                      scale=w.scale)
+        ro, rl = oracle.attn_fwd_rows(qs, ks, vs, [(0, 0, i) for _, i in items], **mask)
         for (t, _), a, c in zip(items, ro, rl):
             ref_o[t] = a
             ref_l[t] = c
@@ -114,12 +126,19 @@ def _run_sampled(w, n_rows=48, extra=()):
     check_close("LSE(sampled)", got_l, ref_l, max_abs=LSE_ABS, mean_abs=None, bf16_out=False)
 
 
-def test_wide_workload_sampled():
-    _run_sampled(WORKLOADS["wide_b1_h128_g16_s8192"])
+@pytest.mark.parametrize("score_bound", [False, True], ids=["plain", "bound"])
+def test_wide_workload_groups(score_bound):
+    """B1 H128 G16 S8192 (the benchmark's forward): the first and last kv
+    groups whole (8 heads x 8192 rows each), through both forward paths."""
+    w = WORKLOADS["wide_b1_h128_g16_s8192"]
+    _run_sampled(w, groups=[(0, 0), (0, w.G - 1)], score_bound=score_bound)
 
 
-def test_window_workload_sampled():
-    _run_sampled(WORKLOADS["window_b1_h128_g16_s32768_w4096_sink128"])
+def test_window_workload_group():
+    """B1 H128 G16 S32768, window 4096 + 128 sinks: the last kv group whole
+    (8 heads x 32768 rows), plus sampled rows of the others."""
+    w = WORKLOADS["window_b1_h128_g16_s32768_w4096_sink128"]
+    _run_sampled(w, groups=[(0, w.G - 1)])
 
 
 def test_model_workload_sampled():
@@ -153,21 +172,22 @@ def _oracle_check(q, k, v, o, lse, **mask):
     check_close("LSE", to64(lse), rl, max_abs=LSE_ABS, mean_abs=None, bf16_out=False)
 
 
-def test_key_norm_prepass_record():
-    """The workspace holds, per kv head, 4 partial maxima: each the largest
-    |k_j|^2 of its slice of ceil(S / 4) keys (float64 reference from the same
-    bf16 keys)."""
-    B, H, G, S = 2, 8, 4, 777
+@pytest.mark.parametrize("S", [777, 20, 4100])
+def test_key_norm_prepass_record(S):
+    """The workspace holds, per kv head, 32 partial maxima: each the largest
+    |k_j|^2 of its slice of ceil(S / 32) keys, 0 for an empty slice (float64
+    reference from the same bf16 keys)."""
+    B, H, G, P = 2, 8, 4, 32
     q, k, v = make_inputs(B, H, G, S, seed=5)
-    ws = torch.zeros(gq.gqa_attn_fwd_workspace_size(B, H, G, S, 64), dtype=torch.uint8,
-                     device="cuda")
-    gq.fwd(q.cuda(), k.cuda(), v.cuda(), workspace=ws)
+    ws = torch.full((gq.gqa_attn_fwd_workspace_size(B, H, G, S, 64),), 0xff, dtype=torch.uint8,
+                    device="cuda")
+    gq.fwd(q.cuda(), k.cuda(), v.cuda(), workspace=ws, score_bound=True)
     torch.cuda.synchronize()
-    rec = ws.view(torch.float32).view(B * G, 4).cpu().numpy().astype(np.float64)
+    rec = ws.view(torch.float32).view(B * G, P).cpu().numpy().astype(np.float64)
     ref = (to64(k) ** 2).sum(-1).reshape(B * G, S)
-    per = -(-S // 4)
-    parts = np.array([[ref[bg, p * per:(p + 1) * per].max() for p in range(4)]
-                      for bg in range(B * G)])
+    per = -(-S // P)
+    parts = np.array([[ref[bg, p * per:(p + 1) * per].max() if p * per < S else 0.0
+                       for p in range(P)] for bg in range(B * G)])
     np.testing.assert_allclose(rec, parts, rtol=1e-5)
 
 
@@ -180,7 +200,7 @@ def test_plain_entry_point(window, n_sink):
     o = torch.empty_like(q)
     lse = torch.empty((B, H, S), dtype=torch.float32, device="cuda")
     assert gq.gqa_attn_fwd(q, k, v, o, lse, B, H, G, S, 64, 1, window, n_sink, 0.125) == gq.GQA_OK
-    o2, l2 = gq.fwd(q, k, v, window=window, n_sink=n_sink)
+    o2, l2 = gq.fwd(q, k, v, window=window, n_sink=n_sink, score_bound=True)
     torch.cuda.synchronize()
     assert gq.gqa_attn_last_device_status() == gq.GQA_OK
     _oracle_check(q, k, v, o, lse, window=window, n_sink=n_sink)
@@ -196,7 +216,7 @@ def test_score_bound_mixed_warps():
     B, H, G, S = 1, 4, 2, 1100
     q, k, v = make_inputs(B, H, G, S, seed=11)
     q[:, :, torch.arange(S) % 128 < 32] *= 8  # exact in bf16
-    o, lse = gq.fwd(q.cuda(), k.cuda(), v.cuda())
+    o, lse = gq.fwd(q.cuda(), k.cuda(), v.cuda(), score_bound=True)
     torch.cuda.synchronize()
     assert gq.gqa_attn_last_device_status() == gq.GQA_OK
     _oracle_check(q, k, v, o, lse)
@@ -209,7 +229,8 @@ def test_score_bound_loose_everywhere(window, n_sink):
     B, H, G, S = 1, 4, 2, 900
     q, k, v = make_inputs(B, H, G, S, seed=13)
     k[:, :, S // 3] *= 8  # exact in bf16
-    o, lse = gq.fwd(q.cuda(), k.cuda(), v.cuda(), window=window, n_sink=n_sink)
+    o, lse = gq.fwd(q.cuda(), k.cuda(), v.cuda(), window=window, n_sink=n_sink,
+                    score_bound=True)
     torch.cuda.synchronize()
     assert gq.gqa_attn_last_device_status() == gq.GQA_OK
     _oracle_check(q, k, v, o, lse, window=window, n_sink=n_sink)
@@ -223,7 +244,7 @@ def test_score_bound_growing_keys():
     q, k, v = make_inputs(B, H, G, S, seed=17)
     ramp = 1.0 + 3.0 * torch.arange(S, dtype=torch.float32) / S
     k = (k.float() * ramp[None, None, :, None]).to(torch.bfloat16)
-    o, lse = gq.fwd(q.cuda(), k.cuda(), v.cuda())
+    o, lse = gq.fwd(q.cuda(), k.cuda(), v.cuda(), score_bound=True)
     torch.cuda.synchronize()
     assert gq.gqa_attn_last_device_status() == gq.GQA_OK
     _oracle_check(q, k, v, o, lse)
@@ -235,7 +256,7 @@ def test_score_bound_tiny_queries():
     B, H, G, S = 1, 2, 1, 600
     q, k, v = make_inputs(B, H, G, S, seed=19)
     q = (q.float() * 2.0 ** -20).to(torch.bfloat16)
-    o, lse = gq.fwd(q.cuda(), k.cuda(), v.cuda())
+    o, lse = gq.fwd(q.cuda(), k.cuda(), v.cuda(), score_bound=True)
     torch.cuda.synchronize()
     assert gq.gqa_attn_last_device_status() == gq.GQA_OK
     _oracle_check(q, k, v, o, lse)
