@@ -11,16 +11,27 @@
 //   dQ_i  = scale sum_j dS_ij k_j
 //   dK_j  = scale sum_{h in group} sum_i dS_ij q_i,    dV_j = sum_{h in group} sum_i P_ij dO_i
 //
-// Three launches on the caller's stream:
-//   prep   D (fp32), LSE * log2(e) (fp32), and the fp32 dQ accumulator cleared;
-//   main   one CTA per (b, kv head g, 128-key tile): for each of the R query
-//          heads of g and each query tile that sees the key tile (a "step"),
-//          on tcgen05:
-//            S^T  = K Q^T       dP^T = V dO^T           (TMEM, fp32)
-//            P^T (bf16) -> TMEM; dS (bf16) -> shared memory, which serves as
-//            dS^T (K-major) for dK and as dS (MN-major) for dQ
-//            dV  += P^T dO      dK  += dS^T Q           (TMEM, fp32, whole CTA life)
-//            dQ   = dS K        -> fp32 TMA reduce-add into the accumulator
+// Four launches on the caller's stream (after clearing one int per kv group):
+//   prep   per query row i: the power of two 2^e_i that brings max_c |dO_ic|
+//          into [2^14, 2^15); an fp16 copy dO' = dO * 2^e_i (exact: fp16 holds
+//          every bf16 value within 2^29 of the row's largest); D' = 2^e_i D
+//          (fp32); LSE * log2(e) + e_i (fp32); E_g = min_i e_i over kv group g;
+//          the fp32 dQ accumulator cleared;
+//   shift  LSE * log2(e) + e_i - E_g, so that the recomputed probabilities come
+//          out as P' = P 2^(E_g - e_i) <= P;
+//   main   one CTA per (b, kv head g, 128-key tile): V' = V 2^ev_j in fp16 in
+//          shared memory (one power of two per key row, taken once); then for
+//          each of the R query heads of g and each query tile that sees the key
+//          tile (a "step"), on tcgen05:
+//            S^T  = K Q^T  (bf16)      dP''^T = V' dO'^T  (fp16)   (TMEM, fp32)
+//            P'^T (fp16) -> TMEM; dS' = P' (dP'' 2^-ev_j - D') = 2^E_g dS
+//            (bf16) -> shared memory, which serves as dS'^T (K-major) for dK
+//            and as dS' (MN-major) for dQ
+//            dV  += P'^T dO' (fp16)   dK  += dS'^T Q (bf16)   (TMEM, fp32, whole CTA life)
+//            dQ   = dS' K (bf16)       -> fp32 TMA reduce-add into the accumulator
+//          (every accumulator holds 2^E_g times its gradient; the epilogues
+//          take the power of two back out exactly).  The fp16 P' and dO' give
+//          the dV product 11-bit operands where bf16 would give 8;
 //          S^T, dP^T of step n+1 are issued as soon as the P/dS warps have read
 //          step n into registers, so those warps overlap step n's dV, dK, dQ;
 //          P^T and dS are handed over separately (dV starts while dS is still
@@ -31,11 +42,12 @@
 //          step n - 1's dK and dQ still read the other one.
 //          dK, dV are summed over the group's heads inside the CTA
 //          (deterministic) and written once as bf16;
-//   convert dQ = bf16(scale * accumulator).
+//   convert dQ = bf16(scale * 2^-E_g * accumulator).
 #pragma once
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 #include <math_constants.h>
@@ -88,6 +100,7 @@ constexpr int SM_BARS = SM_VEC + NSTAGE * 2 * BQ * 4;
 
 struct Bars {
   uint64_t kv_full;
+  uint64_t v_ready;   // V' (fp16) written over V in shared memory (128 threads of P/dS group 0)
   uint64_t qdo_full[NSTAGE];
   uint64_t qdo_empty[NSTAGE];
   uint64_t st_full;   // S^T, dP^T of the step ready (issuer A commit)
@@ -147,8 +160,9 @@ struct MainParams {
   float scale;
   float scale_log2;
   int n_ktiles;
-  const float *lse2;  // [B*H][S_pad]
-  const float *delta; // [B*H][S_pad]
+  const float *lse2;  // [B*H][S_pad]  LSE log2(e) + e_i - E_g
+  const float *delta; // [B*H][S_pad]  D' = 2^e_i D
+  const int *emin;    // [B*G]         E_g
   GradOut *dk;
   GradOut *dv;
   int *status;
@@ -158,10 +172,47 @@ enum : int { kTimeoutCode = -9 };
 
 __host__ __device__ inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
-inline size_t workspace_bytes(int B, int H, int S) {
-  const size_t rows = static_cast<size_t>(B) * H;
-  const size_t s_pad = static_cast<size_t>(round_up(S, BQ));
-  return rows * S * HD * sizeof(float) + 2 * rows * s_pad * sizeof(float);
+// Scratch of one backward call, carved from the caller's workspace (every
+// piece starts on a 16-byte boundary):
+//   dq_acc  fp32 [B*H][S][64]     lse2, delta  fp32 [B*H][S_pad]
+//   dout_h  fp16 [B*H][S][64]     emin  int32 [B*G] (rounded up to 16 bytes)
+struct Workspace {
+  float *dq_acc;
+  float *lse2;
+  float *delta;
+  __half *dout_h;
+  int *emin;
+};
+
+inline size_t workspace_bytes(int B, int H, int G, int S) {
+  const size_t rows = static_cast<size_t>(B) * H * S;
+  const size_t rows_pad = static_cast<size_t>(B) * H * round_up(S, BQ);
+  const size_t groups = (static_cast<size_t>(B) * G * sizeof(int) + 15) / 16 * 16;
+  return rows * HD * sizeof(float) + 2 * rows_pad * sizeof(float) + rows * HD * sizeof(__half) +
+         groups;
+}
+
+inline Workspace carve_workspace(void *ws, int B, int H, int S) {
+  const size_t rows = static_cast<size_t>(B) * H * S;
+  const size_t rows_pad = static_cast<size_t>(B) * H * round_up(S, BQ);
+  Workspace w;
+  w.dq_acc = static_cast<float *>(ws);
+  w.lse2 = w.dq_acc + rows * HD;
+  w.delta = w.lse2 + rows_pad;
+  w.dout_h = reinterpret_cast<__half *>(w.delta + rows_pad);
+  w.emin = reinterpret_cast<int *>(w.dout_h + rows * HD);
+  return w;
+}
+
+// The row exponent e with 2^e * m in [2^14, 2^15) for a finite normal m =
+// max |x| of a row, clamped to [-kEClamp, kEClamp]; rows of zeros (and of
+// subnormals) take the largest shift.  2^e is then exact in fp32 and the
+// scaled row fits fp16 without overflow.
+constexpr int kEClamp = 120;
+__device__ __forceinline__ int row_exponent(float m) {
+  const int be = (__float_as_int(m) >> 23) & 0xff;
+  const int e = be == 0 ? kEClamp : 141 - be;  // 14 - (be - 127)
+  return max(-kEClamp, min(kEClamp, e));
 }
 
 // Query tiles [qlo, qhi] that see at least one key of key tile kb.
@@ -198,83 +249,149 @@ __device__ __forceinline__ bool pair_needs_mask(int qb, int kb, const MainParams
 
 // ------------------------------------------------------------------- prep
 
-// D = rowsum(dO * O) and LSE2 = LSE * log2(e) over [B*H][S_pad] (zeros past S),
-// and the fp32 dQ accumulator [B*H][S][64] set to zero.  Eight lanes share one
-// 128-byte row, so a warp covers four rows per pass with coalesced 16-B loads.
+// Per row r of [B*H][S_pad] (rows past S: D' = LSE2 = 0, no dO' row):
+//   e_r = row_exponent(max_c |dO_rc|),  dO'_r = fp16(dO_r 2^e_r),
+//   D'_r = 2^e_r rowsum(dO_r * O_r),  LSE2_r = LSE_r log2(e) + e_r,
+//   E_g = min e_r over the rows of kv group g (emin cleared to a large value
+//   before the launch), and the fp32 dQ accumulator rows cleared.
+// Each block takes one contiguous range of rows (a multiple of 64); eight
+// lanes share one 128-byte row, so a warp covers eight rows per pass (two
+// groups of four whose loads are all issued before either is used).  Eight
+// consecutive rows always lie in one (b, h), so a warp folds its rows' e into
+// one running minimum per kv group and flushes it with one atomicMin when the
+// group changes.
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__restrict__ o,
                                                        const __nv_bfloat16 *__restrict__ dout,
                                                        const float *__restrict__ lse,
                                                        float *__restrict__ lse2,
                                                        float *__restrict__ delta,
                                                        float *__restrict__ dq_acc,
-                                                       long long rows_pad, int S, int S_pad) {
+                                                       __half *__restrict__ dout_h,
+                                                       int *__restrict__ emin,
+                                                       long long rows_pad, int S, int S_pad,
+                                                       int H, int G, int R) {
   const int lane = threadIdx.x & 31;
-  const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  const int warp = threadIdx.x >> 5;
   const int sub = lane >> 3;  // row within a group of four
   const int ch = lane & 7;    // 16-byte chunk of the row
-  // eight rows per warp and iteration, as two groups of four whose loads are
-  // all issued before either is used (more bytes in flight per warp)
-  for (long long r0 = warp * 8; r0 < rows_pad; r0 += nwarps * 8) {
+  const long long per_block =
+      ((rows_pad + gridDim.x - 1) / gridDim.x + 63) / 64 * 64;
+  const long long r_begin = static_cast<long long>(blockIdx.x) * per_block;
+  const long long r_end = min(rows_pad, r_begin + per_block);
+  int cur_g = -1, cur_min = 0x7fffffff;
+  for (long long r0 = r_begin + warp * 8; r0 < r_end; r0 += 64) {  // warp-uniform bound
+    const long long bh = r0 / S_pad;
+    const int grp = static_cast<int>(bh / H) * G + static_cast<int>(bh % H) / R;
     long long src[2];
     uint4 a[2], c[2];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-      const long long r = r0 + 4 * u + sub;
+      const int i = static_cast<int>(r0 + 4 * u + sub - bh * S_pad);
       src[u] = -1;
       a[u] = c[u] = make_uint4(0, 0, 0, 0);
-      if (r < rows_pad) {
-        const long long bh = r / S_pad;
-        const int i = static_cast<int>(r - bh * S_pad);
-        if (i < S) {
-          src[u] = bh * S + i;
-          a[u] = reinterpret_cast<const uint4 *>(o + src[u] * HD)[ch];
-          c[u] = reinterpret_cast<const uint4 *>(dout + src[u] * HD)[ch];
-        }
+      if (i < S) {
+        src[u] = bh * S + i;
+        a[u] = reinterpret_cast<const uint4 *>(o + src[u] * HD)[ch];
+        c[u] = reinterpret_cast<const uint4 *>(dout + src[u] * HD)[ch];
       }
     }
+    int e_min = 0x7fffffff;
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const long long r = r0 + 4 * u + sub;
-      float acc = 0.f;
+      float acc = 0.f, m = 0.f;
+      float y[8];
       const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&a[u]);
       const __nv_bfloat162 *c2 = reinterpret_cast<const __nv_bfloat162 *>(&c[u]);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float2 x = __bfloat1622float2(a2[e]);
-        const float2 y = __bfloat1622float2(c2[e]);
-        acc = fmaf(x.x, y.x, acc);
-        acc = fmaf(x.y, y.y, acc);
-      }
-      if (src[u] >= 0) {
-        float4 *z = reinterpret_cast<float4 *>(dq_acc + src[u] * HD) + 2 * ch;
-        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float2 d = __bfloat1622float2(c2[e]);
+        acc = fmaf(x.x, d.x, acc);
+        acc = fmaf(x.y, d.y, acc);
+        m = fmaxf(m, fmaxf(fabsf(d.x), fabsf(d.y)));
+        y[2 * e] = d.x;
+        y[2 * e + 1] = d.y;
       }
       acc += __shfl_xor_sync(0xffffffffu, acc, 1);
       acc += __shfl_xor_sync(0xffffffffu, acc, 2);
       acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+      const int er = row_exponent(m);
+      const float sc = exp2i(er);
+      if (src[u] >= 0) {
+        float4 *z = reinterpret_cast<float4 *>(dq_acc + src[u] * HD) + 2 * ch;
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        uint4 hw;
+        hw.x = pack_f16x2(y[0] * sc, y[1] * sc);
+        hw.y = pack_f16x2(y[2] * sc, y[3] * sc);
+        hw.z = pack_f16x2(y[4] * sc, y[5] * sc);
+        hw.w = pack_f16x2(y[6] * sc, y[7] * sc);
+        reinterpret_cast<uint4 *>(dout_h + src[u] * HD)[ch] = hw;
+        e_min = min(e_min, er);
+      }
       if (r < rows_pad && ch == 0) {
-        delta[r] = src[u] >= 0 ? acc : 0.f;
-        lse2[r] = src[u] >= 0 ? lse[src[u]] * 1.4426950408889634f : 0.f;
+        delta[r] = src[u] >= 0 ? acc * sc : 0.f;
+        lse2[r] = src[u] >= 0 ? fmaf(lse[src[u]], 1.4426950408889634f, static_cast<float>(er)) : 0.f;
       }
     }
+    // the warp's eight rows: one minimum
+#pragma unroll
+    for (int o2 = 8; o2 < 32; o2 <<= 1) e_min = min(e_min, __shfl_xor_sync(0xffffffffu, e_min, o2));
+    if (grp != cur_g) {
+      if (lane == 0 && cur_g >= 0 && cur_min != 0x7fffffff) atomicMin(emin + cur_g, cur_min);
+      cur_g = grp;
+      cur_min = e_min;
+    } else {
+      cur_min = min(cur_min, e_min);
+    }
+  }
+  if (lane == 0 && cur_g >= 0 && cur_min != 0x7fffffff) atomicMin(emin + cur_g, cur_min);
+}
+
+// LSE2_r -= E_g for every row r of [B*H][S_pad] (four rows per thread and
+// pass; S_pad is a multiple of 4, so the four share one (b, h)).
+__global__ void __launch_bounds__(256) bwd_shift_kernel(float *__restrict__ lse2,
+                                                        const int *__restrict__ emin,
+                                                        long long n4, int S_pad, int H, int G,
+                                                        int R) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < n4;
+       e += stride) {
+    const long long bh = 4 * e / S_pad;
+    const int grp = static_cast<int>(bh / H) * G + static_cast<int>(bh % H) / R;
+    const float E = static_cast<float>(emin[grp]);
+    float4 x = reinterpret_cast<float4 *>(lse2)[e];
+    x.x -= E;
+    x.y -= E;
+    x.z -= E;
+    x.w -= E;
+    reinterpret_cast<float4 *>(lse2)[e] = x;
   }
 }
 
 // ---------------------------------------------------------------- convert
 
-// dq = bf16(scale * dq_acc), eight elements per thread and pass.
+// dq = bf16(scale * 2^-E_g * dq_acc), eight elements (an eighth of a row) per
+// thread and pass.
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float *__restrict__ dq_acc,
                                                              GradOut *__restrict__ dq,
-                                                             long long n8, float scale) {
+                                                             const int *__restrict__ emin,
+                                                             long long n8, float scale, int S,
+                                                             int H, int G, int R) {
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < n8;
        e += stride) {
+    const long long bh = (e >> 3) / S;
+    const int grp = static_cast<int>(bh / H) * G + static_cast<int>(bh % H) / R;
+    const float f = scale * exp2i(-emin[grp]);
     const uint4 a = reinterpret_cast<const uint4 *>(dq_acc)[2 * e];
     const uint4 b = reinterpret_cast<const uint4 *>(dq_acc)[2 * e + 1];
     const uint32_t v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    store_grad8(dq + 8 * e, v, scale);
+    store_grad8(dq + 8 * e, v, f);
   }
 }
 
@@ -299,9 +416,11 @@ __device__ __forceinline__ uint32_t visible_bits(int cb, int i0, int j, const Ma
 
 // P and dS of 32 query columns [cb, cb+32) for this thread's key row; `vbits`
 // holds their visibility when the tile pair needs the mask.
+// P' goes out as fp16 pairs (pp), dS' = P' (dP'' cv - D') as bf16 pairs (pd);
+// cv = 2^-ev_j takes this key row's V scale out of dP''.
 __device__ __forceinline__ void p_ds_chunk(const uint32_t (&sr)[32], const uint32_t (&dr)[32],
                                            const float *lse2, const float *dlt, int cb,
-                                           uint32_t vbits, bool masked, float sl2,
+                                           uint32_t vbits, bool masked, float sl2, float cv,
                                            uint32_t (&pp)[16], uint32_t (&pd)[16]) {
   // sub-chunks of 8 query columns: two broadcast 16-byte shared loads for the
   // 8 LSE2 and two for the 8 D values, so few values are live at once
@@ -331,15 +450,15 @@ __device__ __forceinline__ void p_ds_chunk(const uint32_t (&sr)[32], const uint3
     for (int e = 0; e < 8; e += 2) {
       float y0, y1;
       f32x2_split(mul_f32x2(f32x2(pv[e], pv[e + 1]),
-                            add_f32x2(f32x2(__uint_as_float(dr[8 * sc + e]), __uint_as_float(dr[8 * sc + e + 1])),
-                                      f32x2(-d8[e], -d8[e + 1]))),
+                            fma_f32x2(f32x2(__uint_as_float(dr[8 * sc + e]), __uint_as_float(dr[8 * sc + e + 1])),
+                                      f32x2(cv, cv), f32x2(-d8[e], -d8[e + 1]))),
                   y0, y1);
       dv[e] = y0;
       dv[e + 1] = y1;
     }
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      pp[4 * sc + e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
+      pp[4 * sc + e] = pack_f16x2(pv[2 * e], pv[2 * e + 1]);
       pd[4 * sc + e] = pack_bf16x2(dv[2 * e], dv[2 * e + 1]);
     }
   }
@@ -373,6 +492,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
+    mbar_init(&bars->v_ready, 128);
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(&bars->qdo_full[s], 1);
       mbar_init(&bars->qdo_empty[s], 1);
@@ -448,7 +568,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_wait_drain(&bars->qdo_full[n % NSTAGE], (n / NSTAGE) & 1);
     } else if (warp == 1 && lane == 0) {
       // ================================================= issuer A: S^T, dP^T
-      const uint32_t id_nn = idesc_bf16_f32(128, 128, false, false);
+      const uint32_t id_nn = idesc_bf16_f32(128, 128, false, false);    // S^T: K, Q bf16
+      const uint32_t id_nn16 = idesc_fp16_f32(128, 128, false, false);  // dP''^T: V', dO' fp16
       const uint64_t k_kmaj = sdesc_sw128(smem_u32(smem + SM_K), 16, 1024);
       const uint64_t v_kmaj = sdesc_sw128(smem_u32(smem + SM_V), 16, 1024);
       const uint32_t q_addr = smem_u32(smem + SM_Q);
@@ -457,6 +578,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int n = 0; ok && n < nsteps; ++n) {
         const int st = n % NSTAGE;
         if (!mbar_wait(&bars->qdo_full[st], (n / NSTAGE) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        // V' (fp16) must be in place before the first dP''^T
+        if (n == 0 && !mbar_wait(&bars->v_ready, 0, ab, p.status, kTimeoutCode)) { ok = false; break; }
         // the P/dS warps must have read the previous step's S^T and dP^T
         if (n > 0 && !mbar_wait(&bars->st_free, (n - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
         GQA_TRACE_EVENT(1, 2, n);
@@ -468,7 +591,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           mma_bf16_ss(tbase + C_S, k_kmaj + 2 * ks, q_kmaj + 2 * ks, id_nn, ks > 0);
 #pragma unroll
         for (int ks = 0; ks < HD / 16; ++ks)
-          mma_bf16_ss(tbase + C_DP, v_kmaj + 2 * ks, do_kmaj + 2 * ks, id_nn, ks > 0);
+          mma_bf16_ss(tbase + C_DP, v_kmaj + 2 * ks, do_kmaj + 2 * ks, id_nn16, ks > 0);
         mma_commit(&bars->st_full);
         GQA_TRACE_EVENT(1, 3, n);
       }
@@ -476,8 +599,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (!ok) mbar_wait_drain(&bars->a_done, 0);
     } else if (warp == 3 && lane == 0) {
       // ============================================ issuer B: dV, dK, dQ
-      const uint32_t id_ts = idesc_bf16_f32(128, 64, false, true);  // dV, dK
-      const uint32_t id_dq = idesc_bf16_f32(128, 64, true, true);   // dQ
+      const uint32_t id_dv = idesc_fp16_f32(128, 64, false, true);  // dV: P'^T, dO' fp16
+      const uint32_t id_dk = idesc_bf16_f32(128, 64, false, true);  // dK: dS'^T, Q bf16
+      const uint32_t id_dq = idesc_bf16_f32(128, 64, true, true);   // dQ: dS', K bf16
       const uint32_t q_addr = smem_u32(smem + SM_Q);
       const uint32_t do_addr = smem_u32(smem + SM_DO);
       const uint32_t ds_addr = smem_u32(smem + SM_DS);
@@ -495,7 +619,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // dV += P^T dO: P^T from TMEM (16 queries = 8 packed columns per step)
 #pragma unroll
         for (int ks = 0; ks < BQ / 16; ++ks)
-          mma_bf16_ts(tbase + C_DV, tbase + C_PT + ks * 8, do_mn + ks * 128, id_ts, (n > 0 || ks > 0));
+          mma_bf16_ts(tbase + C_DV, tbase + C_PT + ks * 8, do_mn + ks * 128, id_dv, (n > 0 || ks > 0));
         mma_commit(&bars->pt_free);
         if (!mbar_wait(&bars->ds_ready, n & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
         tc_fence_after_sync();
@@ -504,7 +628,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int ks = 0; ks < BQ / 16; ++ks) {
           const uint64_t a = sdesc_sw128(ds_t + (ks >> 2) * TILE_BYTES + (ks & 3) * 32, 16, 1024);
-          mma_bf16_ss(tbase + C_DK, a, q_mn + ks * 128, id_ts, (n > 0 || ks > 0));
+          mma_bf16_ss(tbase + C_DK, a, q_mn + ks * 128, id_dk, (n > 0 || ks > 0));
         }
         mma_commit(&bars->qdo_empty[st]);
         if (n > 0 && !mbar_wait(&bars->dq_free, (n - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
@@ -532,8 +656,46 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // this thread's key row of its group's 64-query half of a dS tile; chunk c
     // of 8 queries sits at (c ^ (r & 7)) (128-byte swizzle)
     uint8_t *ds_row0 = smem + SM_DS + wg * TILE_BYTES + r * 128;
-    bool ok = true;
-    for (int n = 0; n < nsteps; ++n) {
+    // V' = fp16(V 2^ev) in place, one key row per thread: both groups read the
+    // row and take cv = 2^-ev, group 0 writes it back once every P/dS thread
+    // has read (a barrier every one of the 256 threads reaches, also on abort).
+    float cv = 1.f;
+    bool ok = mbar_wait_warp(&bars->kv_full, 0, ab, p.status, kTimeoutCode);
+    {
+      uint8_t *vrow = smem + SM_V + r * 128;  // 16-byte chunk c at (c ^ (r & 7))
+      uint4 vv[8];
+      float m = 0.f;
+      if (ok) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          vv[c] = *reinterpret_cast<const uint4 *>(vrow + ((c ^ (r & 7)) << 4));
+          const uint32_t w4[4] = {vv[c].x, vv[c].y, vv[c].z, vv[c].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w4[e] << 16)),
+                               fabsf(__uint_as_float(w4[e] & 0xffff0000u))));
+        }
+      }
+      const int ev = row_exponent(m);
+      cv = exp2i(-ev);
+      ok = named_bar_and(2, 256, ok);
+      if (ok && wg == 0) {
+        const float sc = exp2i(ev);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t w4[4] = {vv[c].x, vv[c].y, vv[c].z, vv[c].w};
+          uint32_t h4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            h4[e] = pack_f16x2(__uint_as_float(w4[e] << 16) * sc,
+                               __uint_as_float(w4[e] & 0xffff0000u) * sc);
+          *reinterpret_cast<uint4 *>(vrow + ((c ^ (r & 7)) << 4)) = make_uint4(h4[0], h4[1], h4[2], h4[3]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars->v_ready);
+      }
+    }
+    for (int n = 0; ok && n < nsteps; ++n) {
       const int st = n % NSTAGE;
       const int qb = qlo + n % nqt;
       const int i0 = qb * BQ;
@@ -552,7 +714,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         reg_fence(sr);
         reg_fence(dr);
         p_ds_chunk(sr, dr, lse2, dlt, 64 * wg, masked ? visible_bits(64 * wg, i0, j, p) : 0u,
-                   masked, sl2, pp0, pd0);
+                   masked, sl2, cv, pp0, pd0);
       }
       // dS goes to the step's tile as soon as each half of the row is computed:
       // the tile was last read by the dK and dQ products of step n - 2
@@ -577,7 +739,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_arrive(&bars->st_free);
         if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 9, n);
         p_ds_chunk(sr, dr, lse2, dlt, 64 * wg + 32,
-                   masked ? visible_bits(64 * wg + 32, i0, j, p) : 0u, masked, sl2, pp1, pd1);
+                   masked ? visible_bits(64 * wg + 32, i0, j, p) : 0u, masked, sl2, cv, pp1, pd1);
       }
 #pragma unroll
       for (int q8 = 0; q8 < 4; ++q8)
@@ -611,7 +773,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       reg_fence(a0);
       reg_fence(a1);
       if (j < p.S && GQA_CHECK(p.status, b < p.B && g < p.G)) {
-        const float f = wg == 0 ? 1.f : p.scale;
+        // the accumulators hold 2^E_g times the gradients
+        const float unscale = exp2i(-p.emin[b * p.G + g]);
+        const float f = wg == 0 ? unscale : p.scale * unscale;
         GradOut *dst = (wg == 0 ? p.dv : p.dk) + ((static_cast<size_t>(b) * p.G + g) * p.S + j) * HD;
 #pragma unroll
         for (int c = 0; c < 4; ++c) store_grad8(dst + 8 * c, a0 + 8 * c, f);
@@ -714,21 +878,20 @@ inline int encode_3d(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap *map,
              : -1;
 }
 
-// Launches prep, main and convert on `st`.  Returns a gqa_status value.
+// Launches prep, shift, main and convert on `st` (after clearing E).
+// Returns 0, -2 (sizes the kernels cannot index) or -8 (CUDA failure).
 inline int launch(const Problem &pr, const void *q, const void *k, const void *v, const void *o,
                   const void *dout, const float *lse, void *dq, void *dk, void *dv, void *ws,
                   int *status, int sm_count, PFN_cuTensorMapEncodeTiled_v12000 enc,
                   cudaStream_t st) {
-  const int B = pr.B, H = pr.H, G = pr.G, S = pr.S;
+  const int B = pr.B, H = pr.H, G = pr.G, S = pr.S, R = H / G;
   const int S_pad = round_up(S, BQ);
   // every size check comes before the first launch
   const long long units = static_cast<long long>((S + BK - 1) / BK) * B * G;
   if (units > 0x7fffffffLL) return -2;
   const long long rows = static_cast<long long>(B) * H * S;
   const long long rows_pad = static_cast<long long>(B) * H * S_pad;
-  float *dq_acc = static_cast<float *>(ws);
-  float *lse2 = dq_acc + rows * HD;
-  float *delta = lse2 + rows_pad;
+  const Workspace w = carve_workspace(ws, B, H, S);
 
   CUtensorMap tq, tk, tv, tdo, tdq;
   if (encode_3d(enc, &tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, HD, S,
@@ -737,24 +900,33 @@ inline int launch(const Problem &pr, const void *q, const void *k, const void *v
                 static_cast<uint64_t>(B) * G, HD, BK) ||
       encode_3d(enc, &tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v, HD, S,
                 static_cast<uint64_t>(B) * G, HD, BK) ||
-      encode_3d(enc, &tdo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dout, HD, S,
+      encode_3d(enc, &tdo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.dout_h, HD, S,
                 static_cast<uint64_t>(B) * H, HD, BQ) ||
-      encode_3d(enc, &tdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dq_acc, HD, S,
+      encode_3d(enc, &tdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, w.dq_acc, HD, S,
                 static_cast<uint64_t>(B) * H, 32, BQ)) {
     set_error_detail("cuTensorMapEncodeTiled rejected a backward tensor map");
     return -8;
   }
 
+  // E_g starts above any row exponent (0x7f7f7f7f), so atomicMin takes the first value
+  if (cuda_failed(cudaMemsetAsync(w.emin, 0x7f, static_cast<size_t>(B) * G * sizeof(int), st),
+                  "cudaMemsetAsync(backward group exponents)"))
+    return -8;
   {
-    const long long warps_needed = (rows_pad + 7) / 8;
-    long long blocks = (warps_needed * 32 + 255) / 256;
+    long long blocks = (rows_pad + 63) / 64;
     blocks = blocks < 1 ? 1 : (blocks > 8LL * sm_count ? 8LL * sm_count : blocks);
     timing_begin(1, st);
     bwd_prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
         static_cast<const __nv_bfloat16 *>(o), static_cast<const __nv_bfloat16 *>(dout), lse,
-        lse2, delta, dq_acc, rows_pad, S, S_pad);
-    timing_end(1, st);
+        w.lse2, w.delta, w.dq_acc, w.dout_h, w.emin, rows_pad, S, S_pad, H, G, R);
     if (cuda_failed(cudaGetLastError(), "launch of the backward prep kernel")) return -8;
+    const long long n4 = rows_pad / 4;
+    long long sblocks = (n4 + 255) / 256;
+    sblocks = sblocks < 1 ? 1 : (sblocks > 4LL * sm_count ? 4LL * sm_count : sblocks);
+    bwd_shift_kernel<<<static_cast<unsigned>(sblocks), 256, 0, st>>>(w.lse2, w.emin, n4, S_pad,
+                                                                      H, G, R);
+    timing_end(1, st);
+    if (cuda_failed(cudaGetLastError(), "launch of the backward shift kernel")) return -8;
   }
   {
     MainParams p{};
@@ -762,7 +934,7 @@ inline int launch(const Problem &pr, const void *q, const void *k, const void *v
     p.H = H;
     p.G = G;
     p.S = S;
-    p.R = H / G;
+    p.R = R;
     p.S_pad = S_pad;
     p.causal = pr.causal;
     p.window = pr.window;
@@ -770,8 +942,9 @@ inline int launch(const Problem &pr, const void *q, const void *k, const void *v
     p.scale = pr.scale;
     p.scale_log2 = pr.scale * 1.4426950408889634f;
     p.n_ktiles = (S + BK - 1) / BK;
-    p.lse2 = lse2;
-    p.delta = delta;
+    p.lse2 = w.lse2;
+    p.delta = w.delta;
+    p.emin = w.emin;
     p.dk = static_cast<GradOut *>(dk);
     p.dv = static_cast<GradOut *>(dv);
     p.status = status;
@@ -787,7 +960,7 @@ inline int launch(const Problem &pr, const void *q, const void *k, const void *v
     blocks = blocks < 1 ? 1 : (blocks > 8LL * sm_count ? 8LL * sm_count : blocks);
     timing_begin(3, st);
     bwd_dq_convert_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-        dq_acc, static_cast<GradOut *>(dq), n8, pr.scale);
+        w.dq_acc, static_cast<GradOut *>(dq), w.emin, n8, pr.scale, S, H, G, R);
     timing_end(3, st);
     if (cuda_failed(cudaGetLastError(), "launch of the dQ convert kernel")) return -8;
   }

@@ -250,7 +250,7 @@ int gqa_attn_fwd_ws(const void *q, const void *k, const void *v, void *o, float 
 
 size_t gqa_attn_bwd_workspace_size(int B, int H, int G, int S, int d) {
   if (check_common(B, H, G, S, d, 1, 0, 0, 1.f) != GQA_OK) return 0;
-  return gqa::bwd::workspace_bytes(B, H, S);
+  return gqa::bwd::workspace_bytes(B, H, G, S);
 }
 
 int gqa_attn_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
@@ -264,7 +264,7 @@ int gqa_attn_bwd(const void *q, const void *k, const void *v, const void *o, con
       !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
       (workspace && !aligned16(workspace)))
     return GQA_ERR_ALIGN;
-  const size_t need = gqa::bwd::workspace_bytes(B, H, S);
+  const size_t need = gqa::bwd::workspace_bytes(B, H, G, S);
   if (workspace && workspace_bytes < need) return GQA_ERR_WORKSPACE;
   DeviceState *ds = nullptr;
   if ((rc = device_state(&ds)) != GQA_OK) return rc;
@@ -305,7 +305,7 @@ int gqa_attn_bwd_noalloc(const void *q, const void *k, const void *v, const void
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
       !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return GQA_ERR_ALIGN;
-  if (gqa::bwd::workspace_bytes(B, H, S) > GQA_NOALLOC_SCRATCH_BYTES) return GQA_ERR_TOO_LARGE;
+  if (gqa::bwd::workspace_bytes(B, H, G, S) > GQA_NOALLOC_SCRATCH_BYTES) return GQA_ERR_TOO_LARGE;
   DeviceState *ds = nullptr;
   if ((rc = device_state(&ds)) != GQA_OK) return rc;
   int dev = 0;

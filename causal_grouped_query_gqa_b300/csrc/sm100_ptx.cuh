@@ -316,15 +316,25 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
-// Instruction descriptor of kind::f16 with bf16 A/B and fp32 accumulation:
-// D format f32 (bits 4-5 = 1), A = bf16 (7-9 = 1), B = bf16 (10-12 = 1),
-// A/B major-ness (bit 15 / 16: 0 = K-major, 1 = MN-major), N >> 3 (17-22),
-// M >> 4 (24-28).
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major,
-                                                      bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+// Instruction descriptor of kind::f16 with fp32 accumulation: D format f32
+// (bits 4-5 = 1), A and B format (7-9, 10-12: 0 = fp16, 1 = bf16; one
+// format for both operands), A/B major-ness (bit 15 / 16: 0 = K-major,
+// 1 = MN-major), N >> 3 (17-22), M >> 4 (24-28).
+__host__ __device__ constexpr uint32_t idesc_f16kind_f32(int M, int N, bool a_mn_major,
+                                                         bool b_mn_major, uint32_t ab_format) {
+  return (1u << 4) | (ab_format << 7) | (ab_format << 10) | ((a_mn_major ? 1u : 0u) << 15) |
          ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
+}
+// bf16 A and B
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major,
+                                                      bool b_mn_major) {
+  return idesc_f16kind_f32(M, N, a_mn_major, b_mn_major, 1u);
+}
+// fp16 A and B
+__host__ __device__ constexpr uint32_t idesc_fp16_f32(int M, int N, bool a_mn_major,
+                                                      bool b_mn_major) {
+  return idesc_f16kind_f32(M, N, a_mn_major, b_mn_major, 0u);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]; issued by one thread.
@@ -373,6 +383,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+
+// Packs two floats to fp16x2 (round to nearest even; beyond 65504 -> inf): lo
+// in bits 0-15.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// 2^e as a float, exactly, for integer e in [-126, 127].
+__device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }
 
 // Packed fp32 pair arithmetic (one instruction for two lanes of a 64-bit register).
 __device__ __forceinline__ uint64_t f32x2(float lo, float hi) {

@@ -113,9 +113,11 @@ GQA_API int gqa_attn_fwd_ws(const void *q, const void *k, const void *v, void *o
 
 /*
  * Bytes of scratch that gqa_attn_bwd needs for these sizes: an fp32 dq
- * accumulator [B][H][S][d], then two fp32 row arrays [B][H][S_pad] with
- * S_pad = S rounded up to a multiple of 128: lse * log2(e) and the row term
- * D = rowsum(dout * o).  Returns 0 for invalid sizes.
+ * accumulator [B][H][S][d]; two fp32 row arrays [B][H][S_pad] with
+ * S_pad = S rounded up to a multiple of 128 (lse * log2(e) and the row term
+ * D = rowsum(dout * o), both carrying the row's power-of-two scale below); an
+ * fp16 copy of dout [B][H][S][d], each row scaled by a power of two; one int32
+ * per kv head (B * G, rounded up to 16 bytes).  Returns 0 for invalid sizes.
  */
 GQA_API size_t gqa_attn_bwd_workspace_size(int B, int H, int G, int S, int d);
 
@@ -127,6 +129,13 @@ GQA_API size_t gqa_attn_bwd_workspace_size(int B, int H, int G, int S, int d);
  * P recomputed from the saved row statistics, dP = dO.V^T, dS = P * (dP - D),
  * D = rowsum(dO * O), dQ reduced across query tiles), and the softmax backward
  * of "nx_f32_gqa_gate.nx source", test T4.
+ * Operand precision of the tensor-core products: S = q.k^T, dK and dQ take
+ * bf16 operands (q, k and dS = P * (dP - D) rounded once); dP = dout.v^T and
+ * dV = P^T.dout take fp16 operands: each dout row and each v row is scaled by
+ * the power of two that brings its largest element into [2^14, 2^15) (exact for
+ * every bf16 value within 2^29 of that element) and P by the matching power of
+ * two, so P reaches the dV product with 11 significant bits instead of 8.
+ * D is taken on the o passed in, as stated above.
  * workspace: device memory of at least gqa_attn_bwd_workspace_size() bytes,
  * 16-byte aligned, owned by the caller and not used by any other call running at
  * the same time.  When workspace is NULL the call takes it with cudaMallocAsync
@@ -153,7 +162,7 @@ GQA_API int gqa_attn_bwd(const void *q, const void *k, const void *v, const void
  * no counterpart of this call.
  *   - A problem whose scratch (gqa_attn_bwd_workspace_size) exceeds
  *     GQA_NOALLOC_SCRATCH_BYTES is rejected with GQA_ERR_TOO_LARGE before
- *     anything is launched (64 MiB holds about 250,000 query rows, B*H*S).
+ *     anything is launched (64 MiB holds about 170,000 query rows, B*H*S).
  *   - The first call on a device looks up the device address of the array with
  *     that device current; make that first call before any stream capture.
  *   - All calls on a device share the one array, which keeps whatever the last

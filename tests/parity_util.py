@@ -4,14 +4,11 @@ the float64 oracle.
 Tolerances (stated for the path: bf16 in, fp32 accumulate):
   O, dQ, dK, dV : max |gpu - oracle| <= 2e-2 and mean |gpu - oracle| <= 2e-3
   LSE           : max |gpu - oracle| <= 1e-3
-Reading for bf16 outputs: the 2e-2 bound applies to the value the kernel
-accumulates in fp32; storing that value as bf16 moves it by at most half a bf16
-ulp of its magnitude (0.0156 at |x| in [4, 8), 0.031 in [8, 16)), so an element
-is accepted when |gpu - oracle| <= 2e-2 + ulp_bf16(|oracle|) / 2.  The mean
-bound is unchanged.  (A float64 emulation of the kernel's own roundings -- bf16
-P and dS operands, bf16 outputs -- reproduces the largest backward errors of
-the 4x32x8x4096 workload to the last digit, e.g. 0.0212 on a dV element of
-magnitude 4.10, so these are the method's bf16 roundings, not kernel defects.)
+Reading for bf16 outputs with |oracle| >= 8: there half a bf16 ulp (0.031 and
+up) alone exceeds 2e-2, so such an element is accepted within
+max(2e-2, ulp_bf16(|oracle|) / 2 + 1e-3); every element with |oracle| < 8 is
+held to the plain 2e-2.  The gradients before the bf16 rounding are held to
+the plain 2e-2 everywhere (tests/test_grad_precision.py, fp32-output build).
 """
 from __future__ import annotations
 
@@ -40,13 +37,17 @@ def check_close(name: str, got, ref, *, max_abs=MAX_ABS, mean_abs=MEAN_ABS, bf16
     assert np.isfinite(got).all(), f"{name}: non-finite values"
     err = np.abs(got - ref)
     bound = np.full(ref.shape, float(max_abs))
+    big = np.zeros(ref.shape, dtype=bool)
     if bf16_out:
-        bound = bound + _bf16_half_ulp(ref)
-    over_plain = int((err > max_abs).sum())  # elements that needed the bf16-store allowance
+        big = np.abs(ref) >= 8.0
+        bound[big] = np.maximum(max_abs, _bf16_half_ulp(ref[big]) + 1e-3)
+    over_small = int((err[~big] > max_abs).sum())
+    over_big = int((err[big] > max_abs).sum())
     worst = np.unravel_index(np.argmax(err - bound), err.shape) if err.size else None
     msg = (f"{name}: max_err={err.max() if err.size else 0:.3e} mean_err="
            f"{err.mean() if err.size else 0:.3e} max|ref|={np.abs(ref).max() if ref.size else 0:.3f}"
-           f" n_over_{max_abs:g}={over_plain} worst_at={worst}")
+           f" n_over_{max_abs:g}: |ref|<8 {over_small}, |ref|>=8 {over_big} worst_at={worst}")
+    assert over_small == 0, msg
     assert (err <= bound).all(), msg
     if mean_abs is not None and err.size:
         assert err.mean() <= mean_abs, msg

@@ -47,9 +47,12 @@ def test_strerror(lib):
 
 def test_workspace_size(lib):
     B, H, G, S = 4, 32, 8, 4096
-    assert gq.gqa_attn_bwd_workspace_size(B, H, G, S, 64) == B * H * S * 64 * 4 + 2 * B * H * S * 4
+    # fp32 dQ accumulator, two fp32 row arrays, an fp16 copy of dout, one int per kv group
+    assert gq.gqa_attn_bwd_workspace_size(B, H, G, S, 64) == (
+        B * H * S * 64 * 4 + 2 * B * H * S * 4 + B * H * S * 64 * 2 + -(-B * G * 4 // 16) * 16)
     # row arrays are padded to a multiple of 128 rows
-    assert gq.gqa_attn_bwd_workspace_size(1, 2, 1, 130, 64) == 2 * 130 * 64 * 4 + 2 * 2 * 256 * 4
+    assert gq.gqa_attn_bwd_workspace_size(1, 2, 1, 130, 64) == (
+        2 * 130 * 64 * 4 + 2 * 2 * 256 * 4 + 2 * 130 * 64 * 2 + 16)
     assert gq.gqa_attn_bwd_workspace_size(B, H, G, S, 128) == 0
     assert gq.gqa_attn_bwd_workspace_size(1, 3, 2, 10, 64) == 0
     assert gq.gqa_attn_bwd_workspace_size(0, 4, 2, 10, 64) == 0

@@ -27,7 +27,7 @@ from bwd_rounding_model import model_bwd_group
 from parity_util import MAX_ABS, MEAN_ABS, check_close
 
 # The 16-bit format of the P operand of dV += P^T dO in the CUDA backward.
-KERNEL_P_OPERAND = "bf16"
+KERNEL_P_OPERAND = "f16_rowscaled"
 
 
 def _group(q, k, v, do, b, g):
@@ -120,6 +120,7 @@ def _fp32_grads(lib, q, k, v, do, *, causal=True, window=0, n_sink=0, scale=0.12
                             S, d, int(causal), window, n_sink, scale, p(ws), ws.numel(), st) == 0
     assert lib.gqa_attn_last_device_status(st) == 0
     f = lambda t: t.to("cpu", torch.float64).numpy()
+    _fp32_grads.last_o = f(o)
     return f(dq), f(dk), f(dv)
 
 
@@ -180,14 +181,17 @@ def test_fp32_gradients_long_window_group(fp32lib):
 
 @pytest.mark.gpu
 def test_fp32_gradients_large_logits(fp32lib):
-    """Scale 0.37: the kernel's fp32 gradients equal the rounding model's
-    (within the fp32 noise of the scores and sums), and the model's distance
-    from the oracle is the method's own (see test_model_large_logits_floor)."""
+    """Scale 0.37: the kernel's fp32 gradients equal the rounding model's, fed
+    the O the forward actually handed over (within the fp32 noise of the scores
+    and sums), and the model's distance from the oracle is the method's own
+    (see test_model_large_logits_floor)."""
     q, k, v, do = make_inputs(1, 4, 2, 300, seed=0, with_grad=True)
     dq, dk, dv = _fp32_grads(fp32lib, q, k, v, do, scale=0.37)
+    o = _fp32_grads.last_o
     for g in range(2):
         grp = _group(q, k, v, do, 0, g)
-        mq, mk, mv = model_bwd_group(*grp, 0.37, p_round=KERNEL_P_OPERAND)
+        mq, mk, mv = model_bwd_group(*grp, 0.37, p_round=KERNEL_P_OPERAND,
+                                     o=o[0, 2 * g:2 * g + 2])
         got = (dq[0, 2 * g:2 * g + 2], dk[0, g], dv[0, g])
         for name, a, b in zip(("dQ", "dK", "dV"), got, (mq, mk, mv)):
             mx, mean = _err(a, b)
