@@ -9,7 +9,8 @@ module only compiles it with gcc on first use and marshals numpy arrays.
 What it computes is stated in the C file's header: the definition printed in
 "nx_f32_gqa_gate.nx source" (scores, causal mask, softmax, attn.V, the GQA
 head map of test T2, the softmax backward of test T4) plus the window/sink
-mask and the backward named in "SnapKitty Transformer 8B".
+mask and the backward named in "SnapKitty Transformer 8B", and the YaRN
+rotary embedding that page names, written from the YaRN paper (section 3).
 """
 from __future__ import annotations
 
@@ -62,6 +63,12 @@ def _declare(lib):
     lib.oracle_attn_bwd_group_rows.restype = None
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = i
+    lib.oracle_yarn_freqs.argtypes = [i, d, d, d, d, d, dp]
+    lib.oracle_yarn_freqs.restype = None
+    lib.oracle_yarn_mscale.argtypes = [d]
+    lib.oracle_yarn_mscale.restype = d
+    lib.oracle_rope_rotate.argtypes = [dp, dp, lp, ctypes.c_long, i, dp]
+    lib.oracle_rope_rotate.restype = None
     return lib
 
 
@@ -175,3 +182,49 @@ def num_threads(lib=None) -> int:
 def visible(i: int, j: int, *, causal=True, window=0, n_sink=0, lib=None) -> bool:
     lib = lib or load()
     return bool(lib.oracle_visible(int(i), int(j), int(causal), int(window), int(n_sink)))
+
+
+# ------------------------------------------------------------------ YaRN RoPE
+
+def yarn_freqs(d=64, base=10000.0, factor=32.0, orig_ctx=6400, alpha=1.0, beta=32.0, lib=None):
+    """Per-pair rotation frequencies h_i (YaRN, NTK-by-parts) -> [d/2] float64."""
+    lib = lib or load()
+    f = np.zeros(d // 2)
+    lib.oracle_yarn_freqs(int(d), float(base), float(factor), float(orig_ctx), float(alpha),
+                          float(beta), _ptr(f))
+    return f
+
+
+def yarn_mscale(factor, lib=None) -> float:
+    """sqrt(1/t) of YaRN's attention temperature: 0.1 ln(s) + 1."""
+    return float((lib or load()).oracle_yarn_mscale(float(factor)))
+
+
+def rope_rotate(x, freqs, positions=None, lib=None):
+    """Rotates x [..., S, d] (positions 0..S-1 along the second-last axis unless
+    given) by the per-pair frequencies; returns float64 of the same shape."""
+    lib = lib or load()
+    x = _f64(x)
+    S, d = x.shape[-2], x.shape[-1]
+    rows = x.reshape(-1, d)
+    pos = np.ascontiguousarray(np.tile(np.arange(S) if positions is None
+                                       else np.asarray(positions), rows.shape[0] // S)
+                               .astype(np.int64))
+    out = np.zeros_like(rows)
+    f = _f64(freqs)
+    lib.oracle_rope_rotate(_ptr(rows), _ptr(out), pos.ctypes.data_as(ctypes.POINTER(ctypes.c_long)),
+                           rows.shape[0], d, _ptr(f))
+    return out.reshape(x.shape)
+
+
+def attn_fwd_yarn(q, k, v, *, base=10000.0, factor=32.0, orig_ctx=6400, alpha=1.0, beta=32.0,
+                  causal=True, window=0, n_sink=0, scale=None, lib=None):
+    """Forward with YaRN rotary embeddings on q and k (positions 0..S-1) and the
+    attention temperature: attn_fwd(rot(q), rot(k), v, scale * (0.1 ln s + 1)^2)."""
+    lib = lib or load()
+    d = q.shape[-1]
+    f = yarn_freqs(d, base, factor, orig_ctx, alpha, beta, lib=lib)
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    ms = yarn_mscale(factor, lib=lib)
+    return attn_fwd(rope_rotate(q, f, lib=lib), rope_rotate(k, f, lib=lib), v, causal=causal,
+                    window=window, n_sink=n_sink, scale=scale * ms * ms, lib=lib)

@@ -284,3 +284,61 @@ void oracle_attn_bwd(const double *q, const double *k, const double *v, const do
                                   dv + (((long)b * G + g) * (long)S) * d,
                                   B, H, G, S, d, causal, window, n_sink, scale, b, g);
 }
+
+/* ------------------------------------------------------------------ YaRN RoPE
+ *
+ * "SnapKitty Transformer 8B" (model specification table and section
+ * "Protected Inventions") applies YaRN-scaled rotary position embeddings with
+ * a 32x factor for 204800-token sequences to the queries and keys.  The pages
+ * give no formula; the definition written out here is the published one:
+ * "YaRN: Efficient Context Window Extension of Large Language Models" (Peng,
+ * Quesnelle, Fan, Shippole, 2023), section 3 ("NTK-by-parts" interpolation and
+ * the attention temperature), on rotary embeddings as defined by RoFormer
+ * (Su et al.): dimension pair i = (2i, 2i+1) of a row at position m is turned
+ * by the angle m * h_i.
+ *
+ *   theta_i   = base^(-2i/d)                 wavelength lambda_i = 2 pi / theta_i
+ *   r_i       = L / lambda_i                 (L: the original context length)
+ *   gamma(r)  = 0 if r < alpha, 1 if r > beta, (r - alpha) / (beta - alpha) else
+ *   h_i       = (1 - gamma(r_i)) theta_i / s + gamma(r_i) theta_i     (s: factor)
+ *   sqrt(1/t) = 0.1 ln(s) + 1                (attention temperature; the logits
+ *                                             are multiplied by 1/t)
+ */
+void oracle_yarn_freqs(int d, double base, double factor, double orig_ctx, double alpha,
+                       double beta, double *freq)
+{
+    for (int i = 0; i < d / 2; ++i) {
+        double theta = pow(base, -2.0 * i / d);
+        double wavelength = 2.0 * acos(-1.0) / theta;   /* 2 pi / theta */
+        double r = orig_ctx / wavelength;
+        double gamma;
+        if (r < alpha)
+            gamma = 0.0;
+        else if (r > beta)
+            gamma = 1.0;
+        else
+            gamma = (r - alpha) / (beta - alpha);
+        freq[i] = (1.0 - gamma) * theta / factor + gamma * theta;
+    }
+}
+
+/* sqrt(1/t) of the attention temperature for scale factor s. */
+double oracle_yarn_mscale(double factor)
+{
+    return 0.1 * log(factor) + 1.0;
+}
+
+/* Rotates n rows of x ([n][d]) to out: row r sits at position pos[r]. */
+void oracle_rope_rotate(const double *x, double *out, const long *pos, long n, int d,
+                        const double *freq)
+{
+    for (long r = 0; r < n; ++r) {
+        for (int i = 0; i < d / 2; ++i) {
+            double a = (double)pos[r] * freq[i];
+            double c = cos(a), s = sin(a);
+            double x0 = x[r * d + 2 * i], x1 = x[r * d + 2 * i + 1];
+            out[r * d + 2 * i] = x0 * c - x1 * s;
+            out[r * d + 2 * i + 1] = x0 * s + x1 * c;
+        }
+    }
+}
