@@ -11,6 +11,10 @@ Low-level calls (same names and argument order as the C header):
     gqa_attn_fwd_ws(q, k, v, o, lse, B, H, G, S, d, causal, window, n_sink, scale,
                     workspace, workspace_bytes, stream)   (score-bound forward)
     gqa_attn_fwd_workspace_size(B, H, G, S, d)
+    gqa_attn_fwd_yarn(q, k, v, o, lse, B, H, G, S, d, causal, window, n_sink, scale, rope_base,
+                      rope_factor, rope_orig_ctx, rope_alpha, rope_beta, workspace,
+                      workspace_bytes, stream)   (YaRN rotary embeddings on q and k)
+    gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d)
     gqa_attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, G, S, d, causal, window,
                  n_sink, scale, workspace, workspace_bytes, stream)
     gqa_attn_bwd_workspace_size(B, H, G, S, d)
@@ -20,13 +24,14 @@ Low-level calls (same names and argument order as the C header):
     gqa_attn_timing_enable(on), gqa_attn_timing_collect(buf)  (per-kernel CUDA-event times)
 Tensor helpers: ``fwd(q, k, v, ...)`` (picks the score-bound entry point for
 problems of at least SCORE_BOUND_MIN_FLOPS causal FLOPs, the plain one below)
-and ``bwd(q, k, v, o, dout, lse, ...)``.
+``fwd_yarn(q, k, v, ...)`` and ``bwd(q, k, v, o, dout, lse, ...)``.
 """
 from __future__ import annotations
 
 from ._lib import (GQA_ERR_ALIGN, GQA_ERR_CUDA, GQA_ERR_DEVICE_TIMEOUT, GQA_ERR_HEADDIM,
                    GQA_ERR_DEVICE_BOUNDS, GQA_ERR_MASK, GQA_ERR_NULL, GQA_ERR_SCALE,
-                   GQA_ERR_SHAPE, GQA_ERR_TOO_LARGE,
+                   GQA_ERR_SHAPE, GQA_ERR_TOO_LARGE, GQA_ERR_ROPE, YARN_DEFAULTS,
+                   fwd_yarn, gqa_attn_fwd_yarn, gqa_attn_fwd_yarn_workspace_size,
                    GQA_ERR_WORKSPACE, GQA_NOALLOC_SCRATCH_BYTES, GQA_OK, SCORE_BOUND_MIN_FLOPS,
                    GqaError, bwd, fwd, visible_pairs,
                    gqa_attn_bwd, gqa_attn_bwd_noalloc,
@@ -36,7 +41,8 @@ from ._lib import (GQA_ERR_ALIGN, GQA_ERR_CUDA, GQA_ERR_DEVICE_TIMEOUT, GQA_ERR_
                    lib_path, load_library, selftest_timeout, timing_buffer)
 
 __all__ = [
-    "fwd", "bwd", "visible_pairs", "SCORE_BOUND_MIN_FLOPS", "gqa_attn_fwd", "gqa_attn_fwd_ws", "gqa_attn_fwd_workspace_size",
+    "fwd", "bwd", "fwd_yarn", "gqa_attn_fwd_yarn", "gqa_attn_fwd_yarn_workspace_size",
+    "GQA_ERR_ROPE", "YARN_DEFAULTS", "visible_pairs", "SCORE_BOUND_MIN_FLOPS", "gqa_attn_fwd", "gqa_attn_fwd_ws", "gqa_attn_fwd_workspace_size",
     "gqa_attn_bwd", "gqa_attn_bwd_noalloc",
     "gqa_attn_bwd_workspace_size", "GQA_ERR_TOO_LARGE", "GQA_ERR_DEVICE_BOUNDS", "GQA_NOALLOC_SCRATCH_BYTES",
     "gqa_attn_strerror", "gqa_attn_last_error_detail", "gqa_attn_last_device_status",

@@ -22,6 +22,7 @@ GQA_ERR_CUDA = -8
 GQA_ERR_DEVICE_TIMEOUT = -9
 GQA_ERR_TOO_LARGE = -10
 GQA_ERR_DEVICE_BOUNDS = -11
+GQA_ERR_ROPE = -12
 GQA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -58,6 +59,11 @@ def load_library():
         lib.gqa_attn_fwd_ws.restype = i
         lib.gqa_attn_fwd_workspace_size.argtypes = [i, i, i, i, i]
         lib.gqa_attn_fwd_workspace_size.restype = sz
+        lib.gqa_attn_fwd_yarn.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f,
+                                          f, f, i, f, f, vp, sz, vp]
+        lib.gqa_attn_fwd_yarn.restype = i
+        lib.gqa_attn_fwd_yarn_workspace_size.argtypes = [i, i, i, i, i]
+        lib.gqa_attn_fwd_yarn_workspace_size.restype = sz
         lib.gqa_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                      i, i, i, i, i, i, i, i, f, vp, sz, vp]
         lib.gqa_attn_bwd.restype = i
@@ -119,6 +125,21 @@ def gqa_attn_fwd_ws(q, k, v, o, lse, B, H, G, S, d, causal, window, n_sink, scal
 
 def gqa_attn_fwd_workspace_size(B, H, G, S, d):
     return load_library().gqa_attn_fwd_workspace_size(B, H, G, S, d)
+
+
+def gqa_attn_fwd_yarn(q, k, v, o, lse, B, H, G, S, d, causal, window, n_sink, scale, rope_base,
+                      rope_factor, rope_orig_ctx, rope_alpha, rope_beta, workspace,
+                      workspace_bytes, stream=None):
+    return load_library().gqa_attn_fwd_yarn(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, G, S, d,
+                                            int(causal), int(window), int(n_sink), float(scale),
+                                            float(rope_base), float(rope_factor),
+                                            int(rope_orig_ctx), float(rope_alpha),
+                                            float(rope_beta), _p(workspace), int(workspace_bytes),
+                                            _stream(stream))
+
+
+def gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d):
+    return load_library().gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d)
 
 
 def gqa_attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, G, S, d, causal, window, n_sink,
@@ -249,6 +270,38 @@ def fwd(q, k, v, *, causal=True, window=0, n_sink=0, scale=None, out=None, lse=N
                          workspace.numel() * workspace.element_size(), stream)
     if rc != GQA_OK:
         raise GqaError(rc, "gqa_attn_fwd_ws")
+    return o, l
+
+
+# YaRN parameters of the model-spec workload: factor 32 over an original
+# context of 204800 / 32 tokens, RoFormer's base 10^4 and the paper's ramp
+# bounds alpha = 1, beta = 32 (the pages give only the factor and the length).
+YARN_DEFAULTS = dict(rope_base=10000.0, rope_factor=32.0, rope_orig_ctx=6400, rope_alpha=1.0,
+                     rope_beta=32.0)
+
+
+def fwd_yarn(q, k, v, *, causal=True, window=0, n_sink=0, scale=None, rope_base=10000.0,
+             rope_factor=32.0, rope_orig_ctx=6400, rope_alpha=1.0, rope_beta=32.0,
+             out=None, lse=None, workspace=None, stream=None):
+    """o, lse = fwd_yarn(q, k, v) with YaRN rotary embeddings on q and k
+    (gqa_attn_fwd_yarn; `workspace` is allocated when not given)."""
+    import torch
+    B, H, S, d = q.shape
+    G = k.shape[1]
+    _check(q, (B, H, S, d), torch.bfloat16, "q")
+    _check(k, (B, G, S, d), torch.bfloat16, "k")
+    _check(v, (B, G, S, d), torch.bfloat16, "v")
+    scale = 1.0 / d ** 0.5 if scale is None else scale
+    o = torch.empty_like(q) if out is None else out
+    l = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if lse is None else lse
+    need = gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    rc = gqa_attn_fwd_yarn(q, k, v, o, l, B, H, G, S, d, causal, window, n_sink, scale, rope_base,
+                           rope_factor, rope_orig_ctx, rope_alpha, rope_beta, workspace,
+                           workspace.numel() * workspace.element_size(), stream)
+    if rc != GQA_OK:
+        raise GqaError(rc, "gqa_attn_fwd_yarn")
     return o, l
 
 

@@ -48,6 +48,7 @@
 #include <type_traits>
 
 #include "device_checks.cuh"
+#include "rope_kernels.cuh"
 #include "sm100_ptx.cuh"
 #include "trace.cuh"
 
@@ -111,6 +112,8 @@ struct Bars {
   uint64_t pv_done[2]; // every P.V product of head t finished (abort drain)
   uint64_t turn[2];    // ping-pong of the exp2 sections: turn[t] opens head t's
                        // section (arrived by the other head's 128 threads)
+  uint64_t q_ready[2]; // rotary embedding only: head t's Q tile rotated in place
+                       // (128 softmax threads of head t, once per unit)
   uint32_t tmem_base;
   AbortState abort;
 };
@@ -125,6 +128,7 @@ struct Params {
   int n_pairs;  // ceil(R / 2) head pairs per kv head
   int n_units;  // n_qblocks * B * G * n_pairs
   const float *kn2;  // [B*G][kKnParts] partial maxima of |k_j|^2, or null (no score bound)
+  const float2 *rope_tab;  // rotary embedding: [S][32] (cos, sin) per position and pair
   __nv_bfloat16 *o;
   float *lse;
   int *status;
@@ -247,6 +251,9 @@ __device__ __forceinline__ int unit_at(int k, const Params &p) {
   return base + c < p.n_units ? base + c : -1;
 }
 
+// kRope: the query tiles are turned by the rotary embedding (rope_kernels.cuh)
+// in shared memory before their first Q K^T; the keys arrive already rotated.
+template <bool kRope>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gqa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
@@ -275,6 +282,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&bars->o_empty[t], 128);
       mbar_init(&bars->turn[t], 128);
       mbar_init(&bars->pv_done[t], 1);
+      mbar_init(&bars->q_ready[t], 128);
     }
     mbar_init(&bars->qk_done, 1);
     bars->abort.flag = 0;
@@ -355,6 +363,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t k_addr0 = smem_u32(smem + SM_K);
     int gt = 0;             // K/V tiles consumed (all units)
     int ts[2] = {0, 0};     // S products issued per head (all units)
+    int qr[2] = {0, 0};     // rotated Q tiles consumed per head (rotary embedding)
     bool ok = true;
     for (int k = 0; ok; ++k) {
       const int u = unit_at(k, p);
@@ -370,6 +379,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (ts[t] > 0 && !mbar_wait(&bars->s_free[t], (ts[t] - 1) & 1, ab, p.status, kTimeoutCode)) {
             ok = false;
             break;
+          }
+          if constexpr (kRope) {
+            // the unit's first product of head t needs its Q tile rotated
+            if (it == 0) {
+              if (!mbar_wait(&bars->q_ready[t], qr[t] & 1, ab, p.status, kTimeoutCode)) {
+                ok = false;
+                break;
+              }
+              ++qr[t];
+            }
           }
           tc_fence_after_sync();
           const uint64_t ad = sdesc_sw128(q_addr0 + t * TILE_BYTES, 16, 1024);
@@ -479,6 +498,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int lo = win ? i - p.window : -1;
       const int ns = win ? p.n_sink : 0;
 
+      if constexpr (kRope) {
+        // turn this row of head t's Q tile (position i) before any Q K^T reads it
+        if (!mbar_wait(&bars->q_full, k & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        if (i < p.S)
+          rope::rope_rotate_smem_row(smem + SM_Q + t * TILE_BYTES + r * 128, r,
+                                     p.rope_tab + static_cast<size_t>(i) * rope::kPairs);
+        fence_proxy_async_smem();
+        mbar_arrive(&bars->q_ready[t]);
+      }
       float m_run = -CUDART_INF_F;  // running max of scaled scores, base-2 units
       float l_run = 0.f;            // running sum of 2^(s - m_run)
       // Score bound (kBoundMax): decided per warp before the unit's first tile.

@@ -66,20 +66,20 @@ int device_state(DeviceState **out) {
             cudaGetSymbolAddress(reinterpret_cast<void **>(&st.status), g_device_status),
             "cudaGetSymbolAddress(device status word)"))
       return GQA_ERR_CUDA;
-    if (gqa::cuda_failed(cudaFuncSetAttribute(gqa::fwd::gqa_fwd_kernel,
-                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              gqa::fwd::SMEM_BYTES),
-                         "cudaFuncSetAttribute(forward shared memory)"))
-      return GQA_ERR_CUDA;
-    // The forward rebalances registers between warpgroups (setmaxnreg); that is
-    // only safe when the compiled launch allocation covers the split.
-    cudaFuncAttributes fa{};
-    if (gqa::cuda_failed(cudaFuncGetAttributes(&fa, gqa::fwd::gqa_fwd_kernel),
-                         "cudaFuncGetAttributes(forward)"))
-      return GQA_ERR_CUDA;
-    if (fa.numRegs < gqa::fwd::kMinLaunchRegs) {
-      gqa::set_error_detail("forward kernel compiled with fewer registers than its warpgroup split needs");
-      return GQA_ERR_CUDA;
+    for (auto kern : {gqa::fwd::gqa_fwd_kernel<false>, gqa::fwd::gqa_fwd_kernel<true>}) {
+      if (gqa::cuda_failed(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                gqa::fwd::SMEM_BYTES),
+                           "cudaFuncSetAttribute(forward shared memory)"))
+        return GQA_ERR_CUDA;
+      // The forward rebalances registers between warpgroups (setmaxnreg); that
+      // is only safe when the compiled launch allocation covers the split.
+      cudaFuncAttributes fa{};
+      if (gqa::cuda_failed(cudaFuncGetAttributes(&fa, kern), "cudaFuncGetAttributes(forward)"))
+        return GQA_ERR_CUDA;
+      if (fa.numRegs < gqa::fwd::kMinLaunchRegs) {
+        gqa::set_error_detail("forward kernel compiled with fewer registers than its warpgroup split needs");
+        return GQA_ERR_CUDA;
+      }
     }
     int rc = gqa::bwd::configure_kernels();
     if (rc != 0) return GQA_ERR_CUDA;  // detail recorded by configure_kernels
@@ -154,17 +154,19 @@ const char *gqa_attn_strerror(int status) {
     case GQA_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait";
     case GQA_ERR_TOO_LARGE: return "problem needs more scratch than gqa_attn_bwd_noalloc holds";
     case GQA_ERR_DEVICE_BOUNDS: return "a kernel's run-time index check failed (debug build)";
+    case GQA_ERR_ROPE: return "invalid rotary embedding parameters (base > 1, factor >= 1, original context > 0, 0 <= alpha < beta)";
     default: return "unknown status";
   }
 }
 
 namespace {
 
-// The forward launch shared by both entry points; kn2 (the score-bound record
-// that fwd_knorm_kernel writes first, on the same stream) may be null.
+// The forward launch shared by the entry points; kn2 (the score-bound record
+// that fwd_knorm_kernel writes first, on the same stream) may be null, and so
+// may rope_tab (the rotary table; k is then already rotated).
 int launch_forward(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
                    int G, int S, int causal, int window, int n_sink, float scale, float *kn2,
-                   cudaStream_t st) {
+                   const float2 *rope_tab, cudaStream_t st) {
   DeviceState *ds = nullptr;
   int rc = device_state(&ds);
   if (rc != GQA_OK) return rc;
@@ -189,6 +191,7 @@ int launch_forward(const void *q, const void *k, const void *v, void *o, float *
   p.n_qblocks = (S + BM - 1) / BM;
   p.n_pairs = (p.R + 1) / 2;
   p.kn2 = kn2;
+  p.rope_tab = rope_tab;
   p.o = static_cast<__nv_bfloat16 *>(o);
   p.lse = lse;
   p.status = ds->status;
@@ -209,7 +212,10 @@ int launch_forward(const void *q, const void *k, const void *v, void *o, float *
       return GQA_ERR_CUDA;
   }
   gqa::timing_begin(GQA_KERNEL_FWD, st);
-  gqa_fwd_kernel<<<static_cast<unsigned>(grid), NTHREADS, SMEM_BYTES, st>>>(tq, tk, tv, p);
+  if (rope_tab)
+    gqa_fwd_kernel<true><<<static_cast<unsigned>(grid), NTHREADS, SMEM_BYTES, st>>>(tq, tk, tv, p);
+  else
+    gqa_fwd_kernel<false><<<static_cast<unsigned>(grid), NTHREADS, SMEM_BYTES, st>>>(tq, tk, tv, p);
   gqa::timing_end(GQA_KERNEL_FWD, st);
   return gqa::cuda_failed(cudaGetLastError(), "launch of the forward kernel") ? GQA_ERR_CUDA
                                                                                : GQA_OK;
@@ -226,7 +232,7 @@ int gqa_attn_fwd(const void *q, const void *k, const void *v, void *o, float *ls
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return GQA_ERR_ALIGN;
   return launch_forward(q, k, v, o, lse, B, H, G, S, causal, window, n_sink, scale, nullptr,
-                        static_cast<cudaStream_t>(stream));
+                        nullptr, static_cast<cudaStream_t>(stream));
 }
 
 size_t gqa_attn_fwd_workspace_size(int B, int H, int G, int S, int d) {
@@ -245,7 +251,54 @@ int gqa_attn_fwd_ws(const void *q, const void *k, const void *v, void *o, float 
     return GQA_ERR_ALIGN;
   if (workspace_bytes < gqa_attn_fwd_workspace_size(B, H, G, S, d)) return GQA_ERR_WORKSPACE;
   return launch_forward(q, k, v, o, lse, B, H, G, S, causal, window, n_sink, scale,
-                        static_cast<float *>(workspace), static_cast<cudaStream_t>(stream));
+                        static_cast<float *>(workspace), nullptr, static_cast<cudaStream_t>(stream));
+}
+
+size_t gqa_attn_fwd_yarn_workspace_size(int B, int H, int G, int S, int d) {
+  if (check_common(B, H, G, S, d, 1, 0, 0, 1.f) != GQA_OK) return 0;
+  const size_t krot = static_cast<size_t>(B) * G * S * 64 * 2;  // a multiple of 16
+  return krot + static_cast<size_t>(S) * gqa::rope::kPairs * sizeof(float2);
+}
+
+int gqa_attn_fwd_yarn(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                      int H, int G, int S, int d, int causal, int window, int n_sink, float scale,
+                      float rope_base, float rope_factor, int rope_orig_ctx, float rope_alpha,
+                      float rope_beta, void *workspace, size_t workspace_bytes, void *stream) {
+  int rc = check_common(B, H, G, S, d, causal, window, n_sink, scale);
+  if (rc != GQA_OK) return rc;
+  gqa::rope::Freqs f;
+  if (!gqa::rope::yarn_freqs(rope_base, rope_factor, rope_orig_ctx, rope_alpha, rope_beta, &f))
+    return GQA_ERR_ROPE;
+  if (!q || !k || !v || !o || !lse || !workspace) return GQA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(workspace))
+    return GQA_ERR_ALIGN;
+  if (workspace_bytes < gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d)) return GQA_ERR_WORKSPACE;
+  const double tempered = static_cast<double>(scale) * gqa::rope::yarn_score_factor(rope_factor);
+  if (!(tempered < 3.0e38)) return GQA_ERR_SCALE;
+  DeviceState *ds = nullptr;
+  if ((rc = device_state(&ds)) != GQA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  __nv_bfloat16 *k_rot = static_cast<__nv_bfloat16 *>(workspace);
+  float2 *tab = reinterpret_cast<float2 *>(static_cast<char *>(workspace) +
+                                           static_cast<size_t>(B) * G * S * 64 * 2);
+  {
+    const long long n = static_cast<long long>(S) * gqa::rope::kPairs;
+    long long blocks = (n + 255) / 256;
+    blocks = blocks > 4LL * ds->sm_count ? 4LL * ds->sm_count : blocks;
+    gqa::rope::rope_table_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(f, S, tab);
+    if (gqa::cuda_failed(cudaGetLastError(), "launch of the rotary table kernel")) return GQA_ERR_CUDA;
+  }
+  {
+    const long long n = static_cast<long long>(B) * G * S * 8;
+    long long blocks = (n + 255) / 256;
+    blocks = blocks > 8LL * ds->sm_count ? 8LL * ds->sm_count : blocks;
+    gqa::rope::rope_rotate_k_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+        static_cast<const __nv_bfloat16 *>(k), k_rot, tab, n, S);
+    if (gqa::cuda_failed(cudaGetLastError(), "launch of the key rotation kernel")) return GQA_ERR_CUDA;
+  }
+  return launch_forward(q, k_rot, v, o, lse, B, H, G, S, causal, window, n_sink,
+                        static_cast<float>(tempered), nullptr, tab, st);
 }
 
 size_t gqa_attn_bwd_workspace_size(int B, int H, int G, int S, int d) {

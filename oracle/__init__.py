@@ -69,6 +69,8 @@ def _declare(lib):
     lib.oracle_yarn_mscale.restype = d
     lib.oracle_rope_rotate.argtypes = [dp, dp, lp, ctypes.c_long, i, dp]
     lib.oracle_rope_rotate.restype = None
+    lib.oracle_round_bf16.argtypes = [dp, ctypes.c_long]
+    lib.oracle_round_bf16.restype = None
     return lib
 
 
@@ -217,14 +219,36 @@ def rope_rotate(x, freqs, positions=None, lib=None):
     return out.reshape(x.shape)
 
 
+def round_bf16(x, lib=None):
+    """Nearest bf16 (ties to even) of each value, as float64."""
+    lib = lib or load()
+    y = _f64(x).copy()
+    lib.oracle_round_bf16(_ptr(y), y.size)
+    return y
+
+
+def yarn_rotated(q, k, *, base=10000.0, factor=32.0, orig_ctx=6400, alpha=1.0, beta=32.0,
+                 rounded=True, lib=None):
+    """rot(q), rot(k) at positions 0..S-1, rounded once to bf16 when `rounded`
+    (the tensors a bf16 model hands to attention after its rotary embedding)."""
+    lib = lib or load()
+    f = yarn_freqs(q.shape[-1], base, factor, orig_ctx, alpha, beta, lib=lib)
+    qr, kr = rope_rotate(q, f, lib=lib), rope_rotate(k, f, lib=lib)
+    if rounded:
+        qr, kr = round_bf16(qr, lib=lib), round_bf16(kr, lib=lib)
+    return qr, kr
+
+
 def attn_fwd_yarn(q, k, v, *, base=10000.0, factor=32.0, orig_ctx=6400, alpha=1.0, beta=32.0,
-                  causal=True, window=0, n_sink=0, scale=None, lib=None):
+                  causal=True, window=0, n_sink=0, scale=None, rounded=True, lib=None):
     """Forward with YaRN rotary embeddings on q and k (positions 0..S-1) and the
-    attention temperature: attn_fwd(rot(q), rot(k), v, scale * (0.1 ln s + 1)^2)."""
+    attention temperature: attn_fwd(rot(q), rot(k), v, scale * (0.1 ln s + 1)^2),
+    the rotated q and k rounded once to bf16 unless `rounded` is False."""
     lib = lib or load()
     d = q.shape[-1]
-    f = yarn_freqs(d, base, factor, orig_ctx, alpha, beta, lib=lib)
     scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
     ms = yarn_mscale(factor, lib=lib)
-    return attn_fwd(rope_rotate(q, f, lib=lib), rope_rotate(k, f, lib=lib), v, causal=causal,
-                    window=window, n_sink=n_sink, scale=scale * ms * ms, lib=lib)
+    qr, kr = yarn_rotated(q, k, base=base, factor=factor, orig_ctx=orig_ctx, alpha=alpha,
+                          beta=beta, rounded=rounded, lib=lib)
+    return attn_fwd(qr, kr, v, causal=causal, window=window, n_sink=n_sink, scale=scale * ms * ms,
+                    lib=lib)

@@ -342,3 +342,21 @@ void oracle_rope_rotate(const double *x, double *out, const long *pos, long n, i
         }
     }
 }
+
+/* Rounds each value to the nearest bf16 (ties to even) by way of fp32: the
+ * rotated queries and keys are bf16 tensors in a bf16 model, so the attention
+ * that follows the rotation sees them rounded once.  n values in place. */
+void oracle_round_bf16(double *x, long n)
+{
+    for (long e = 0; e < n; ++e) {
+        float f = (float)x[e];
+        unsigned int u;
+        memcpy(&u, &f, sizeof u);
+        if ((u & 0x7f800000u) != 0x7f800000u) {      /* finite: round the low 16 bits */
+            u += 0x7fffu + ((u >> 16) & 1u);
+        }
+        u &= 0xffff0000u;
+        memcpy(&f, &u, sizeof f);
+        x[e] = (double)f;
+    }
+}

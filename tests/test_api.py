@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_strerror(lib):
-    for code in range(0, -10, -1):
+    for code in range(0, -13, -1):
         s = gq.gqa_attn_strerror(code)
         assert isinstance(s, str) and s and s != "unknown status"
     assert gq.gqa_attn_strerror(12345) == "unknown status"
@@ -93,7 +93,18 @@ def _bwd(**kw):
                            a["window"], a["n_sink"], a["scale"], a["ws"], a["wsb"], a["stream"])
 
 
-@pytest.mark.parametrize("call", [_fwd, _fwd_ws, _bwd])
+def _fwd_yarn(**kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=4, G=2, S=128, d=64,
+             causal=1, window=0, n_sink=0, scale=0.125, base=10000.0, factor=32.0, L=6400,
+             alpha=1.0, beta=32.0, ws=FAKE, wsb=1 << 24, stream=0)
+    a.update(kw)
+    return gq.gqa_attn_fwd_yarn(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["G"],
+                                a["S"], a["d"], a["causal"], a["window"], a["n_sink"], a["scale"],
+                                a["base"], a["factor"], a["L"], a["alpha"], a["beta"], a["ws"],
+                                a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("call", [_fwd, _fwd_ws, _fwd_yarn, _bwd])
 def test_argument_errors(lib, call):
     assert call(B=0) == gq.GQA_ERR_SHAPE
     assert call(S=0) == gq.GQA_ERR_SHAPE
@@ -123,6 +134,22 @@ def test_fwd_ws_specific_errors(lib):
     assert _fwd_ws(ws=FAKE + 4) == gq.GQA_ERR_ALIGN
     assert _fwd_ws(wsb=1 * 2 * 16 - 1) == gq.GQA_ERR_WORKSPACE
     assert _fwd_ws(lse=None) == gq.GQA_ERR_NULL
+
+
+def test_fwd_yarn_specific_errors(lib):
+    assert _fwd_yarn(base=1.0) == gq.GQA_ERR_ROPE
+    assert _fwd_yarn(factor=0.5) == gq.GQA_ERR_ROPE
+    assert _fwd_yarn(L=0) == gq.GQA_ERR_ROPE
+    assert _fwd_yarn(alpha=32.0, beta=32.0) == gq.GQA_ERR_ROPE
+    assert _fwd_yarn(alpha=-1.0) == gq.GQA_ERR_ROPE
+    assert _fwd_yarn(base=float("nan")) == gq.GQA_ERR_ROPE
+    assert _fwd_yarn(ws=None) == gq.GQA_ERR_NULL
+    assert _fwd_yarn(ws=FAKE + 4) == gq.GQA_ERR_ALIGN
+    need = gq.gqa_attn_fwd_yarn_workspace_size(1, 4, 2, 128, 64)
+    # rotated keys (bf16) and the (cos, sin) table
+    assert need == 1 * 2 * 128 * 64 * 2 + 128 * 32 * 8
+    assert _fwd_yarn(wsb=need - 1) == gq.GQA_ERR_WORKSPACE
+    assert gq.gqa_attn_fwd_yarn_workspace_size(1, 3, 2, 128, 64) == 0
 
 
 def test_bwd_specific_errors(lib):

@@ -99,7 +99,7 @@ def test_yarn_attention_keeps_t1_and_row_sums():
     """Causal attention over rotated q, k still returns out[0] = V[0] (test T1),
     and its LSE is that of the tempered scores of the rotated inputs."""
     q, k, v = (t.double().numpy() for t in make_inputs(1, 2, 1, 40, seed=3))
-    o, lse = oracle.attn_fwd_yarn(q, k, v)
+    o, lse = oracle.attn_fwd_yarn(q, k, v, rounded=False)
     np.testing.assert_allclose(o[0, :, 0], np.repeat(v[0, :1, 0], 2, axis=0), atol=1e-12)
     f = oracle.yarn_freqs()
     t = oracle.yarn_mscale(32.0) ** 2 / 8.0
@@ -107,6 +107,20 @@ def test_yarn_attention_keeps_t1_and_row_sums():
     i = 17
     s = t * (qr[0, 1, i] @ kr[0, 0, :i + 1].T)
     assert abs(lse[0, 1, i] - (s.max() + math.log(np.exp(s - s.max()).sum()))) < 1e-12
+
+
+def test_round_bf16_ties_and_library_cast():
+    """Ties go to the even neighbour: 1 + 2^-8 -> 1, 1 + 3 * 2^-8 -> 1 + 2^-6,
+    -(1 + 2^-8) -> -1; exact bf16 values, zeros and infinities are unchanged; and
+    on random values the result equals torch's float32 -> bfloat16 cast."""
+    import torch
+    x = np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8), 1.5, 0.0, -0.0, np.inf, 2 ** -130])
+    y = oracle.round_bf16(x)
+    assert list(y[:6]) == [1.0, 1 + 2 ** -6, -1.0, 1.5, 0.0, 0.0]
+    assert y[6] == np.inf
+    r = np.random.default_rng(5).standard_normal(10000) * 37.0
+    ref = torch.from_numpy(r.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(oracle.round_bf16(r.astype(np.float32).astype(np.float64)), ref)
 
 
 YARN_MUTANTS = {
@@ -118,6 +132,8 @@ YARN_MUTANTS = {
     "wavelength_not_2pi": ("double wavelength = 2.0 * acos(-1.0) / theta;",
                            "double wavelength = 1.0 / theta;"),
     "temperature_log2": ("return 0.1 * log(factor) + 1.0;", "return 0.1 * log2(factor) + 1.0;"),
+    "round_half_up": ("u += 0x7fffu + ((u >> 16) & 1u);", "u += 0x8000u;"),
+    "round_truncates": ("u += 0x7fffu + ((u >> 16) & 1u);", "u += 0u;"),
 }
 
 
@@ -136,7 +152,8 @@ def test_planted_yarn_mistake_is_caught(name, tmp_path):
     try:
         for pin in (test_factor_one_is_plain_rope, test_ramp_closed_form_when_alpha_one_beta_s,
                     test_ramp_ends, test_temperature_of_the_paper, test_rotation_hand_values,
-                    test_rotation_preserves_pair_norms, test_scores_depend_on_distance_only):
+                    test_rotation_preserves_pair_norms, test_scores_depend_on_distance_only,
+                    test_round_bf16_ties_and_library_cast):
             try:
                 pin()
             except AssertionError:
