@@ -40,7 +40,7 @@ if ROOT not in sys.path:
 
 METRIC = "attention fwd/bwd TFLOPS (causal FLOPs) and % of B300 BF16 tensor peak"
 KERNEL_NAMES = ["gqa_fwd_kernel", "bwd_prep_kernel", "bwd_main_kernel", "bwd_dq_convert_kernel",
-                "fwd_knorm_kernel"]
+                "fwd_knorm_kernel", "rope_table_and_key_rotation"]
 N_KERNELS = len(KERNEL_NAMES)
 L2_FLUSH_BYTES = 1 << 30
 
@@ -180,7 +180,7 @@ class ClockSampler:
 class Problem:
     """Device tensors of one workload and the calls of one step (through the C ABI)."""
 
-    def __init__(self, w, dev, seed, with_bwd):
+    def __init__(self, w, dev, seed, with_bwd, yarn=False):
         import torch
         import causal_grouped_query_gqa_b300 as gq
         from causal_grouped_query_gqa_b300.inputs import make_inputs
@@ -199,6 +199,12 @@ class Problem:
         # the forward entry point the library's own fwd() picks for this size
         fwd_f, _ = step_flops(w, False)
         self.score_bound = fwd_f >= gq.SCORE_BOUND_MIN_FLOPS
+        # the YaRN forward (rotary embeddings on q and k) instead of the plain one
+        self.yarn = yarn
+        if yarn:
+            self.score_bound = False
+            self.yws_bytes = gq.gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d)
+            self.yws = torch.empty(max(self.yws_bytes, 16), dtype=torch.uint8, device=dev)
 
     def step_on(self, ins, outs, strm, score_bound=None):
         import causal_grouped_query_gqa_b300 as gq
@@ -207,7 +213,13 @@ class Problem:
         q_, k_, v_, do_ = ins
         o_, lse_, dq_, dk_, dv_ = outs
         bound = self.score_bound if score_bound is None else score_bound
-        if bound:
+        if self.yarn:
+            y = gq.YARN_DEFAULTS
+            rc = gq.gqa_attn_fwd_yarn(q_, k_, v_, o_, lse_, B, H, G, S, d, w.causal, w.window,
+                                      w.n_sink, w.scale, y["rope_base"], y["rope_factor"],
+                                      y["rope_orig_ctx"], y["rope_alpha"], y["rope_beta"],
+                                      self.yws, self.yws_bytes, strm)
+        elif bound:
             rc = gq.gqa_attn_fwd_ws(q_, k_, v_, o_, lse_, B, H, G, S, d, w.causal, w.window,
                                     w.n_sink, w.scale, self.fws, self.fws_bytes, strm)
         else:
@@ -224,7 +236,7 @@ class Problem:
 
     def launches_per_step(self, score_bound=None):
         bound = self.score_bound if score_bound is None else score_bound
-        return (2 if bound else 1) + (3 if self.with_bwd else 0)
+        return (3 if self.yarn else (2 if bound else 1)) + (4 if self.with_bwd else 0)
 
 
 def timed_steps(pb, steps, warmup, flush, stream, world, score_bound=None, clocks=False):
@@ -286,7 +298,7 @@ def tensor_roofline(kernel, flops, ms, peaks, workload):
 def summarize(w, pb, kernel_ms, total_ms, steps, world, peaks, workload):
     fwd_f, bwd_f = step_flops(w, pb.with_bwd)
     avg = {kid: kernels_ms_avg(kernel_ms, kid) for kid in range(N_KERNELS)}
-    fwd_ms = avg[0] + avg[4]
+    fwd_ms = avg[0] + avg[4] + avg[5]
     bwd_ms = avg[1] + avg[2] + avg[3]
     tot = [sum(x) for x in kernel_ms]
     dom = max(range(N_KERNELS), key=lambda kid: tot[kid])
@@ -392,14 +404,14 @@ def run_ours(args, w, rank, world, local_rank):
         extras = {}
         for name, step in EXTRA_WORKLOADS:
             ew = WORKLOADS[name]
-            epb = Problem(ew, dev, seed=0, with_bwd=(step == "fwd+bwd"))
+            epb = Problem(ew, dev, seed=0, with_bwd=(step == "fwd+bwd"), yarn=(step == "fwd_yarn"))
             e_steps = max(3, min(args.steps, 10))
             e_ms, e_kernel, e_clk = timed_steps(epb, e_steps, 3, flush, stream, 1, clocks=True)
             res = summarize(ew, epb, e_kernel, e_ms, e_steps, 1, peaks, name)
             res.update({"step": step, "steps": e_steps, "clocks": e_clk,
                         "config": {"B": ew.B, "H": ew.H, "G": ew.G, "S": ew.S,
                                    "window": ew.window, "n_sink": ew.n_sink}})
-            extras[name] = res
+            extras[name if step != "fwd_yarn" else name + "+yarn"] = res
             del epb
             torch.cuda.empty_cache()
         out["extra_workloads"] = extras
@@ -412,6 +424,7 @@ EXTRA_WORKLOADS = [
     ("gqa_b2_h32_g8_s2048", "fwd"),
     ("window_b1_h128_g16_s32768_w4096_sink128", "fwd"),
     ("bwd_b4_h32_g8_s4096", "fwd+bwd"),
+    ("wide_b1_h128_g16_s8192", "fwd_yarn"),   # YaRN rotary forward (table + key rotation + forward)
 ]
 
 

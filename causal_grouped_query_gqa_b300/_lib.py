@@ -189,7 +189,7 @@ def selftest_timeout(budget_ms: int = 20, stream=None):
     return rc, [int(x) for x in el], [int(x) for x in ok]
 
 
-GQA_KERNEL_COUNT = 5  # fwd, bwd prep, bwd main, bwd dq convert, fwd key norms
+GQA_KERNEL_COUNT = 6  # fwd, bwd prep, bwd main, bwd dq convert, fwd key norms, rotary pre-pass
 
 
 def gqa_attn_timing_enable(on: bool) -> int:

@@ -286,6 +286,7 @@ int gqa_attn_fwd_yarn(const void *q, const void *k, const void *v, void *o, floa
     const long long n = static_cast<long long>(S) * gqa::rope::kPairs;
     long long blocks = (n + 255) / 256;
     blocks = blocks > 4LL * ds->sm_count ? 4LL * ds->sm_count : blocks;
+    gqa::timing_begin(GQA_KERNEL_ROPE, st);
     gqa::rope::rope_table_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(f, S, tab);
     if (gqa::cuda_failed(cudaGetLastError(), "launch of the rotary table kernel")) return GQA_ERR_CUDA;
   }
@@ -295,6 +296,7 @@ int gqa_attn_fwd_yarn(const void *q, const void *k, const void *v, void *o, floa
     blocks = blocks > 8LL * ds->sm_count ? 8LL * ds->sm_count : blocks;
     gqa::rope::rope_rotate_k_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
         static_cast<const __nv_bfloat16 *>(k), k_rot, tab, n, S);
+    gqa::timing_end(GQA_KERNEL_ROPE, st);
     if (gqa::cuda_failed(cudaGetLastError(), "launch of the key rotation kernel")) return GQA_ERR_CUDA;
   }
   return launch_forward(q, k_rot, v, o, lse, B, H, G, S, causal, window, n_sink,

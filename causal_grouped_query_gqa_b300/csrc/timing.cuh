@@ -7,7 +7,8 @@
 
 namespace gqa {
 
-constexpr int kNumKernelIds = 5;  // fwd, bwd prep, bwd main, bwd dq convert, fwd key norms
+constexpr int kNumKernelIds = 6;  // fwd, bwd prep, bwd main, bwd dq convert, fwd key norms,
+                                   // rotary pre-pass
 
 struct TimingState {
   bool on = false;

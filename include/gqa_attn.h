@@ -263,11 +263,12 @@ GQA_API int gqa_attn_selftest_timeout(unsigned budget_ms, unsigned long long *el
  */
 typedef enum {
     GQA_KERNEL_FWD = 0,       /* forward (one launch per gqa_attn_fwd) */
-    GQA_KERNEL_BWD_PREP = 1,  /* backward: D = rowsum(dout * o), dq accumulator cleared */
+    GQA_KERNEL_BWD_PREP = 1,  /* backward: D, fp16 dout, dq accumulator cleared, LSE shift */
     GQA_KERNEL_BWD_MAIN = 2,  /* backward: dk, dv and the dq accumulation */
     GQA_KERNEL_BWD_DQ = 3,    /* backward: dq accumulator -> bf16 dq */
     GQA_KERNEL_FWD_KNORM = 4, /* gqa_attn_fwd_ws: key-norm maxima for the score bound */
-    GQA_KERNEL_COUNT = 5
+    GQA_KERNEL_ROPE = 5,      /* gqa_attn_fwd_yarn: rotary table and key rotation */
+    GQA_KERNEL_COUNT = 6
 } gqa_kernel_id;
 
 GQA_API int gqa_attn_timing_enable(int on);
