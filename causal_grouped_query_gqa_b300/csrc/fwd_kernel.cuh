@@ -96,8 +96,12 @@ constexpr int SM_V = SM_K + NSTAGE * TILE_BYTES;
 constexpr int SM_BARS = SM_V + NSTAGE * TILE_BYTES;
 
 struct Bars {
-  alignas(16) float kn[2][kKnParts];  // the unit's |k_j|^2 record (units alternate slots)
-  uint64_t q_full;     // the unit's Q tiles (and |k|^2 record) landed (TMA transaction bytes)
+  alignas(16) float kn[2][2][kKnParts];  // |k_j|^2 record per head and slot (a head's units
+                                         // alternate slots)
+  uint64_t q_full[2];  // head t's Q tile (and its |k|^2 record) landed (TMA transaction
+                       // bytes).  One barrier per head: head 1 sits out the single-head
+                       // units, and counting its own phases keeps it from mistaking an
+                       // older completed phase for the one it waits on
   uint64_t q_empty;    // every Q K^T of the unit finished: Q may be reloaded
   uint64_t kv_full[NSTAGE];   // K and V tile landed (TMA transaction bytes)
   uint64_t kv_empty[NSTAGE];  // every head's products with the tile finished (the
@@ -267,7 +271,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_full[0], 1);
+    mbar_init(&bars->q_full[1], 1);
     mbar_init(&bars->q_empty, 1);
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(&bars->kv_full[s], 1);
@@ -308,7 +313,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       int gt = 0;       // K/V tiles issued (all units): ring stage and phase
-      int q_loads = 0;  // units whose Q was issued
+      int q_loads[2] = {0, 0};  // Q tiles issued per head (all units)
       bool ok = true;
       for (int k = 0; ok; ++k) {
         const int u = unit_at(k, p);
@@ -320,14 +325,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int qrow = un.qb * BM, qz = un.b * p.H + un.h0;
         GQA_REPORT(p.status, un.qb >= 0 && un.qb < p.n_qblocks && kr.count >= 1 &&
                                 qz + (un.two ? 1 : 0) < p.B * p.H);
-        mbar_arrive_expect_tx(&bars->q_full,
-                              (un.two ? 2 : 1) * TILE_BYTES + (p.kn2 ? kKnParts * 4 : 0));
-        tma_load_3d(smem + SM_Q, &tm_q, &bars->q_full, 0, qrow, qz);
-        if (p.kn2)  // the kv head's |k|^2 record, for the softmax's score bound
-          bulk_load(&bars->kn[k & 1][0], p.kn2 + static_cast<size_t>(kvz_of(un, p)) * kKnParts,
-                    kKnParts * 4, &bars->q_full);
-        if (un.two) tma_load_3d(smem + SM_Q + TILE_BYTES, &tm_q, &bars->q_full, 0, qrow, qz + 1);
-        q_loads = k + 1;
+        for (int t = 0; t < (un.two ? 2 : 1); ++t) {
+          mbar_arrive_expect_tx(&bars->q_full[t], TILE_BYTES + (p.kn2 ? kKnParts * 4 : 0));
+          tma_load_3d(smem + SM_Q + t * TILE_BYTES, &tm_q, &bars->q_full[t], 0, qrow, qz + t);
+          if (p.kn2)  // the kv head's |k|^2 record, for the softmax's score bound
+            bulk_load(&bars->kn[t][q_loads[t] & 1][0],
+                      p.kn2 + static_cast<size_t>(kvz_of(un, p)) * kKnParts, kKnParts * 4,
+                      &bars->q_full[t]);
+          ++q_loads[t];
+        }
         const int kvz = un.b * p.G + un.g;
         for (int it = 0; it < kr.count; ++it, ++gt) {
           const int st = gt % NSTAGE;
@@ -352,7 +358,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       // Exit drain: every copy this CTA issued must have landed before the CTA
       // leaves (no-op on the normal path, where the consumers already saw them).
-      if (q_loads > 0) mbar_wait_drain(&bars->q_full, (q_loads - 1) & 1);
+      for (int t = 0; t < 2; ++t)
+        if (q_loads[t] > 0) mbar_wait_drain(&bars->q_full[t], (q_loads[t] - 1) & 1);
       for (int x = max(0, gt - NSTAGE); x < gt; ++x)
         mbar_wait_drain(&bars->kv_full[x % NSTAGE], (x / NSTAGE) & 1);
     }
@@ -363,6 +370,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t k_addr0 = smem_u32(smem + SM_K);
     int gt = 0;             // K/V tiles consumed (all units)
     int ts[2] = {0, 0};     // S products issued per head (all units)
+    int qf[2] = {0, 0};     // Q tiles consumed per head (all units)
     int qr[2] = {0, 0};     // rotated Q tiles consumed per head (rotary embedding)
     bool ok = true;
     for (int k = 0; ok; ++k) {
@@ -370,7 +378,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (u < 0) break;
       const Unit un = unit_of(u, p);
       const int n = kv_range(un.qb, p).count;
-      if (!mbar_wait(&bars->q_full, k & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
       for (int it = 0; it < n; ++it, ++gt) {
         const int st = gt % NSTAGE;
         if (!mbar_wait(&bars->kv_full[st], (gt / NSTAGE) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
@@ -380,8 +387,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             ok = false;
             break;
           }
+          if (it == 0) {  // the unit's first product of head t needs its Q tile
+            if (!mbar_wait(&bars->q_full[t], qf[t] & 1, ab, p.status, kTimeoutCode)) {
+              ok = false;
+              break;
+            }
+            ++qf[t];
+          }
           if constexpr (kRope) {
-            // the unit's first product of head t needs its Q tile rotated
+            // and, with the rotary embedding, that tile turned
             if (it == 0) {
               if (!mbar_wait(&bars->q_ready[t], qr[t] & 1, ab, p.status, kTimeoutCode)) {
                 ok = false;
@@ -482,12 +496,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     int ts = 0;  // tiles of this head (all units): S, P and O-done phases
     int uo = 0;  // units of this head: O-full / O-empty phases
     int tt = 0;  // tiles of two-head units: ping-pong phases (same count in both heads)
+    int uq = 0;  // Q tiles of this head (all units): Q-full phases and record slots
     bool ok = true;
     for (int k = 0; ok; ++k) {
       const int u = unit_at(k, p);
       if (u < 0) break;
       const Unit un = unit_of(u, p);
       if (t == 1 && !un.two) continue;
+      const int qk = uq++;  // this head's Q tile count: phase of q_full[t], record slot
       const KvRange kr = kv_range(un.qb, p);
       const int n = kr.count;
       const int qb = un.qb;
@@ -500,7 +516,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
       if constexpr (kRope) {
         // turn this row of head t's Q tile (position i) before any Q K^T reads it
-        if (!mbar_wait(&bars->q_full, k & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        if (!mbar_wait(&bars->q_full[t], qk & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
         if (i < p.S)
           rope::rope_rotate_smem_row(smem + SM_Q + t * TILE_BYTES + r * 128, r,
                                      p.rope_tab + static_cast<size_t>(i) * rope::kPairs);
@@ -514,11 +530,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // soon as their only Q K^T is done, before this read could happen.
       bool fast = false;
       if (p.kn2 != nullptr && n >= 2) {
-        // Q and the record landed with q_full (phase k); they stay until every
-        // Q K^T of the unit is done, and the last one (tile n - 1 >= 1) waits
-        // for this thread's release of S of tile n - 2 >= 0.
-        if (!mbar_wait(&bars->q_full, k & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
-        const float bound = score_bound(smem + SM_Q + t * TILE_BYTES + r * 128, r, &bars->kn[k & 1][0], sl2);
+        // Q and the record landed with q_full[t] (phase qk); they stay until
+        // every Q K^T of the unit is done, and the last one (tile n - 1 >= 1)
+        // waits for this thread's release of S of tile n - 2 >= 0.
+        if (!mbar_wait(&bars->q_full[t], qk & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        const float bound = score_bound(smem + SM_Q + t * TILE_BYTES + r * 128, r, &bars->kn[t][qk & 1][0], sl2);
         fast = __all_sync(0xffffffffu, bound <= kBoundMax);
         if (fast) m_run = bound - kFastSlack;
       }

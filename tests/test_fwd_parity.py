@@ -260,3 +260,19 @@ def test_score_bound_tiny_queries():
     torch.cuda.synchronize()
     assert gq.gqa_attn_last_device_status() == gq.GQA_OK
     _oracle_check(q, k, v, o, lse)
+
+
+@pytest.mark.parametrize("window,n_sink", [(0, 0), (300, 70)])
+def test_score_bound_persistent_varying_norms(window, n_sink):
+    """R = 3 (every other unit has one head) and more units than SMs, with the
+    queries of every other 128-row block scaled 8x: the bound decisions differ
+    from unit to unit, so each head must read its own unit's Q tile and record
+    (one Q barrier per head; a phase left over from an earlier unit must not
+    pass for the current one)."""
+    B, H, G, S = 4, 6, 2, 2048
+    q, k, v = make_inputs(B, H, G, S, seed=23)
+    q[:, :, (torch.arange(S) // 128) % 2 == 0] *= 8  # exact in bf16
+    o, lse = gq.fwd(q.cuda(), k.cuda(), v.cuda(), window=window, n_sink=n_sink, score_bound=True)
+    torch.cuda.synchronize()
+    assert gq.gqa_attn_last_device_status() == gq.GQA_OK
+    _oracle_check(q, k, v, o, lse, window=window, n_sink=n_sink)
