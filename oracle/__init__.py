@@ -71,6 +71,10 @@ def _declare(lib):
     lib.oracle_rope_rotate.restype = None
     lib.oracle_round_bf16.argtypes = [dp, ctypes.c_long]
     lib.oracle_round_bf16.restype = None
+    lib.oracle_decode_e4m3.argtypes = [ctypes.c_ubyte]
+    lib.oracle_decode_e4m3.restype = d
+    lib.oracle_decode_e4m3_array.argtypes = [ctypes.POINTER(ctypes.c_ubyte), dp, ctypes.c_long, d]
+    lib.oracle_decode_e4m3_array.restype = None
     return lib
 
 
@@ -252,3 +256,25 @@ def attn_fwd_yarn(q, k, v, *, base=10000.0, factor=32.0, orig_ctx=6400, alpha=1.
                           beta=beta, rounded=rounded, lib=lib)
     return attn_fwd(qr, kr, v, causal=causal, window=window, n_sink=n_sink, scale=scale * ms * ms,
                     lib=lib)
+
+
+# ------------------------------------------------------------------ FP8 E4M3
+
+def decode_e4m3(x, scale=1.0, lib=None):
+    """Exact float64 values of OCP E4M3 bytes (uint8 array) times `scale`."""
+    lib = lib or load()
+    b = np.ascontiguousarray(np.asarray(x, dtype=np.uint8))
+    out = np.zeros(b.shape, dtype=np.float64)
+    lib.oracle_decode_e4m3_array(b.ctypes.data_as(ctypes.POINTER(ctypes.c_ubyte)), _ptr(out),
+                                 b.size, float(scale))
+    return out
+
+
+def attn_fwd_fp8(q8, k8, v, q_scale, k_scale, *, causal=True, window=0, n_sink=0, scale=None,
+                 lib=None):
+    """Forward on fp8 queries and keys: attn_fwd(decode(q8) * q_scale,
+    decode(k8) * k_scale, v) with v as given (float64 of the bf16 values)."""
+    lib = lib or load()
+    q = decode_e4m3(q8, q_scale, lib=lib)
+    k = decode_e4m3(k8, k_scale, lib=lib)
+    return attn_fwd(q, k, v, causal=causal, window=window, n_sink=n_sink, scale=scale, lib=lib)

@@ -360,3 +360,34 @@ void oracle_round_bf16(double *x, long n)
         x[e] = (double)f;
     }
 }
+
+/* ---------------------------------------------------------------- FP8 E4M3
+ *
+ * "SnapKitty Transformer 8B" (section "Protected Inventions") names a forward
+ * "with FP8 computation"; the pages give no format.  The format taken is the
+ * OCP 8-bit floating point specification's E4M3 (the fp8 type of the sm_100
+ * tensor cores): 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits;
+ * exponent field 0 encodes subnormals m / 8 * 2^-6; S.1111.111 is NaN and
+ * there are no infinities (largest finite value 448).  A tensor is stored as
+ * bytes plus one fp32 scale: value = decode(byte) * scale.  The oracle takes
+ * those exact values and runs the float64 definition on them.
+ */
+double oracle_decode_e4m3(unsigned char b)
+{
+    int sign = (b >> 7) & 1, e = (b >> 3) & 15, m = b & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* out[i] = decode(bytes[i]) * scale for n values. */
+void oracle_decode_e4m3_array(const unsigned char *bytes, double *out, long n, double scale)
+{
+    for (long i = 0; i < n; ++i)
+        out[i] = oracle_decode_e4m3(bytes[i]) * scale;
+}
