@@ -180,7 +180,7 @@ class ClockSampler:
 class Problem:
     """Device tensors of one workload and the calls of one step (through the C ABI)."""
 
-    def __init__(self, w, dev, seed, with_bwd, yarn=False):
+    def __init__(self, w, dev, seed, with_bwd, yarn=False, fp8=False):
         import torch
         import causal_grouped_query_gqa_b300 as gq
         from causal_grouped_query_gqa_b300.inputs import make_inputs
@@ -199,6 +199,17 @@ class Problem:
         # the forward entry point the library's own fwd() picks for this size
         fwd_f, _ = step_flops(w, False)
         self.score_bound = fwd_f >= gq.SCORE_BOUND_MIN_FLOPS
+        # the fp8 forward: q and k quantised once to E4M3 (before any timing)
+        self.fp8 = fp8
+        if fp8:
+            self.score_bound = False
+            self.q8, self.k8 = torch.empty_like(q, dtype=torch.uint8), torch.empty_like(
+                self.ins[1], dtype=torch.uint8)
+            self.fp8_scales = []
+            for src, dst in ((q, self.q8), (self.ins[1], self.k8)):
+                inv = 440.0 / float(src.float().abs().max())
+                dst.copy_(gq.quantize_e4m3(src, inv))
+                self.fp8_scales.append(1.0 / inv)
         # the YaRN forward (rotary embeddings on q and k) instead of the plain one
         self.yarn = yarn
         if yarn:
@@ -213,7 +224,11 @@ class Problem:
         q_, k_, v_, do_ = ins
         o_, lse_, dq_, dk_, dv_ = outs
         bound = self.score_bound if score_bound is None else score_bound
-        if self.yarn:
+        if self.fp8:
+            rc = gq.gqa_attn_fwd_fp8(self.q8, self.k8, v_, o_, lse_, B, H, G, S, d, w.causal,
+                                     w.window, w.n_sink, w.scale, self.fp8_scales[0],
+                                     self.fp8_scales[1], strm)
+        elif self.yarn:
             y = gq.YARN_DEFAULTS
             rc = gq.gqa_attn_fwd_yarn(q_, k_, v_, o_, lse_, B, H, G, S, d, w.causal, w.window,
                                       w.n_sink, w.scale, y["rope_base"], y["rope_factor"],
@@ -236,7 +251,7 @@ class Problem:
 
     def launches_per_step(self, score_bound=None):
         bound = self.score_bound if score_bound is None else score_bound
-        return (3 if self.yarn else (2 if bound else 1)) + (4 if self.with_bwd else 0)
+        return (3 if self.yarn else (2 if bound and not self.fp8 else 1)) + (4 if self.with_bwd else 0)
 
 
 def timed_steps(pb, steps, warmup, flush, stream, world, score_bound=None, clocks=False):
@@ -404,14 +419,15 @@ def run_ours(args, w, rank, world, local_rank):
         extras = {}
         for name, step in EXTRA_WORKLOADS:
             ew = WORKLOADS[name]
-            epb = Problem(ew, dev, seed=0, with_bwd=(step == "fwd+bwd"), yarn=(step == "fwd_yarn"))
+            epb = Problem(ew, dev, seed=0, with_bwd=(step == "fwd+bwd"), yarn=(step == "fwd_yarn"),
+                          fp8=(step == "fwd_fp8"))
             e_steps = max(3, min(args.steps, 10))
             e_ms, e_kernel, e_clk = timed_steps(epb, e_steps, 3, flush, stream, 1, clocks=True)
             res = summarize(ew, epb, e_kernel, e_ms, e_steps, 1, peaks, name)
             res.update({"step": step, "steps": e_steps, "clocks": e_clk,
                         "config": {"B": ew.B, "H": ew.H, "G": ew.G, "S": ew.S,
                                    "window": ew.window, "n_sink": ew.n_sink}})
-            extras[name if step != "fwd_yarn" else name + "+yarn"] = res
+            extras[name + {"fwd_yarn": "+yarn", "fwd_fp8": "+fp8"}.get(step, "")] = res
             del epb
             torch.cuda.empty_cache()
         out["extra_workloads"] = extras
@@ -425,6 +441,7 @@ EXTRA_WORKLOADS = [
     ("window_b1_h128_g16_s32768_w4096_sink128", "fwd"),
     ("bwd_b4_h32_g8_s4096", "fwd+bwd"),
     ("wide_b1_h128_g16_s8192", "fwd_yarn"),   # YaRN rotary forward (table + key rotation + forward)
+    ("wide_b1_h128_g16_s8192", "fwd_fp8"),    # E4M3 queries and keys (quantised before timing)
 ]
 
 

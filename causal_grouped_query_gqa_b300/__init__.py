@@ -15,6 +15,9 @@ Low-level calls (same names and argument order as the C header):
                       rope_factor, rope_orig_ctx, rope_alpha, rope_beta, workspace,
                       workspace_bytes, stream)   (YaRN rotary embeddings on q and k)
     gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d)
+    gqa_attn_fwd_fp8(q8, k8, v, o, lse, B, H, G, S, d, causal, window, n_sink, scale, q_scale,
+                     k_scale, stream)   (E4M3 queries and keys, tcgen05 kind::f8f6f4 Q K^T)
+    gqa_attn_quantize_e4m3(x, out, n, inv_scale, stream)   (bf16 -> E4M3 bytes)
     gqa_attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, G, S, d, causal, window,
                  n_sink, scale, workspace, workspace_bytes, stream)
     gqa_attn_bwd_workspace_size(B, H, G, S, d)
@@ -24,7 +27,8 @@ Low-level calls (same names and argument order as the C header):
     gqa_attn_timing_enable(on), gqa_attn_timing_collect(buf)  (per-kernel CUDA-event times)
 Tensor helpers: ``fwd(q, k, v, ...)`` (picks the score-bound entry point for
 problems of at least SCORE_BOUND_MIN_FLOPS causal FLOPs, the plain one below)
-``fwd_yarn(q, k, v, ...)`` and ``bwd(q, k, v, o, dout, lse, ...)``.
+``fwd_yarn(q, k, v, ...)``, ``fwd_fp8(q8, k8, v, q_scale, k_scale, ...)``,
+``quantize_e4m3(x, inv_scale)`` and ``bwd(q, k, v, o, dout, lse, ...)``.
 """
 from __future__ import annotations
 
@@ -32,6 +36,7 @@ from ._lib import (GQA_ERR_ALIGN, GQA_ERR_CUDA, GQA_ERR_DEVICE_TIMEOUT, GQA_ERR_
                    GQA_ERR_DEVICE_BOUNDS, GQA_ERR_MASK, GQA_ERR_NULL, GQA_ERR_SCALE,
                    GQA_ERR_SHAPE, GQA_ERR_TOO_LARGE, GQA_ERR_ROPE, YARN_DEFAULTS,
                    fwd_yarn, gqa_attn_fwd_yarn, gqa_attn_fwd_yarn_workspace_size,
+                   fwd_fp8, gqa_attn_fwd_fp8, gqa_attn_quantize_e4m3, quantize_e4m3,
                    GQA_ERR_WORKSPACE, GQA_NOALLOC_SCRATCH_BYTES, GQA_OK, SCORE_BOUND_MIN_FLOPS,
                    GqaError, bwd, fwd, visible_pairs,
                    gqa_attn_bwd, gqa_attn_bwd_noalloc,
@@ -41,7 +46,8 @@ from ._lib import (GQA_ERR_ALIGN, GQA_ERR_CUDA, GQA_ERR_DEVICE_TIMEOUT, GQA_ERR_
                    lib_path, load_library, selftest_timeout, timing_buffer)
 
 __all__ = [
-    "fwd", "bwd", "fwd_yarn", "gqa_attn_fwd_yarn", "gqa_attn_fwd_yarn_workspace_size",
+    "fwd", "bwd", "fwd_yarn", "fwd_fp8", "gqa_attn_fwd_fp8", "gqa_attn_quantize_e4m3",
+    "quantize_e4m3", "gqa_attn_fwd_yarn", "gqa_attn_fwd_yarn_workspace_size",
     "GQA_ERR_ROPE", "YARN_DEFAULTS", "visible_pairs", "SCORE_BOUND_MIN_FLOPS", "gqa_attn_fwd", "gqa_attn_fwd_ws", "gqa_attn_fwd_workspace_size",
     "gqa_attn_bwd", "gqa_attn_bwd_noalloc",
     "gqa_attn_bwd_workspace_size", "GQA_ERR_TOO_LARGE", "GQA_ERR_DEVICE_BOUNDS", "GQA_NOALLOC_SCRATCH_BYTES",

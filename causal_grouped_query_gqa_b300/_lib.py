@@ -64,6 +64,10 @@ def load_library():
         lib.gqa_attn_fwd_yarn.restype = i
         lib.gqa_attn_fwd_yarn_workspace_size.argtypes = [i, i, i, i, i]
         lib.gqa_attn_fwd_yarn_workspace_size.restype = sz
+        lib.gqa_attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, f, f, vp]
+        lib.gqa_attn_fwd_fp8.restype = i
+        lib.gqa_attn_quantize_e4m3.argtypes = [vp, vp, ctypes.c_longlong, f, vp]
+        lib.gqa_attn_quantize_e4m3.restype = i
         lib.gqa_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                      i, i, i, i, i, i, i, i, f, vp, sz, vp]
         lib.gqa_attn_bwd.restype = i
@@ -136,6 +140,18 @@ def gqa_attn_fwd_yarn(q, k, v, o, lse, B, H, G, S, d, causal, window, n_sink, sc
                                             int(rope_orig_ctx), float(rope_alpha),
                                             float(rope_beta), _p(workspace), int(workspace_bytes),
                                             _stream(stream))
+
+
+def gqa_attn_fwd_fp8(q8, k8, v, o, lse, B, H, G, S, d, causal, window, n_sink, scale, q_scale,
+                     k_scale, stream=None):
+    return load_library().gqa_attn_fwd_fp8(_p(q8), _p(k8), _p(v), _p(o), _p(lse), B, H, G, S, d,
+                                           int(causal), int(window), int(n_sink), float(scale),
+                                           float(q_scale), float(k_scale), _stream(stream))
+
+
+def gqa_attn_quantize_e4m3(x, out, n, inv_scale, stream=None):
+    return load_library().gqa_attn_quantize_e4m3(_p(x), _p(out), int(n), float(inv_scale),
+                                                 _stream(stream))
 
 
 def gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d):
@@ -302,6 +318,40 @@ def fwd_yarn(q, k, v, *, causal=True, window=0, n_sink=0, scale=None, rope_base=
                            workspace.numel() * workspace.element_size(), stream)
     if rc != GQA_OK:
         raise GqaError(rc, "gqa_attn_fwd_yarn")
+    return o, l
+
+
+def quantize_e4m3(x, inv_scale, *, stream=None):
+    """E4M3 bytes of a bf16 CUDA tensor: round(x * inv_scale), saturating
+    (gqa_attn_quantize_e4m3); returns a uint8 tensor of the same shape."""
+    import torch
+    if x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous() or x.numel() % 16:
+        raise ValueError("quantize_e4m3: contiguous CUDA bf16 tensor with a multiple of 16 elements")
+    out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    rc = gqa_attn_quantize_e4m3(x, out, x.numel(), inv_scale, stream)
+    if rc != GQA_OK:
+        raise GqaError(rc, "gqa_attn_quantize_e4m3")
+    return out
+
+
+def fwd_fp8(q8, k8, v, q_scale, k_scale, *, causal=True, window=0, n_sink=0, scale=None,
+            out=None, lse=None, stream=None):
+    """o, lse = fwd_fp8(q8 [B,H,S,64] uint8, k8 [B,G,S,64] uint8 (E4M3 bytes), v
+    [B,G,S,64] bf16, q_scale, k_scale): attention over decode(q8) * q_scale and
+    decode(k8) * k_scale (gqa_attn_fwd_fp8)."""
+    import torch
+    B, H, S, d = q8.shape
+    G = k8.shape[1]
+    _check(q8, (B, H, S, d), torch.uint8, "q8")
+    _check(k8, (B, G, S, d), torch.uint8, "k8")
+    _check(v, (B, G, S, d), torch.bfloat16, "v")
+    scale = 1.0 / d ** 0.5 if scale is None else scale
+    o = torch.empty((B, H, S, d), dtype=torch.bfloat16, device=v.device) if out is None else out
+    l = torch.empty((B, H, S), dtype=torch.float32, device=v.device) if lse is None else lse
+    rc = gqa_attn_fwd_fp8(q8, k8, v, o, l, B, H, G, S, d, causal, window, n_sink, scale, q_scale,
+                          k_scale, stream)
+    if rc != GQA_OK:
+        raise GqaError(rc, "gqa_attn_fwd_fp8")
     return o, l
 
 

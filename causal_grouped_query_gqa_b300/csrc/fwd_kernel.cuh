@@ -257,7 +257,11 @@ __device__ __forceinline__ int unit_at(int k, const Params &p) {
 
 // kRope: the query tiles are turned by the rotary embedding (rope_kernels.cuh)
 // in shared memory before their first Q K^T; the keys arrive already rotated.
-template <bool kRope>
+// kFp8: queries and keys are OCP E4M3 bytes (64-byte rows, 64-byte swizzle,
+// 8 KB tiles in the 16 KB slots); S = Q K^T runs as tcgen05.mma
+// kind::f8f6f4 (K = 32 per instruction) and the two per-tensor scales are
+// folded into scale_log2 on the host.  P.V stays bf16.
+template <bool kRope, bool kFp8>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gqa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
@@ -269,6 +273,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   Bars *bars = reinterpret_cast<Bars *>(smem + SM_BARS);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // bytes of one Q or K tile as loaded (fp8 rows are half as long)
+  constexpr uint32_t kQTileBytes = kFp8 ? TILE_BYTES / 2 : TILE_BYTES;
+  static_assert(!(kFp8 && kRope), "the fp8 forward takes no rotary embedding");
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full[0], 1);
@@ -326,7 +333,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         GQA_REPORT(p.status, un.qb >= 0 && un.qb < p.n_qblocks && kr.count >= 1 &&
                                 qz + (un.two ? 1 : 0) < p.B * p.H);
         for (int t = 0; t < (un.two ? 2 : 1); ++t) {
-          mbar_arrive_expect_tx(&bars->q_full[t], TILE_BYTES + (p.kn2 ? kKnParts * 4 : 0));
+          mbar_arrive_expect_tx(&bars->q_full[t], kQTileBytes + (p.kn2 ? kKnParts * 4 : 0));
           tma_load_3d(smem + SM_Q + t * TILE_BYTES, &tm_q, &bars->q_full[t], 0, qrow, qz + t);
           if (p.kn2)  // the kv head's |k|^2 record, for the softmax's score bound
             bulk_load(&bars->kn[t][q_loads[t] & 1][0],
@@ -350,7 +357,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (blockIdx.x == 0 && k == 0 && it == min(1, kr.count - 1)) continue;
 #endif
           GQA_REPORT(p.status, kb >= 0 && kb * BN < p.S && kvz < p.B * p.G);
-          mbar_arrive_expect_tx(&bars->kv_full[st], 2 * TILE_BYTES);
+          mbar_arrive_expect_tx(&bars->kv_full[st], kQTileBytes + TILE_BYTES);
           tma_load_3d(smem + SM_K + st * TILE_BYTES, &tm_k, &bars->kv_full[st], 0, kb * BN, kvz);
           tma_load_3d(smem + SM_V + st * TILE_BYTES, &tm_v, &bars->kv_full[st], 0, kb * BN, kvz);
           GQA_TRACE_EVENT(0, 1, k == 0 ? it : kTraceSteps);
@@ -365,7 +372,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else if (warp == 2 && lane == 0) {
     // ================================================================ QK issuer
-    const uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false, false);
+    const uint32_t idesc_qk = kFp8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN, false, false);
     const uint32_t q_addr0 = smem_u32(smem + SM_Q);
     const uint32_t k_addr0 = smem_u32(smem + SM_K);
     int gt = 0;             // K/V tiles consumed (all units)
@@ -405,11 +412,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
           }
           tc_fence_after_sync();
-          const uint64_t ad = sdesc_sw128(q_addr0 + t * TILE_BYTES, 16, 1024);
-          const uint64_t bd = sdesc_sw128(k_addr0 + st * TILE_BYTES, 16, 1024);
+          if constexpr (kFp8) {
+            const uint64_t ad = sdesc_sw64(q_addr0 + t * TILE_BYTES, 16, 512);
+            const uint64_t bd = sdesc_sw64(k_addr0 + st * TILE_BYTES, 16, 512);
 #pragma unroll
-          for (int ks = 0; ks < HD / 16; ++ks)  // K step 16 bf16 = 32 B inside the 128-B row
-            mma_bf16_ss(tbase + col_s(t), ad + 2 * ks, bd + 2 * ks, idesc_qk, ks > 0);
+            for (int ks = 0; ks < HD / 32; ++ks)  // K step 32 bytes inside the 64-B row
+              mma_f8_ss(tbase + col_s(t), ad + 2 * ks, bd + 2 * ks, idesc_qk, ks > 0);
+          } else {
+            const uint64_t ad = sdesc_sw128(q_addr0 + t * TILE_BYTES, 16, 1024);
+            const uint64_t bd = sdesc_sw128(k_addr0 + st * TILE_BYTES, 16, 1024);
+#pragma unroll
+            for (int ks = 0; ks < HD / 16; ++ks)  // K step 16 bf16 = 32 B inside the 128-B row
+              mma_bf16_ss(tbase + col_s(t), ad + 2 * ks, bd + 2 * ks, idesc_qk, ks > 0);
+          }
           mma_commit(&bars->s_full[t]);
           ++ts[t];
         }

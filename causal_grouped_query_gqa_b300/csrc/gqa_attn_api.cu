@@ -16,6 +16,7 @@
 #include "trace.cuh"
 #include "bwd_kernels.cuh"
 #include "fwd_kernel.cuh"
+#include "quantize_kernel.cuh"
 #include "selftest_kernel.cuh"
 
 namespace {
@@ -66,7 +67,8 @@ int device_state(DeviceState **out) {
             cudaGetSymbolAddress(reinterpret_cast<void **>(&st.status), g_device_status),
             "cudaGetSymbolAddress(device status word)"))
       return GQA_ERR_CUDA;
-    for (auto kern : {gqa::fwd::gqa_fwd_kernel<false>, gqa::fwd::gqa_fwd_kernel<true>}) {
+    for (auto kern : {gqa::fwd::gqa_fwd_kernel<false, false>, gqa::fwd::gqa_fwd_kernel<true, false>,
+                      gqa::fwd::gqa_fwd_kernel<false, true>}) {
       if (gqa::cuda_failed(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                 gqa::fwd::SMEM_BYTES),
                            "cudaFuncSetAttribute(forward shared memory)"))
@@ -103,6 +105,25 @@ int make_tmap_bf16(CUtensorMap *map, const void *base, uint64_t outer, uint64_t 
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     gqa::set_error_detail("cuTensorMapEncodeTiled rejected a bf16 tensor map");
+    return GQA_ERR_CUDA;
+  }
+  return GQA_OK;
+}
+
+// 3-D E4M3 (byte) tensor map over [outer][rows][64] with a box of
+// [1][box_rows][64]: 64-byte rows, 64-byte swizzle; rows past `rows` read as zeros.
+int make_tmap_e4m3(CUtensorMap *map, const void *base, uint64_t outer, uint64_t rows,
+                   uint32_t box_rows) {
+  cuuint64_t dims[3] = {64, rows, outer};
+  cuuint64_t strides[2] = {64, rows * 64};
+  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    gqa::set_error_detail("cuTensorMapEncodeTiled rejected an fp8 tensor map");
     return GQA_ERR_CUDA;
   }
   return GQA_OK;
@@ -163,20 +184,26 @@ namespace {
 
 // The forward launch shared by the entry points; kn2 (the score-bound record
 // that fwd_knorm_kernel writes first, on the same stream) may be null, and so
-// may rope_tab (the rotary table; k is then already rotated).
+// may rope_tab (the rotary table; k is then already rotated).  fp8: q and k
+// are E4M3 bytes and `scale` already carries their two dequantisation scales.
 int launch_forward(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
                    int G, int S, int causal, int window, int n_sink, float scale, float *kn2,
-                   const float2 *rope_tab, cudaStream_t st) {
+                   const float2 *rope_tab, cudaStream_t st, bool fp8 = false) {
   DeviceState *ds = nullptr;
   int rc = device_state(&ds);
   if (rc != GQA_OK) return rc;
 
   using namespace gqa::fwd;
   CUtensorMap tq, tk, tv;
-  if (make_tmap_bf16(&tq, q, static_cast<uint64_t>(B) * H, S, BM) != GQA_OK ||
-      make_tmap_bf16(&tk, k, static_cast<uint64_t>(B) * G, S, BN) != GQA_OK ||
-      make_tmap_bf16(&tv, v, static_cast<uint64_t>(B) * G, S, BN) != GQA_OK)
+  if (fp8) {
+    if (make_tmap_e4m3(&tq, q, static_cast<uint64_t>(B) * H, S, BM) != GQA_OK ||
+        make_tmap_e4m3(&tk, k, static_cast<uint64_t>(B) * G, S, BN) != GQA_OK)
+      return GQA_ERR_CUDA;
+  } else if (make_tmap_bf16(&tq, q, static_cast<uint64_t>(B) * H, S, BM) != GQA_OK ||
+             make_tmap_bf16(&tk, k, static_cast<uint64_t>(B) * G, S, BN) != GQA_OK) {
     return GQA_ERR_CUDA;
+  }
+  if (make_tmap_bf16(&tv, v, static_cast<uint64_t>(B) * G, S, BN) != GQA_OK) return GQA_ERR_CUDA;
 
   Params p{};
   p.B = B;
@@ -212,10 +239,12 @@ int launch_forward(const void *q, const void *k, const void *v, void *o, float *
       return GQA_ERR_CUDA;
   }
   gqa::timing_begin(GQA_KERNEL_FWD, st);
-  if (rope_tab)
-    gqa_fwd_kernel<true><<<static_cast<unsigned>(grid), NTHREADS, SMEM_BYTES, st>>>(tq, tk, tv, p);
+  if (fp8)
+    gqa_fwd_kernel<false, true><<<static_cast<unsigned>(grid), NTHREADS, SMEM_BYTES, st>>>(tq, tk, tv, p);
+  else if (rope_tab)
+    gqa_fwd_kernel<true, false><<<static_cast<unsigned>(grid), NTHREADS, SMEM_BYTES, st>>>(tq, tk, tv, p);
   else
-    gqa_fwd_kernel<false><<<static_cast<unsigned>(grid), NTHREADS, SMEM_BYTES, st>>>(tq, tk, tv, p);
+    gqa_fwd_kernel<false, false><<<static_cast<unsigned>(grid), NTHREADS, SMEM_BYTES, st>>>(tq, tk, tv, p);
   gqa::timing_end(GQA_KERNEL_FWD, st);
   return gqa::cuda_failed(cudaGetLastError(), "launch of the forward kernel") ? GQA_ERR_CUDA
                                                                                : GQA_OK;
@@ -252,6 +281,42 @@ int gqa_attn_fwd_ws(const void *q, const void *k, const void *v, void *o, float 
   if (workspace_bytes < gqa_attn_fwd_workspace_size(B, H, G, S, d)) return GQA_ERR_WORKSPACE;
   return launch_forward(q, k, v, o, lse, B, H, G, S, causal, window, n_sink, scale,
                         static_cast<float *>(workspace), nullptr, static_cast<cudaStream_t>(stream));
+}
+
+int gqa_attn_fwd_fp8(const void *q8, const void *k8, const void *v, void *o, float *lse, int B,
+                     int H, int G, int S, int d, int causal, int window, int n_sink, float scale,
+                     float q_scale, float k_scale, void *stream) {
+  int rc = check_common(B, H, G, S, d, causal, window, n_sink, scale);
+  if (rc != GQA_OK) return rc;
+  if (!(std::isfinite(q_scale) && q_scale > 0.f && std::isfinite(k_scale) && k_scale > 0.f))
+    return GQA_ERR_SCALE;
+  const double folded = static_cast<double>(scale) * q_scale * k_scale;
+  if (!(folded < 3.0e38 && folded > 1.0e-37)) return GQA_ERR_SCALE;
+  if (!q8 || !k8 || !v || !o || !lse) return GQA_ERR_NULL;
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return GQA_ERR_ALIGN;
+  return launch_forward(q8, k8, v, o, lse, B, H, G, S, causal, window, n_sink,
+                        static_cast<float>(folded), nullptr, nullptr,
+                        static_cast<cudaStream_t>(stream), true);
+}
+
+int gqa_attn_quantize_e4m3(const void *x, void *out, long long n, float inv_scale, void *stream) {
+  if (!x || !out) return GQA_ERR_NULL;
+  if (n <= 0 || (n & 15) != 0) return GQA_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(out)) return GQA_ERR_ALIGN;
+  if (!(std::isfinite(inv_scale) && inv_scale > 0.f)) return GQA_ERR_SCALE;
+  DeviceState *ds = nullptr;
+  int rc = device_state(&ds);
+  if (rc != GQA_OK) return rc;
+  const long long n16 = n / 16;
+  long long blocks = (n16 + 255) / 256;
+  blocks = blocks < 1 ? 1 : (blocks > 8LL * ds->sm_count ? 8LL * ds->sm_count : blocks);
+  gqa::quantize_e4m3_kernel<<<static_cast<unsigned>(blocks), 256, 0,
+                              static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const __nv_bfloat16 *>(x), static_cast<uint8_t *>(out), n16, inv_scale);
+  return gqa::cuda_failed(cudaGetLastError(), "launch of the fp8 quantisation kernel")
+             ? GQA_ERR_CUDA
+             : GQA_OK;
 }
 
 size_t gqa_attn_fwd_yarn_workspace_size(int B, int H, int G, int S, int d) {

@@ -316,6 +316,47 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
+// The same descriptor for the 64-byte swizzle (TMA CU_TENSOR_MAP_SWIZZLE_64B):
+// layout type 4 (bits 61-63); a K-major operand then has 64-byte rows and its
+// 8-row groups 512 bytes apart (SBO = 512).
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t lbo_bytes,
+                                               uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(4) << 61;
+  return d;
+}
+
+// Instruction descriptor of kind::f8f6f4 with fp32 accumulation: D format f32
+// (bits 4-5 = 1), A and B format E4M3 (bits 7-9 and 10-12 = 0), both K-major
+// (bits 15, 16 = 0), N >> 3 (17-22), M >> 4 (24-28).
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem] with 8-bit operands (K = 32 per instruction);
+// issued by one thread.
+__device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Two floats to two OCP E4M3 bytes (round to nearest even, saturating to
+// +-448; NaN stays NaN): lo in bits 0-7.
+__device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // Instruction descriptor of kind::f16 with fp32 accumulation: D format f32
 // (bits 4-5 = 1), A and B format (7-9, 10-12: 0 = fp16, 1 = bf16; one
 // format for both operands), A/B major-ness (bit 15 / 16: 0 = K-major,

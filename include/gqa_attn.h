@@ -148,6 +148,34 @@ GQA_API int gqa_attn_fwd_yarn(const void *q, const void *k, const void *v, void 
                       void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Forward on FP8 queries and keys.  Page: "SnapKitty Transformer 8B", section
+ * "Protected Inventions" (a forward "with FP8 computation"; the pages name no
+ * format).  q8 [B][H][S][d] and k8 [B][G][S][d] are OCP E4M3 bytes (1 sign, 4
+ * exponent bits with bias 7, 3 mantissa bits; S.1111.111 is NaN), standing for
+ * decode(byte) * q_scale and decode(byte) * k_scale; v [B][G][S][d] is bf16.
+ * S = Q K^T runs on the tensor cores as tcgen05.mma kind::f8f6f4 with fp32
+ * accumulation, the scores are scale * q_scale * k_scale * q8 . k8, and P.V is
+ * the bf16 product of gqa_attn_fwd, so o and lse are those of gqa_attn_fwd on
+ * the decoded queries and keys.  q8, k8 16-byte aligned.  Errors as
+ * gqa_attn_fwd, plus GQA_ERR_SCALE when q_scale or k_scale is not finite and
+ * positive or scale * q_scale * k_scale leaves the fp32 range.
+ */
+GQA_API int gqa_attn_fwd_fp8(const void *q8, const void *k8, const void *v, void *o, float *lse,
+                     int B, int H, int G, int S, int d,
+                     int causal, int window, int n_sink, float scale,
+                     float q_scale, float k_scale, void *stream);
+
+/*
+ * Quantisation to the fp8 forward's input format: out[i] = E4M3(x[i] *
+ * inv_scale) for n bf16 values x (device), round to nearest even, saturating
+ * to +-448 (NaN stays NaN); byte out[i] then stands for decode(out[i]) /
+ * inv_scale.  n a positive multiple of 16; x and out 16-byte aligned.  No page
+ * describes this call: it prepares inputs for gqa_attn_fwd_fp8.
+ */
+GQA_API int gqa_attn_quantize_e4m3(const void *x, void *out, long long n, float inv_scale,
+                                   void *stream);
+
+/*
  * Bytes of scratch that gqa_attn_bwd needs for these sizes: an fp32 dq
  * accumulator [B][H][S][d]; two fp32 row arrays [B][H][S_pad] with
  * S_pad = S rounded up to a multiple of 128 (lse * log2(e) and the row term

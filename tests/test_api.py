@@ -104,7 +104,16 @@ def _fwd_yarn(**kw):
                                 a["wsb"], a["stream"])
 
 
-@pytest.mark.parametrize("call", [_fwd, _fwd_ws, _fwd_yarn, _bwd])
+def _fwd_fp8(**kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=4, G=2, S=128, d=64,
+             causal=1, window=0, n_sink=0, scale=0.125, qs=0.01, ks=0.01, stream=0)
+    a.update(kw)
+    return gq.gqa_attn_fwd_fp8(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["G"],
+                               a["S"], a["d"], a["causal"], a["window"], a["n_sink"], a["scale"],
+                               a["qs"], a["ks"], a["stream"])
+
+
+@pytest.mark.parametrize("call", [_fwd, _fwd_ws, _fwd_yarn, _fwd_fp8, _bwd])
 def test_argument_errors(lib, call):
     assert call(B=0) == gq.GQA_ERR_SHAPE
     assert call(S=0) == gq.GQA_ERR_SHAPE
@@ -150,6 +159,19 @@ def test_fwd_yarn_specific_errors(lib):
     assert need == 1 * 2 * 128 * 64 * 2 + 128 * 32 * 8
     assert _fwd_yarn(wsb=need - 1) == gq.GQA_ERR_WORKSPACE
     assert gq.gqa_attn_fwd_yarn_workspace_size(1, 3, 2, 128, 64) == 0
+
+
+def test_fp8_specific_errors(lib):
+    assert _fwd_fp8(qs=0.0) == gq.GQA_ERR_SCALE
+    assert _fwd_fp8(ks=float("inf")) == gq.GQA_ERR_SCALE
+    assert _fwd_fp8(qs=1e-30, ks=1e-30) == gq.GQA_ERR_SCALE
+    assert _fwd_fp8(lse=None) == gq.GQA_ERR_NULL
+    q = gq.gqa_attn_quantize_e4m3
+    assert q(None, FAKE, 16, 1.0, 0) == gq.GQA_ERR_NULL
+    assert q(FAKE, FAKE, 15, 1.0, 0) == gq.GQA_ERR_SHAPE
+    assert q(FAKE, FAKE, 0, 1.0, 0) == gq.GQA_ERR_SHAPE
+    assert q(FAKE + 2, FAKE, 16, 1.0, 0) == gq.GQA_ERR_ALIGN
+    assert q(FAKE, FAKE, 16, 0.0, 0) == gq.GQA_ERR_SCALE
 
 
 def test_bwd_specific_errors(lib):
