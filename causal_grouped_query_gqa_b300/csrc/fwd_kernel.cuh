@@ -770,7 +770,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // (their scores are NaN whatever the reference); an infinite row gives an
 // infinite bound, hence the exact step.
 constexpr int kKnormThreads = 256;
-constexpr int kKnormUnroll = 4;
+constexpr int kKnormUnroll = 8;  // 256 rows (32 KB) per CTA pass: one slice of S = 8192 at once
 __global__ void __launch_bounds__(kKnormThreads)
     fwd_knorm_kernel(const __nv_bfloat16 *__restrict__ k, int S, float *__restrict__ kn2) {
   constexpr int kRowsPerPass = kKnormThreads / 8;
