@@ -19,9 +19,8 @@
 //          the fp32 dQ accumulator cleared;
 //   shift  LSE * log2(e) + e_i - E_g, so that the recomputed probabilities come
 //          out as P' = P 2^(E_g - e_i) <= P;
-//   main   one CTA per (b, kv head g, 128-key tile): the key rows (bf16) and
-//          V' = V 2^ev_j (fp16, one power of two per key row) stored once in
-//          TMEM as the A operands of S^T and dP''^T; then for
+//   main   one CTA per (b, kv head g, 128-key tile): V' = V 2^ev_j in fp16 in
+//          shared memory (one power of two per key row, taken once); then for
 //          each of the R query heads of g and each query tile that sees the key
 //          tile (a "step"), on tcgen05:
 //            S^T  = K Q^T  (bf16)      dP''^T = V' dO'^T  (fp16)   (TMEM, fp32)
@@ -82,17 +81,11 @@ constexpr int kMinLaunchRegs =
 constexpr uint32_t TMEM_COLS = 512;
 // TMEM columns
 constexpr uint32_t C_S = 0;     // S^T (128 fp32)
-constexpr uint32_t C_DP = 128;  // dP''^T (128 fp32)
-constexpr uint32_t C_PT = 256;  // P'^T (64 columns of fp16 pairs: 128 queries) until the
-                                // step's dV has read it, then the step's dQ tile (64 fp32)
+constexpr uint32_t C_DP = 128;  // dP^T (128 fp32)
+constexpr uint32_t C_PT = 256;  // P^T (64 columns of bf16 pairs: 128 queries)
 constexpr uint32_t C_DV = 320;  // dV accumulator (64 fp32)
 constexpr uint32_t C_DK = 384;  // dK accumulator (64 fp32)
-constexpr uint32_t C_KT = 448;  // the CTA's key rows: A operand of S^T (32 columns of bf16 pairs)
-constexpr uint32_t C_VT = 480;  // its V' rows: A operand of dP''^T (32 columns of fp16 pairs)
-constexpr uint32_t C_DQ = C_PT;
-// K and V' stay in TMEM for the CTA's life, so S^T and dP''^T read only Q and
-// dO' from shared memory (32 KB less per step on the shared-memory pipe, which
-// bounds this kernel); dQ borrows P'^T's columns, which dV has finished with.
+constexpr uint32_t C_DQ = 448;  // dQ tile (64 fp32)
 
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int SM_K = 0;
@@ -107,7 +100,7 @@ constexpr int SM_BARS = SM_VEC + NSTAGE * 2 * BQ * 4;
 
 struct Bars {
   uint64_t kv_full;
-  uint64_t v_ready;   // K and V' (fp16) rows stored in TMEM (256 P/dS threads)
+  uint64_t v_ready;   // V' (fp16) written over V in shared memory (128 threads of P/dS group 0)
   uint64_t qdo_full[NSTAGE];
   uint64_t qdo_empty[NSTAGE];
   uint64_t st_full;   // S^T, dP^T of the step ready (issuer A commit)
@@ -499,7 +492,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
-    mbar_init(&bars->v_ready, 256);
+    mbar_init(&bars->v_ready, 128);
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(&bars->qdo_full[s], 1);
       mbar_init(&bars->qdo_empty[s], 1);
@@ -577,13 +570,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // ================================================= issuer A: S^T, dP^T
       const uint32_t id_nn = idesc_bf16_f32(128, 128, false, false);    // S^T: K, Q bf16
       const uint32_t id_nn16 = idesc_fp16_f32(128, 128, false, false);  // dP''^T: V', dO' fp16
+      const uint64_t k_kmaj = sdesc_sw128(smem_u32(smem + SM_K), 16, 1024);
+      const uint64_t v_kmaj = sdesc_sw128(smem_u32(smem + SM_V), 16, 1024);
       const uint32_t q_addr = smem_u32(smem + SM_Q);
       const uint32_t do_addr = smem_u32(smem + SM_DO);
       bool ok = mbar_wait(&bars->kv_full, 0, ab, p.status, kTimeoutCode);
       for (int n = 0; ok && n < nsteps; ++n) {
         const int st = n % NSTAGE;
         if (!mbar_wait(&bars->qdo_full[st], (n / NSTAGE) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
-        // K and V' must be in TMEM before the first products
+        // V' (fp16) must be in place before the first dP''^T
         if (n == 0 && !mbar_wait(&bars->v_ready, 0, ab, p.status, kTimeoutCode)) { ok = false; break; }
         // the P/dS warps must have read the previous step's S^T and dP^T
         if (n > 0 && !mbar_wait(&bars->st_free, (n - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
@@ -591,13 +586,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_after_sync();
         const uint64_t q_kmaj = sdesc_sw128(q_addr + st * TILE_BYTES, 16, 1024);
         const uint64_t do_kmaj = sdesc_sw128(do_addr + st * TILE_BYTES, 16, 1024);
-        // A operands from TMEM (16 head dims = 8 packed columns per step)
 #pragma unroll
         for (int ks = 0; ks < HD / 16; ++ks)
-          mma_bf16_ts(tbase + C_S, tbase + C_KT + ks * 8, q_kmaj + 2 * ks, id_nn, ks > 0);
+          mma_bf16_ss(tbase + C_S, k_kmaj + 2 * ks, q_kmaj + 2 * ks, id_nn, ks > 0);
 #pragma unroll
         for (int ks = 0; ks < HD / 16; ++ks)
-          mma_bf16_ts(tbase + C_DP, tbase + C_VT + ks * 8, do_kmaj + 2 * ks, id_nn16, ks > 0);
+          mma_bf16_ss(tbase + C_DP, v_kmaj + 2 * ks, do_kmaj + 2 * ks, id_nn16, ks > 0);
         mma_commit(&bars->st_full);
         GQA_TRACE_EVENT(1, 3, n);
       }
@@ -638,8 +632,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         mma_commit(&bars->qdo_empty[st]);
         if (n > 0 && !mbar_wait(&bars->dq_free, (n - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
-        // dQ overwrites P'^T's columns: this step's dV must have read them
-        if (!mbar_wait(&bars->pt_free, n & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
         GQA_TRACE_EVENT(1, 5, n);
         tc_fence_after_sync();
 #pragma unroll
@@ -664,52 +656,44 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // this thread's key row of its group's 64-query half of a dS tile; chunk c
     // of 8 queries sits at (c ^ (r & 7)) (128-byte swizzle)
     uint8_t *ds_row0 = smem + SM_DS + wg * TILE_BYTES + r * 128;
-    // This thread's key row into TMEM for the CTA's life: group 0 stores
-    // V' = fp16(V 2^ev) (columns C_VT), group 1 the bf16 K row (C_KT); both
-    // take cv = 2^-ev from the V row (rows in shared memory: 16-byte chunk c
-    // at c ^ (r & 7); in TMEM: packed pair c of the row in column c).
+    // V' = fp16(V 2^ev) in place, one key row per thread: both groups read the
+    // row and take cv = 2^-ev, group 0 writes it back once every P/dS thread
+    // has read (a barrier every one of the 256 threads reaches, also on abort).
     float cv = 1.f;
     bool ok = mbar_wait_warp(&bars->kv_full, 0, ab, p.status, kTimeoutCode);
-    if (ok) {
-      const uint8_t *vrow = smem + SM_V + r * 128;
-      uint32_t vv[32];
+    {
+      uint8_t *vrow = smem + SM_V + r * 128;  // 16-byte chunk c at (c ^ (r & 7))
+      uint4 vv[8];
       float m = 0.f;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 w = *reinterpret_cast<const uint4 *>(vrow + ((c ^ (r & 7)) << 4));
-        vv[4 * c] = w.x;
-        vv[4 * c + 1] = w.y;
-        vv[4 * c + 2] = w.z;
-        vv[4 * c + 3] = w.w;
-      }
-#pragma unroll
-      for (int e = 0; e < 32; ++e)
-        m = fmaxf(m, fmaxf(fabsf(__uint_as_float(vv[e] << 16)),
-                           fabsf(__uint_as_float(vv[e] & 0xffff0000u))));
-      const int ev = row_exponent(m);
-      cv = exp2i(-ev);
-      if (wg == 0) {
-        const float sc = exp2i(ev);
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-          vv[e] = pack_f16x2(__uint_as_float(vv[e] << 16) * sc,
-                             __uint_as_float(vv[e] & 0xffff0000u) * sc);
-        tmem_st_32x32b_x32(tbase + lane_off + C_VT, vv);
-      } else {
-        const uint8_t *krow = smem + SM_K + r * 128;
+      if (ok) {
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const uint4 w = *reinterpret_cast<const uint4 *>(krow + ((c ^ (r & 7)) << 4));
-          vv[4 * c] = w.x;
-          vv[4 * c + 1] = w.y;
-          vv[4 * c + 2] = w.z;
-          vv[4 * c + 3] = w.w;
+          vv[c] = *reinterpret_cast<const uint4 *>(vrow + ((c ^ (r & 7)) << 4));
+          const uint32_t w4[4] = {vv[c].x, vv[c].y, vv[c].z, vv[c].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w4[e] << 16)),
+                               fabsf(__uint_as_float(w4[e] & 0xffff0000u))));
         }
-        tmem_st_32x32b_x32(tbase + lane_off + C_KT, vv);
       }
-      tmem_wait_st();
-      tc_fence_before_sync();
-      mbar_arrive(&bars->v_ready);
+      const int ev = row_exponent(m);
+      cv = exp2i(-ev);
+      ok = named_bar_and(2, 256, ok);
+      if (ok && wg == 0) {
+        const float sc = exp2i(ev);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t w4[4] = {vv[c].x, vv[c].y, vv[c].z, vv[c].w};
+          uint32_t h4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            h4[e] = pack_f16x2(__uint_as_float(w4[e] << 16) * sc,
+                               __uint_as_float(w4[e] & 0xffff0000u) * sc);
+          *reinterpret_cast<uint4 *>(vrow + ((c ^ (r & 7)) << 4)) = make_uint4(h4[0], h4[1], h4[2], h4[3]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars->v_ready);
+      }
     }
     for (int n = 0; ok && n < nsteps; ++n) {
       const int st = n % NSTAGE;
@@ -761,11 +745,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int q8 = 0; q8 < 4; ++q8)
         *reinterpret_cast<uint4 *>(ds_row + (((4 + q8) ^ (r & 7)) << 4)) =
             make_uint4(pd1[4 * q8], pd1[4 * q8 + 1], pd1[4 * q8 + 2], pd1[4 * q8 + 3]);
-      // the previous step's dV must be done with P'^T, and the drain with the
-      // previous dQ tile that shared its columns
+      // the previous step's dV must be done with P^T
       if (n > 0) {
         if (!mbar_wait_warp(&bars->pt_free, (n - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
-        if (!mbar_wait_warp(&bars->dq_free, (n - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
         tc_fence_after_sync();
       }
       if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 10, n);
