@@ -180,13 +180,16 @@ class ClockSampler:
 class Problem:
     """Device tensors of one workload and the calls of one step (through the C ABI)."""
 
-    def __init__(self, w, dev, seed, with_bwd, yarn=False, fp8=False):
+    def __init__(self, w, dev, seed, with_bwd, yarn=False, fp8=False, outliers=False):
         import torch
         import causal_grouped_query_gqa_b300 as gq
         from causal_grouped_query_gqa_b300.inputs import make_inputs
         self.w, self.dev, self.with_bwd = w, dev, with_bwd
         B, H, G, S, d = w.B, w.H, w.G, w.S, w.d
         self.host = make_inputs(B, H, G, S, seed=seed, with_grad=True)
+        if outliers:  # rows 0..31 of every 128-row block 8x larger: a quarter of the warps
+            # then exceed the score bound and take the exact step (8x is exact in bf16)
+            self.host[0][:, :, torch.arange(S) % 128 < 32] *= 8
         self.ins = tuple(t.to(dev) for t in self.host)
         q = self.ins[0]
         self.outs = (torch.empty_like(q), torch.empty((B, H, S), dtype=torch.float32, device=dev),
@@ -213,7 +216,6 @@ class Problem:
         # the YaRN forward (rotary embeddings on q and k) instead of the plain one
         self.yarn = yarn
         if yarn:
-            self.score_bound = False
             self.yws_bytes = gq.gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d)
             self.yws = torch.empty(max(self.yws_bytes, 16), dtype=torch.uint8, device=dev)
 
@@ -233,7 +235,7 @@ class Problem:
             rc = gq.gqa_attn_fwd_yarn(q_, k_, v_, o_, lse_, B, H, G, S, d, w.causal, w.window,
                                       w.n_sink, w.scale, y["rope_base"], y["rope_factor"],
                                       y["rope_orig_ctx"], y["rope_alpha"], y["rope_beta"],
-                                      self.yws, self.yws_bytes, strm)
+                                      bound, self.yws, self.yws_bytes, strm)
         elif bound:
             rc = gq.gqa_attn_fwd_ws(q_, k_, v_, o_, lse_, B, H, G, S, d, w.causal, w.window,
                                     w.n_sink, w.scale, self.fws, self.fws_bytes, strm)
@@ -251,7 +253,8 @@ class Problem:
 
     def launches_per_step(self, score_bound=None):
         bound = self.score_bound if score_bound is None else score_bound
-        return (3 if self.yarn else (2 if bound and not self.fp8 else 1)) + (4 if self.with_bwd else 0)
+        fwd_launches = 1 + (1 if bound and not self.fp8 else 0) + (2 if self.yarn else 0)
+        return fwd_launches + (4 if self.with_bwd else 0)
 
 
 def timed_steps(pb, steps, warmup, flush, stream, world, score_bound=None, clocks=False):
@@ -420,14 +423,15 @@ def run_ours(args, w, rank, world, local_rank):
         for name, step in EXTRA_WORKLOADS:
             ew = WORKLOADS[name]
             epb = Problem(ew, dev, seed=0, with_bwd=(step == "fwd+bwd"), yarn=(step == "fwd_yarn"),
-                          fp8=(step == "fwd_fp8"))
+                          fp8=(step == "fwd_fp8"), outliers=(step == "fwd_outliers"))
             e_steps = max(3, min(args.steps, 10))
             e_ms, e_kernel, e_clk = timed_steps(epb, e_steps, 3, flush, stream, 1, clocks=True)
             res = summarize(ew, epb, e_kernel, e_ms, e_steps, 1, peaks, name)
             res.update({"step": step, "steps": e_steps, "clocks": e_clk,
                         "config": {"B": ew.B, "H": ew.H, "G": ew.G, "S": ew.S,
                                    "window": ew.window, "n_sink": ew.n_sink}})
-            extras[name + {"fwd_yarn": "+yarn", "fwd_fp8": "+fp8"}.get(step, "")] = res
+            extras[name + {"fwd_yarn": "+yarn", "fwd_fp8": "+fp8",
+                           "fwd_outliers": "+outlier_rows"}.get(step, "")] = res
             del epb
             torch.cuda.empty_cache()
         out["extra_workloads"] = extras
@@ -442,6 +446,7 @@ EXTRA_WORKLOADS = [
     ("bwd_b4_h32_g8_s4096", "fwd+bwd"),
     ("wide_b1_h128_g16_s8192", "fwd_yarn"),   # YaRN rotary forward (table + key rotation + forward)
     ("wide_b1_h128_g16_s8192", "fwd_fp8"),    # E4M3 queries and keys (quantised before timing)
+    ("wide_b1_h128_g16_s8192", "fwd_outliers"),  # score bound with a quarter of the warps exact
 ]
 
 

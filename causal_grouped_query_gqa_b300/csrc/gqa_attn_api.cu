@@ -322,13 +322,15 @@ int gqa_attn_quantize_e4m3(const void *x, void *out, long long n, float inv_scal
 size_t gqa_attn_fwd_yarn_workspace_size(int B, int H, int G, int S, int d) {
   if (check_common(B, H, G, S, d, 1, 0, 0, 1.f) != GQA_OK) return 0;
   const size_t krot = static_cast<size_t>(B) * G * S * 64 * 2;  // a multiple of 16
-  return krot + static_cast<size_t>(S) * gqa::rope::kPairs * sizeof(float2);
+  const size_t tab = static_cast<size_t>(S) * gqa::rope::kPairs * sizeof(float2);
+  return krot + tab + static_cast<size_t>(B) * G * gqa::fwd::kKnParts * sizeof(float);
 }
 
 int gqa_attn_fwd_yarn(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                       int H, int G, int S, int d, int causal, int window, int n_sink, float scale,
                       float rope_base, float rope_factor, int rope_orig_ctx, float rope_alpha,
-                      float rope_beta, void *workspace, size_t workspace_bytes, void *stream) {
+                      float rope_beta, int score_bound, void *workspace, size_t workspace_bytes,
+                      void *stream) {
   int rc = check_common(B, H, G, S, d, causal, window, n_sink, scale);
   if (rc != GQA_OK) return rc;
   gqa::rope::Freqs f;
@@ -364,8 +366,12 @@ int gqa_attn_fwd_yarn(const void *q, const void *k, const void *v, void *o, floa
     gqa::timing_end(GQA_KERNEL_ROPE, st);
     if (gqa::cuda_failed(cudaGetLastError(), "launch of the key rotation kernel")) return GQA_ERR_CUDA;
   }
+  float *kn2 = nullptr;
+  if (score_bound)  // the key-norm record of the rotated keys, after the table
+    kn2 = reinterpret_cast<float *>(reinterpret_cast<char *>(tab) +
+                                    static_cast<size_t>(S) * gqa::rope::kPairs * sizeof(float2));
   return launch_forward(q, k_rot, v, o, lse, B, H, G, S, causal, window, n_sink,
-                        static_cast<float>(tempered), nullptr, tab, st);
+                        static_cast<float>(tempered), kn2, tab, st);
 }
 
 size_t gqa_attn_bwd_workspace_size(int B, int H, int G, int S, int d) {

@@ -131,20 +131,23 @@ GQA_API int gqa_attn_fwd_ws(const void *q, const void *k, const void *v, void *o
  * and errors as gqa_attn_fwd, plus GQA_ERR_ROPE when rope_base <= 1,
  * rope_factor < 1, rope_orig_ctx <= 0 or not 0 <= rope_alpha < rope_beta, and
  * GQA_ERR_NULL / GQA_ERR_WORKSPACE for a missing or short workspace.
+ * score_bound: 0 takes the online maximum on every tile as gqa_attn_fwd does;
+ * non-zero takes the score bound of gqa_attn_fwd_ws on the rotated queries and
+ * keys (one more launch: the key-norm pre-pass on the rotated keys; same input
+ * range note as gqa_attn_fwd_ws).
  * workspace: device memory of at least gqa_attn_fwd_yarn_workspace_size()
  * bytes, 16-byte aligned, owned by the caller and not used by any other call
- * running at the same time: the rotated keys [B][G][S][d] bf16 and a
- * [S][d/2] table of (cos, sin) fp32 pairs, both written by this call (three
- * launches: table, key rotation, forward; the query tiles are rotated inside
- * the forward kernel).  The rotary forward takes the online maximum on every
- * tile (no score bound).
+ * running at the same time: the rotated keys [B][G][S][d] bf16, a [S][d/2]
+ * table of (cos, sin) fp32 pairs and the key-norm record (B * G * 128 bytes),
+ * written by this call (table, key rotation, [key norms,] forward; the query
+ * tiles are rotated inside the forward kernel).
  */
 GQA_API size_t gqa_attn_fwd_yarn_workspace_size(int B, int H, int G, int S, int d);
 GQA_API int gqa_attn_fwd_yarn(const void *q, const void *k, const void *v, void *o, float *lse,
                       int B, int H, int G, int S, int d,
                       int causal, int window, int n_sink, float scale,
                       float rope_base, float rope_factor, int rope_orig_ctx,
-                      float rope_alpha, float rope_beta,
+                      float rope_alpha, float rope_beta, int score_bound,
                       void *workspace, size_t workspace_bytes, void *stream);
 
 /*

@@ -96,12 +96,12 @@ def _bwd(**kw):
 def _fwd_yarn(**kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=4, G=2, S=128, d=64,
              causal=1, window=0, n_sink=0, scale=0.125, base=10000.0, factor=32.0, L=6400,
-             alpha=1.0, beta=32.0, ws=FAKE, wsb=1 << 24, stream=0)
+             alpha=1.0, beta=32.0, sb=1, ws=FAKE, wsb=1 << 24, stream=0)
     a.update(kw)
     return gq.gqa_attn_fwd_yarn(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["G"],
                                 a["S"], a["d"], a["causal"], a["window"], a["n_sink"], a["scale"],
-                                a["base"], a["factor"], a["L"], a["alpha"], a["beta"], a["ws"],
-                                a["wsb"], a["stream"])
+                                a["base"], a["factor"], a["L"], a["alpha"], a["beta"], a["sb"],
+                                a["ws"], a["wsb"], a["stream"])
 
 
 def _fwd_fp8(**kw):
@@ -155,8 +155,8 @@ def test_fwd_yarn_specific_errors(lib):
     assert _fwd_yarn(ws=None) == gq.GQA_ERR_NULL
     assert _fwd_yarn(ws=FAKE + 4) == gq.GQA_ERR_ALIGN
     need = gq.gqa_attn_fwd_yarn_workspace_size(1, 4, 2, 128, 64)
-    # rotated keys (bf16) and the (cos, sin) table
-    assert need == 1 * 2 * 128 * 64 * 2 + 128 * 32 * 8
+    # rotated keys (bf16), the (cos, sin) table and the key-norm record
+    assert need == 1 * 2 * 128 * 64 * 2 + 128 * 32 * 8 + 1 * 2 * 128
     assert _fwd_yarn(wsb=need - 1) == gq.GQA_ERR_WORKSPACE
     assert gq.gqa_attn_fwd_yarn_workspace_size(1, 3, 2, 128, 64) == 0
 

@@ -59,3 +59,50 @@ def test_graph_replay_matches_eager(fwd_ws):
         assert torch.equal(got[0], ro) and torch.equal(got[1], rl)
         assert torch.equal(got[3], rk) and torch.equal(got[4], rv)
         assert (got[2].float() - rq.float()).abs().max().item() <= 2e-2
+
+
+@pytest.mark.parametrize("kind", ["yarn", "fp8"])
+def test_graph_replay_yarn_and_fp8(kind):
+    """The rotary forward (table, key rotation, forward) and the fp8 forward
+    captured and replayed with new inputs: bit-identical to eager calls."""
+    B, H, G, S, d, scale = 1, 8, 2, 1000, 64, 0.125
+    q, k, v = (t.cuda() for t in make_inputs(B, H, G, S, seed=31))
+    q8 = torch.empty(q.shape, dtype=torch.uint8, device="cuda")
+    k8 = torch.empty(k.shape, dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device="cuda")
+    yws = torch.empty(gq.gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d), dtype=torch.uint8,
+                      device="cuda")
+
+    def forward(o_, lse_, stream):
+        if kind == "yarn":
+            return gq.gqa_attn_fwd_yarn(q, k, v, o_, lse_, B, H, G, S, d, 1, 0, 0, scale, 10000.0,
+                                        32.0, 6400, 1.0, 32.0, 1, yws, yws.numel(), stream)
+        return gq.gqa_attn_fwd_fp8(q8, k8, v, o_, lse_, B, H, G, S, d, 1, 0, 0, scale, 1 / 64,
+                                   1 / 64, stream)
+
+    def step(stream):
+        if kind == "fp8":
+            assert gq.gqa_attn_quantize_e4m3(q, q8, q.numel(), 64.0, stream) == gq.GQA_OK
+            assert gq.gqa_attn_quantize_e4m3(k, k8, k.numel(), 64.0, stream) == gq.GQA_OK
+        assert forward(o, lse, stream) == gq.GQA_OK
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        step(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step(s)
+    for seed in (32, 33):
+        new = make_inputs(B, H, G, S, seed=seed)
+        for dst, src in zip((q, k, v), new):
+            dst.copy_(src)
+        g.replay()
+        torch.cuda.synchronize()
+        assert gq.gqa_attn_last_device_status() == gq.GQA_OK
+        got = (o.clone(), lse.clone())
+        ro, rl = torch.empty_like(o), torch.empty_like(lse)
+        assert forward(ro, rl, None) == gq.GQA_OK
+        torch.cuda.synchronize()
+        assert torch.equal(got[0], ro) and torch.equal(got[1], rl)

@@ -40,6 +40,11 @@ def checked():
     lib.gqa_attn_bwd_workspace_size.argtypes = [i, i, i, i, i]
     lib.gqa_attn_bwd_workspace_size.restype = sz
     lib.gqa_attn_last_device_status.argtypes = [vp]
+    lib.gqa_attn_fwd_yarn.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f,
+                                      f, f, i, f, f, i, vp, sz, vp]
+    lib.gqa_attn_fwd_yarn_workspace_size.argtypes = [i, i, i, i, i]
+    lib.gqa_attn_fwd_yarn_workspace_size.restype = sz
+    lib.gqa_attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, f, f, vp]
     return lib
 
 
@@ -67,3 +72,32 @@ def test_checked_build_runs_clean(checked, B, H, G, S, causal, window, n_sink):
     check_close("dQ", to64(dq), rq)
     check_close("dK", to64(dk), rk)
     check_close("dV", to64(dv), rv)
+
+
+@pytest.mark.parametrize("B,H,G,S,causal,window,n_sink", [SHAPES[1], SHAPES[5], SHAPES[7]])
+def test_checked_build_yarn_and_fp8(checked, B, H, G, S, causal, window, n_sink):
+    """The rotary and fp8 forwards under the index checks: clean, and equal to
+    the oracle (rotated-and-rounded q, k; decoded E4M3 q, k)."""
+    d, scale = 64, 0.125
+    q, k, v = make_inputs(B, H, G, S, seed=S + 1)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o = torch.empty_like(qd)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device="cuda")
+    ws = torch.empty(checked.gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d), dtype=torch.uint8,
+                     device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+    p = lambda t: t.data_ptr()
+    assert checked.gqa_attn_fwd_yarn(p(qd), p(kd), p(vd), p(o), p(lse), B, H, G, S, d, causal,
+                                     window, n_sink, scale, 10000.0, 32.0, 6400, 1.0, 32.0, 1,
+                                     p(ws), ws.numel(), st) == gq.GQA_OK
+    assert checked.gqa_attn_last_device_status(st) == gq.GQA_OK
+    kw = dict(causal=bool(causal), window=window, n_sink=n_sink, scale=scale)
+    ro, _ = oracle.attn_fwd_yarn(to64(q), to64(k), to64(v), **kw)
+    check_close("O (YaRN)", to64(o), ro)
+    q8 = (q.float() * 64).to(torch.float8_e4m3fn).view(torch.uint8)
+    k8 = (k.float() * 64).to(torch.float8_e4m3fn).view(torch.uint8)
+    assert checked.gqa_attn_fwd_fp8(p(q8.cuda()), p(k8.cuda()), p(vd), p(o), p(lse), B, H, G, S, d,
+                                    causal, window, n_sink, scale, 1 / 64, 1 / 64, st) == gq.GQA_OK
+    assert checked.gqa_attn_last_device_status(st) == gq.GQA_OK
+    ro, _ = oracle.attn_fwd_fp8(q8.numpy(), k8.numpy(), to64(v), 1 / 64, 1 / 64, **kw)
+    check_close("O (fp8)", to64(o), ro)

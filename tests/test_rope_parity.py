@@ -19,10 +19,11 @@ pytestmark = pytest.mark.gpu
 DEFAULT = dict(base=10000.0, factor=32.0, orig_ctx=6400, alpha=1.0, beta=32.0)
 
 
-def _gpu(q, k, v, rope, **mask):
+def _gpu(q, k, v, rope, score_bound=None, **mask):
     o, lse = gq.fwd_yarn(q.cuda(), k.cuda(), v.cuda(), rope_base=rope["base"],
                          rope_factor=rope["factor"], rope_orig_ctx=rope["orig_ctx"],
-                         rope_alpha=rope["alpha"], rope_beta=rope["beta"], **mask)
+                         rope_alpha=rope["alpha"], rope_beta=rope["beta"],
+                         score_bound=score_bound, **mask)
     torch.cuda.synchronize()
     assert gq.gqa_attn_last_device_status() == gq.GQA_OK
     return o, lse
@@ -36,10 +37,11 @@ def _gpu(q, k, v, rope, **mask):
     (1, 8, 1, 520, True, 0, 0),
     (4, 6, 2, 2048, True, 0, 0),      # more units than SMs: rotations carried across units
 ])
-def test_yarn_forward(B, H, G, S, causal, window, n_sink):
+@pytest.mark.parametrize("score_bound", [False, True], ids=["plain", "bound"])
+def test_yarn_forward(B, H, G, S, causal, window, n_sink, score_bound):
     q, k, v = make_inputs(B, H, G, S, seed=S)
     mask = dict(causal=causal, window=window, n_sink=n_sink)
-    o, lse = _gpu(q, k, v, DEFAULT, **mask)
+    o, lse = _gpu(q, k, v, DEFAULT, score_bound=score_bound, **mask)
     ro, rl = oracle.attn_fwd_yarn(to64(q), to64(k), to64(v), **DEFAULT, **mask)
     check_close("O", to64(o), ro)
     check_close("LSE", to64(lse), rl, max_abs=LSE_ABS, mean_abs=None, bf16_out=False)
@@ -76,11 +78,12 @@ def test_rotated_keys_in_workspace():
     assert (diff > 0).mean() <= 1e-3
 
 
-def test_wide_workload_group():
+@pytest.mark.parametrize("score_bound", [False, True], ids=["plain", "bound"])
+def test_wide_workload_group(score_bound):
     """B1 H128 G16 S8192 with YaRN: the last kv group whole (8 heads x 8192 rows)."""
     w = WORKLOADS["wide_b1_h128_g16_s8192"]
     q, k, v = make_inputs(w.B, w.H, w.G, w.S, seed=0)
-    o, lse = _gpu(q, k, v, DEFAULT)
+    o, lse = _gpu(q, k, v, DEFAULT, score_bound=score_bound)
     R, g = w.H // w.G, w.G - 1
     hs = slice(g * R, (g + 1) * R)
     ro, rl = oracle.attn_fwd_yarn(to64(q[:, hs]), to64(k[:, g:g + 1]), to64(v[:, g:g + 1]),
