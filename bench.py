@@ -423,15 +423,17 @@ def run_ours(args, w, rank, world, local_rank):
         for name, step in EXTRA_WORKLOADS:
             ew = WORKLOADS[name]
             epb = Problem(ew, dev, seed=0, with_bwd=(step == "fwd+bwd"), yarn=(step == "fwd_yarn"),
-                          fp8=(step == "fwd_fp8"), outliers=(step == "fwd_outliers"))
+                          fp8=(step == "fwd_fp8"), outliers=step.startswith("fwd_outliers"))
+            if step == "fwd_outliers_plain":
+                epb.score_bound = False
             e_steps = max(3, min(args.steps, 10))
             e_ms, e_kernel, e_clk = timed_steps(epb, e_steps, 3, flush, stream, 1, clocks=True)
             res = summarize(ew, epb, e_kernel, e_ms, e_steps, 1, peaks, name)
             res.update({"step": step, "steps": e_steps, "clocks": e_clk,
                         "config": {"B": ew.B, "H": ew.H, "G": ew.G, "S": ew.S,
                                    "window": ew.window, "n_sink": ew.n_sink}})
-            extras[name + {"fwd_yarn": "+yarn", "fwd_fp8": "+fp8",
-                           "fwd_outliers": "+outlier_rows"}.get(step, "")] = res
+            extras[name + {"fwd_yarn": "+yarn", "fwd_fp8": "+fp8", "fwd_outliers": "+outlier_rows",
+                           "fwd_outliers_plain": "+outlier_rows_plain"}.get(step, "")] = res
             del epb
             torch.cuda.empty_cache()
         out["extra_workloads"] = extras
@@ -447,6 +449,7 @@ EXTRA_WORKLOADS = [
     ("wide_b1_h128_g16_s8192", "fwd_yarn"),   # YaRN rotary forward (table + key rotation + forward)
     ("wide_b1_h128_g16_s8192", "fwd_fp8"),    # E4M3 queries and keys (quantised before timing)
     ("wide_b1_h128_g16_s8192", "fwd_outliers"),  # score bound with a quarter of the warps exact
+    ("wide_b1_h128_g16_s8192", "fwd_outliers_plain"),  # the same input through gqa_attn_fwd
 ]
 
 

@@ -74,7 +74,7 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr float kRescaleThreshold = 8.0f;
 // Score bound (gqa_attn_fwd_ws only): |s_ij| * scale * log2(e) <= U_i =
 // |q_i| * max_j |k_j| * scale * log2(e) (Cauchy-Schwarz), with max_j |k_j|^2 over
-// the kv head from fwd_knorm_kernel.  A warp whose rows all have U_i <=
+// the kv head from fwd_knorm_kernel.  A head whose 128 rows all have U_i <=
 // kBoundMax runs the whole unit against the fixed reference m_i = U_i -
 // kFastSlack and takes no row maxima: every term 2^(s * sl2 - m_i) lies in
 // [2^(kFastSlack - 2 U_i), 2^kFastSlack], so none overflows and the largest of
@@ -118,6 +118,8 @@ struct Bars {
                        // section (arrived by the other head's 128 threads)
   uint64_t q_ready[2]; // rotary embedding only: head t's Q tile rotated in place
                        // (128 softmax threads of head t, once per unit)
+  uint64_t vote_bar[2];  // score bound: head t's four warps have cast their vote
+  int vote[2][2];        // score bound: AND of head t's warp votes, two alternating slots
   uint32_t tmem_base;
   AbortState abort;
 };
@@ -295,6 +297,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&bars->turn[t], 128);
       mbar_init(&bars->pv_done[t], 1);
       mbar_init(&bars->q_ready[t], 128);
+      mbar_init(&bars->vote_bar[t], 128);
+      bars->vote[t][0] = 1;
+      bars->vote[t][1] = 1;
     }
     mbar_init(&bars->qk_done, 1);
     bars->abort.flag = 0;
@@ -512,6 +517,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     int uo = 0;  // units of this head: O-full / O-empty phases
     int tt = 0;  // tiles of two-head units: ping-pong phases (same count in both heads)
     int uq = 0;  // Q tiles of this head (all units): Q-full phases and record slots
+    int uv = 0;  // score-bound votes of this head: vote phases and slots
     bool ok = true;
     for (int k = 0; ok; ++k) {
       const int u = unit_at(k, p);
@@ -540,9 +546,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       float m_run = -CUDART_INF_F;  // running max of scaled scores, base-2 units
       float l_run = 0.f;            // running sum of 2^(s - m_run)
-      // Score bound (kBoundMax): decided per warp before the unit's first tile.
-      // Units of one key tile keep the exact step: their Q may be reloaded as
-      // soon as their only Q K^T is done, before this read could happen.
+      // Score bound (kBoundMax): decided for the head's 128 rows together
+      // (all four warps) before the unit's first tile: a head whose warps mixed
+      // the two steps measured about 50 % slower than one on the exact step
+      // throughout.  Units of one key tile keep the exact step: their Q may be
+      // reloaded as soon as their only Q K^T is done, before this read could
+      // happen.
       bool fast = false;
       if (p.kn2 != nullptr && n >= 2) {
         // Q and the record landed with q_full[t] (phase qk); they stay until
@@ -550,7 +559,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // waits for this thread's release of S of tile n - 2 >= 0.
         if (!mbar_wait(&bars->q_full[t], qk & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
         const float bound = score_bound(smem + SM_Q + t * TILE_BYTES + r * 128, r, &bars->kn[t][qk & 1][0], sl2);
-        fast = __all_sync(0xffffffffu, bound <= kBoundMax);
+        // each warp ANDs its vote into the slot, then the 128 threads meet on an
+        // mbarrier (a bounded wait, so an abort cannot leave a thread behind)
+        const int slot = uv & 1;
+        if (!__all_sync(0xffffffffu, bound <= kBoundMax) && lane == 0) atomicAnd(&bars->vote[t][slot], 0);
+        mbar_arrive(&bars->vote_bar[t]);
+        if (!mbar_wait(&bars->vote_bar[t], uv & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        ++uv;
+        fast = *reinterpret_cast<volatile int *>(&bars->vote[t][slot]) != 0;
+        // every thread of the head has read the other slot (its previous vote)
+        // before arriving here: reset it for the head's next vote
+        if (r == 0) bars->vote[t][slot ^ 1] = 1;
         if (fast) m_run = bound - kFastSlack;
       }
       // One key tile of the unit.  kFast: the warp runs against the score

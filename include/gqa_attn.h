@@ -92,10 +92,10 @@ GQA_API size_t gqa_attn_fwd_workspace_size(int B, int H, int G, int S, int d);
  * kernel writes into `workspace` the largest squared norm of each kv head's key
  * rows (32 partial maxima per kv head).  Every scaled score of query row i is
  * at most U_i = |q_i| * max_j |k_j| * scale * log2(e) in magnitude
- * (Cauchy-Schwarz, base-2 units); a warp whose 32 rows all have U_i <= 64
- * computes its whole unit of key tiles against the fixed reference U_i - 32
- * instead of a running row maximum (every term 2^(s - reference) then lies in
- * [2^-96, 2^32]), and rows with larger bounds keep the online maximum of
+ * (Cauchy-Schwarz, base-2 units); a query head whose 128 rows of a work unit
+ * all have U_i <= 64 computes the unit's key tiles against the fixed reference
+ * U_i - 32 instead of a running row maximum (every term 2^(s - reference) then
+ * lies in [2^-96, 2^32]), and heads with larger bounds keep the online maximum of
  * "SnapKitty Transformer 8B", section "FlashAttention Inference".  The bound is
  * this library's.
  * Input range: the fp32 sums of O then hold up to S * 2^32 * max|v|, so the

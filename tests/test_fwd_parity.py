@@ -160,11 +160,12 @@ def test_repeat_is_deterministic():
 
 
 # ---------------------------------------------------------------- score bound
-# gq.fwd runs gqa_attn_fwd_ws: a key-norm pre-pass, then the forward kernel in
-# which a warp whose rows' score bounds U_i = |q_i| max_j |k_j| scale log2(e) are
-# all <= 64 runs its unit against the fixed reference U_i - 32 without row
-# maxima.  The tests above therefore cover that path on their inputs; these pin
-# the pre-pass, the plain entry point and the warps that keep the exact step.
+# gqa_attn_fwd_ws (gq.fwd with score_bound=True, and gq.fwd's default on large
+# problems): a key-norm pre-pass, then the forward kernel in which a query head
+# whose 128 rows' score bounds U_i = |q_i| max_j |k_j| scale log2(e) are all
+# <= 64 runs its unit against the fixed reference U_i - 32 without row maxima.
+# The tests above cover that path on their inputs (the "bound" cases); these pin
+# the pre-pass, the plain entry point and the heads that keep the exact step.
 
 def _oracle_check(q, k, v, o, lse, **mask):
     ro, rl = oracle.attn_fwd(to64(q), to64(k), to64(v), **mask)
@@ -211,8 +212,8 @@ def test_plain_entry_point(window, n_sink):
 
 def test_score_bound_mixed_warps():
     """Rows 0..31 of every 128-row block have 8x larger queries (bound > 64):
-    those warps keep the exact step while the other warps of the same heads run
-    against the bound's reference."""
+    the other warps of the same heads would qualify, and the head's vote sends
+    all four warps down the exact step together."""
     B, H, G, S = 1, 4, 2, 1100
     q, k, v = make_inputs(B, H, G, S, seed=11)
     q[:, :, torch.arange(S) % 128 < 32] *= 8  # exact in bf16
