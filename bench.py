@@ -40,7 +40,7 @@ if ROOT not in sys.path:
 
 METRIC = "attention fwd/bwd TFLOPS (causal FLOPs) and % of B300 BF16 tensor peak"
 KERNEL_NAMES = ["gqa_fwd_kernel", "bwd_prep_kernel", "bwd_main_kernel", "bwd_dq_convert_kernel",
-                "fwd_knorm_kernel", "rope_table_and_key_rotation"]
+                "fwd_knorm_kernel", "rope_table_and_rotation"]
 N_KERNELS = len(KERNEL_NAMES)
 L2_FLUSH_BYTES = 1 << 30
 
@@ -346,7 +346,8 @@ def summarize(w, pb, kernel_ms, total_ms, steps, world, peaks, workload):
         out["fwd_hbm"] = {"achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                           "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": fb,
                           "kernel": "gqa_fwd_kernel"}
-    for kid, nbytes in ((4, knorm_bytes(w)), (1, prep_bytes(w)), (3, convert_bytes(w))):
+    for kid, nbytes in ((4, knorm_bytes(w)), (1, prep_bytes(w)), (3, convert_bytes(w)),
+                       (5, rope_bytes(w))):
         if avg[kid] > 0:
             gbs = nbytes / (avg[kid] * 1e-3) / 1e9
             out.setdefault("hbm_kernels", {})[KERNEL_NAMES[kid]] = {
@@ -446,7 +447,7 @@ EXTRA_WORKLOADS = [
     ("gqa_b2_h32_g8_s2048", "fwd"),
     ("window_b1_h128_g16_s32768_w4096_sink128", "fwd"),
     ("bwd_b4_h32_g8_s4096", "fwd+bwd"),
-    ("wide_b1_h128_g16_s8192", "fwd_yarn"),   # YaRN rotary forward (table + key rotation + forward)
+    ("wide_b1_h128_g16_s8192", "fwd_yarn"),   # YaRN rotary forward (table, q and k rotation, forward)
     ("wide_b1_h128_g16_s8192", "fwd_fp8"),    # E4M3 queries and keys (quantised before timing)
     ("wide_b1_h128_g16_s8192", "fwd_outliers"),  # score bound with a quarter of the warps exact
     ("wide_b1_h128_g16_s8192", "fwd_outliers_plain"),  # the same input through gqa_attn_fwd
@@ -456,6 +457,12 @@ EXTRA_WORKLOADS = [
 def knorm_bytes(w):
     """Key-norm pre-pass: reads K, writes one 128-byte record per kv head."""
     return 2 * w.d * w.S * w.B * w.G + 128 * w.B * w.G
+
+
+def rope_bytes(w):
+    """Rotary pre-pass: writes the (cos, sin) table ([S][32] float2), reads q and
+    k (bf16) and writes their rotations (bf16)."""
+    return 8 * 32 * w.S + 2 * 2 * w.d * w.S * w.B * (w.H + w.G)
 
 
 def prep_bytes(w):

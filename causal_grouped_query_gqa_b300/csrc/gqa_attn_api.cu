@@ -17,6 +17,7 @@
 #include "bwd_kernels.cuh"
 #include "fwd_kernel.cuh"
 #include "quantize_kernel.cuh"
+#include "rope_kernels.cuh"
 #include "selftest_kernel.cuh"
 
 namespace {
@@ -67,8 +68,7 @@ int device_state(DeviceState **out) {
             cudaGetSymbolAddress(reinterpret_cast<void **>(&st.status), g_device_status),
             "cudaGetSymbolAddress(device status word)"))
       return GQA_ERR_CUDA;
-    for (auto kern : {gqa::fwd::gqa_fwd_kernel<false, false>, gqa::fwd::gqa_fwd_kernel<true, false>,
-                      gqa::fwd::gqa_fwd_kernel<false, true>}) {
+    for (auto kern : {gqa::fwd::gqa_fwd_kernel<false>, gqa::fwd::gqa_fwd_kernel<true>}) {
       if (gqa::cuda_failed(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                 gqa::fwd::SMEM_BYTES),
                            "cudaFuncSetAttribute(forward shared memory)"))
@@ -183,12 +183,11 @@ const char *gqa_attn_strerror(int status) {
 namespace {
 
 // The forward launch shared by the entry points; kn2 (the score-bound record
-// that fwd_knorm_kernel writes first, on the same stream) may be null, and so
-// may rope_tab (the rotary table; k is then already rotated).  fp8: q and k
+// that fwd_knorm_kernel writes first, on the same stream) may be null.  fp8: q and k
 // are E4M3 bytes and `scale` already carries their two dequantisation scales.
 int launch_forward(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
                    int G, int S, int causal, int window, int n_sink, float scale, float *kn2,
-                   const float2 *rope_tab, cudaStream_t st, bool fp8 = false) {
+                   cudaStream_t st, bool fp8 = false) {
   DeviceState *ds = nullptr;
   int rc = device_state(&ds);
   if (rc != GQA_OK) return rc;
@@ -218,7 +217,6 @@ int launch_forward(const void *q, const void *k, const void *v, void *o, float *
   p.n_qblocks = (S + BM - 1) / BM;
   p.n_pairs = (p.R + 1) / 2;
   p.kn2 = kn2;
-  p.rope_tab = rope_tab;
   p.o = static_cast<__nv_bfloat16 *>(o);
   p.lse = lse;
   p.status = ds->status;
@@ -240,11 +238,9 @@ int launch_forward(const void *q, const void *k, const void *v, void *o, float *
   }
   gqa::timing_begin(GQA_KERNEL_FWD, st);
   if (fp8)
-    gqa_fwd_kernel<false, true><<<static_cast<unsigned>(grid), NTHREADS, SMEM_BYTES, st>>>(tq, tk, tv, p);
-  else if (rope_tab)
-    gqa_fwd_kernel<true, false><<<static_cast<unsigned>(grid), NTHREADS, SMEM_BYTES, st>>>(tq, tk, tv, p);
+    gqa_fwd_kernel<true><<<static_cast<unsigned>(grid), NTHREADS, SMEM_BYTES, st>>>(tq, tk, tv, p);
   else
-    gqa_fwd_kernel<false, false><<<static_cast<unsigned>(grid), NTHREADS, SMEM_BYTES, st>>>(tq, tk, tv, p);
+    gqa_fwd_kernel<false><<<static_cast<unsigned>(grid), NTHREADS, SMEM_BYTES, st>>>(tq, tk, tv, p);
   gqa::timing_end(GQA_KERNEL_FWD, st);
   return gqa::cuda_failed(cudaGetLastError(), "launch of the forward kernel") ? GQA_ERR_CUDA
                                                                                : GQA_OK;
@@ -261,7 +257,7 @@ int gqa_attn_fwd(const void *q, const void *k, const void *v, void *o, float *ls
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return GQA_ERR_ALIGN;
   return launch_forward(q, k, v, o, lse, B, H, G, S, causal, window, n_sink, scale, nullptr,
-                        nullptr, static_cast<cudaStream_t>(stream));
+                        static_cast<cudaStream_t>(stream));
 }
 
 size_t gqa_attn_fwd_workspace_size(int B, int H, int G, int S, int d) {
@@ -280,7 +276,7 @@ int gqa_attn_fwd_ws(const void *q, const void *k, const void *v, void *o, float 
     return GQA_ERR_ALIGN;
   if (workspace_bytes < gqa_attn_fwd_workspace_size(B, H, G, S, d)) return GQA_ERR_WORKSPACE;
   return launch_forward(q, k, v, o, lse, B, H, G, S, causal, window, n_sink, scale,
-                        static_cast<float *>(workspace), nullptr, static_cast<cudaStream_t>(stream));
+                        static_cast<float *>(workspace), static_cast<cudaStream_t>(stream));
 }
 
 int gqa_attn_fwd_fp8(const void *q8, const void *k8, const void *v, void *o, float *lse, int B,
@@ -296,7 +292,7 @@ int gqa_attn_fwd_fp8(const void *q8, const void *k8, const void *v, void *o, flo
   if (!aligned16(q8) || !aligned16(k8) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return GQA_ERR_ALIGN;
   return launch_forward(q8, k8, v, o, lse, B, H, G, S, causal, window, n_sink,
-                        static_cast<float>(folded), nullptr, nullptr,
+                        static_cast<float>(folded), nullptr,
                         static_cast<cudaStream_t>(stream), true);
 }
 
@@ -321,9 +317,10 @@ int gqa_attn_quantize_e4m3(const void *x, void *out, long long n, float inv_scal
 
 size_t gqa_attn_fwd_yarn_workspace_size(int B, int H, int G, int S, int d) {
   if (check_common(B, H, G, S, d, 1, 0, 0, 1.f) != GQA_OK) return 0;
-  const size_t krot = static_cast<size_t>(B) * G * S * 64 * 2;  // a multiple of 16
+  const size_t qrot = static_cast<size_t>(B) * H * S * 64 * 2;  // multiples of 16
+  const size_t krot = static_cast<size_t>(B) * G * S * 64 * 2;
   const size_t tab = static_cast<size_t>(S) * gqa::rope::kPairs * sizeof(float2);
-  return krot + tab + static_cast<size_t>(B) * G * gqa::fwd::kKnParts * sizeof(float);
+  return qrot + krot + tab + static_cast<size_t>(B) * G * gqa::fwd::kKnParts * sizeof(float);
 }
 
 int gqa_attn_fwd_yarn(const void *q, const void *k, const void *v, void *o, float *lse, int B,
@@ -346,32 +343,35 @@ int gqa_attn_fwd_yarn(const void *q, const void *k, const void *v, void *o, floa
   DeviceState *ds = nullptr;
   if ((rc = device_state(&ds)) != GQA_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  __nv_bfloat16 *k_rot = static_cast<__nv_bfloat16 *>(workspace);
-  float2 *tab = reinterpret_cast<float2 *>(static_cast<char *>(workspace) +
-                                           static_cast<size_t>(B) * G * S * 64 * 2);
+  // workspace: q_rot, k_rot, the (cos, sin) table, the key-norm record
+  char *wp = static_cast<char *>(workspace);
+  __nv_bfloat16 *q_rot = reinterpret_cast<__nv_bfloat16 *>(wp);
+  wp += static_cast<size_t>(B) * H * S * 64 * 2;
+  __nv_bfloat16 *k_rot = reinterpret_cast<__nv_bfloat16 *>(wp);
+  wp += static_cast<size_t>(B) * G * S * 64 * 2;
+  float2 *tab = reinterpret_cast<float2 *>(wp);
+  wp += static_cast<size_t>(S) * gqa::rope::kPairs * sizeof(float2);
+  float *kn2 = score_bound ? reinterpret_cast<float *>(wp) : nullptr;
+  gqa::timing_begin(GQA_KERNEL_ROPE, st);
   {
     const long long n = static_cast<long long>(S) * gqa::rope::kPairs;
     long long blocks = (n + 255) / 256;
     blocks = blocks > 4LL * ds->sm_count ? 4LL * ds->sm_count : blocks;
-    gqa::timing_begin(GQA_KERNEL_ROPE, st);
     gqa::rope::rope_table_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(f, S, tab);
     if (gqa::cuda_failed(cudaGetLastError(), "launch of the rotary table kernel")) return GQA_ERR_CUDA;
   }
   {
-    const long long n = static_cast<long long>(B) * G * S * 8;
-    long long blocks = (n + 255) / 256;
+    const long long nq = static_cast<long long>(B) * H * S * 8, nk = static_cast<long long>(B) * G * S * 8;
+    long long blocks = (nq + nk + 255) / 256;
     blocks = blocks > 8LL * ds->sm_count ? 8LL * ds->sm_count : blocks;
-    gqa::rope::rope_rotate_k_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-        static_cast<const __nv_bfloat16 *>(k), k_rot, tab, n, S);
+    gqa::rope::rope_rotate_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+        static_cast<const __nv_bfloat16 *>(q), q_rot, nq, static_cast<const __nv_bfloat16 *>(k),
+        k_rot, nk, tab, S);
     gqa::timing_end(GQA_KERNEL_ROPE, st);
-    if (gqa::cuda_failed(cudaGetLastError(), "launch of the key rotation kernel")) return GQA_ERR_CUDA;
+    if (gqa::cuda_failed(cudaGetLastError(), "launch of the rotation kernel")) return GQA_ERR_CUDA;
   }
-  float *kn2 = nullptr;
-  if (score_bound)  // the key-norm record of the rotated keys, after the table
-    kn2 = reinterpret_cast<float *>(reinterpret_cast<char *>(tab) +
-                                    static_cast<size_t>(S) * gqa::rope::kPairs * sizeof(float2));
-  return launch_forward(q, k_rot, v, o, lse, B, H, G, S, causal, window, n_sink,
-                        static_cast<float>(tempered), kn2, tab, st);
+  return launch_forward(q_rot, k_rot, v, o, lse, B, H, G, S, causal, window, n_sink,
+                        static_cast<float>(tempered), kn2, st);
 }
 
 size_t gqa_attn_bwd_workspace_size(int B, int H, int G, int S, int d) {

@@ -13,14 +13,14 @@
 // scale.
 //
 // Kernels (on the caller's stream, into the caller's workspace):
-//   rope_table_kernel    cos / sin of m h_i for every position m < S and pair
-//                        i < 32 ([S][32] float2); the angle is reduced modulo
-//                        2 pi in fp64 (m h_i / pi in fp64, minus the nearest
-//                        even integer) before an fp32 sincospif, so positions
-//                        up to 2^24 keep full fp32 accuracy;
-//   rope_rotate_k_kernel the rotated keys [B*G][S][64] bf16 (one rounding);
-// the forward kernel rotates each query tile in shared memory after it lands
-// (fwd_kernel.cuh, kRope), from the same table.
+//   rope_table_kernel   cos / sin of m h_i for every position m < S and pair
+//                       i < 32 ([S][32] float2); the angle is reduced modulo
+//                       2 pi in fp64 (m h_i / pi in fp64, minus the nearest
+//                       even integer) before an fp32 sincospif, so positions
+//                       up to 2^24 keep full fp32 accuracy;
+//   rope_rotate_kernel  the rotated queries [B*H][S][64] and keys [B*G][S][64]
+//                       in bf16 (one rounding), in one launch; the forward
+//                       kernel then runs on them as on unrotated inputs.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -81,54 +81,43 @@ __global__ void __launch_bounds__(256) rope_table_kernel(const Freqs f, int S,
   }
 }
 
-// k_rot = rotation of k's rows (row r of kv head bg sits at position r);
-// one 16-byte chunk (4 pairs) per thread and pass.
-__global__ void __launch_bounds__(256) rope_rotate_k_kernel(const __nv_bfloat16 *__restrict__ k,
-                                                            __nv_bfloat16 *__restrict__ k_rot,
-                                                            const float2 *__restrict__ tab,
-                                                            long long n_chunks, int S) {
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < n_chunks;
-       e += stride) {
-    const long long row = e >> 3;
-    const int ch = static_cast<int>(e & 7);
-    const int m = static_cast<int>(row % S);
-    const uint4 w = reinterpret_cast<const uint4 *>(k)[e];
-    const float4 *t4 = reinterpret_cast<const float4 *>(tab + static_cast<size_t>(m) * kPairs + 4 * ch);
-    const float4 cs01 = t4[0], cs23 = t4[1];  // (c0, s0, c1, s1), (c2, s2, c3, s3)
-    const uint32_t in[4] = {w.x, w.y, w.z, w.w};
-    const float cs[8] = {cs01.x, cs01.y, cs01.z, cs01.w, cs23.x, cs23.y, cs23.z, cs23.w};
-    uint32_t out[4];
+// One rotated 16-byte chunk (4 pairs) of a row at position m.
+__device__ __forceinline__ uint4 rope_rotate_chunk(const uint4 w, const float2 *__restrict__ tab_m,
+                                                   int ch) {
+  const float4 *t4 = reinterpret_cast<const float4 *>(tab_m + 4 * ch);
+  const float4 cs01 = __ldg(t4), cs23 = __ldg(t4 + 1);  // (c0, s0, c1, s1), (c2, s2, c3, s3)
+  const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+  const float cs[8] = {cs01.x, cs01.y, cs01.z, cs01.w, cs23.x, cs23.y, cs23.z, cs23.w};
+  uint32_t out[4];
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
-      const float x0 = __uint_as_float(in[p] << 16), x1 = __uint_as_float(in[p] & 0xffff0000u);
-      const float c = cs[2 * p], s = cs[2 * p + 1];
-      out[p] = pack_bf16x2(x0 * c - x1 * s, x0 * s + x1 * c);
-    }
-    reinterpret_cast<uint4 *>(k_rot)[e] = make_uint4(out[0], out[1], out[2], out[3]);
+  for (int p = 0; p < 4; ++p) {
+    const float x0 = __uint_as_float(in[p] << 16), x1 = __uint_as_float(in[p] & 0xffff0000u);
+    const float c = cs[2 * p], s = cs[2 * p + 1];
+    out[p] = pack_bf16x2(x0 * c - x1 * s, x0 * s + x1 * c);
   }
+  return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
-// Rotates one 128-byte bf16 row (64 elements; 128-byte swizzle: 16-byte chunk c
-// at c ^ (r & 7)) in shared memory by the table row of position m.
-__device__ __forceinline__ void rope_rotate_smem_row(uint8_t *row, int r,
-                                                     const float2 *__restrict__ tab_m) {
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    uint4 *p = reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) << 4));
-    const uint4 w = *p;
-    const float4 *t4 = reinterpret_cast<const float4 *>(tab_m + 4 * c);
-    const float4 cs01 = __ldg(t4), cs23 = __ldg(t4 + 1);
-    const uint32_t in[4] = {w.x, w.y, w.z, w.w};
-    const float cs[8] = {cs01.x, cs01.y, cs01.z, cs01.w, cs23.x, cs23.y, cs23.z, cs23.w};
-    uint32_t out[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float x0 = __uint_as_float(in[q] << 16), x1 = __uint_as_float(in[q] & 0xffff0000u);
-      const float co = cs[2 * q], si = cs[2 * q + 1];
-      out[q] = pack_bf16x2(x0 * co - x1 * si, x0 * si + x1 * co);
-    }
-    *p = make_uint4(out[0], out[1], out[2], out[3]);
+// q_rot, k_rot = rotations of q's and k's rows (row r of a head sits at
+// position r % S): chunks [0, n_q) are q's, [n_q, n_q + n_k) k's; 8 chunks a
+// row, one chunk per thread and pass.
+__global__ void __launch_bounds__(256) rope_rotate_kernel(const __nv_bfloat16 *__restrict__ q,
+                                                          __nv_bfloat16 *__restrict__ q_rot,
+                                                          long long n_q,
+                                                          const __nv_bfloat16 *__restrict__ k,
+                                                          __nv_bfloat16 *__restrict__ k_rot,
+                                                          long long n_k,
+                                                          const float2 *__restrict__ tab, int S) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < n_q + n_k;
+       e += stride) {
+    const bool is_q = e < n_q;
+    const long long c = is_q ? e : e - n_q;
+    const uint4 *src = reinterpret_cast<const uint4 *>(is_q ? q : k);
+    uint4 *dst = reinterpret_cast<uint4 *>(is_q ? q_rot : k_rot);
+    const int m = static_cast<int>((c >> 3) % S);
+    dst[c] = rope_rotate_chunk(__ldcs(src + c), tab + static_cast<size_t>(m) * kPairs,
+                               static_cast<int>(c & 7));
   }
 }
 

@@ -137,10 +137,10 @@ GQA_API int gqa_attn_fwd_ws(const void *q, const void *k, const void *v, void *o
  * range note as gqa_attn_fwd_ws).
  * workspace: device memory of at least gqa_attn_fwd_yarn_workspace_size()
  * bytes, 16-byte aligned, owned by the caller and not used by any other call
- * running at the same time: the rotated keys [B][G][S][d] bf16, a [S][d/2]
- * table of (cos, sin) fp32 pairs and the key-norm record (B * G * 128 bytes),
- * written by this call (table, key rotation, [key norms,] forward; the query
- * tiles are rotated inside the forward kernel).
+ * running at the same time: the rotated queries [B][H][S][d] and keys
+ * [B][G][S][d] in bf16, a [S][d/2] table of (cos, sin) fp32 pairs and the
+ * key-norm record (B * G * 128 bytes), written by this call in that order of
+ * launches (table, rotation of q and k, [key norms,] forward).
  */
 GQA_API size_t gqa_attn_fwd_yarn_workspace_size(int B, int H, int G, int S, int d);
 GQA_API int gqa_attn_fwd_yarn(const void *q, const void *k, const void *v, void *o, float *lse,

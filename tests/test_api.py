@@ -155,8 +155,8 @@ def test_fwd_yarn_specific_errors(lib):
     assert _fwd_yarn(ws=None) == gq.GQA_ERR_NULL
     assert _fwd_yarn(ws=FAKE + 4) == gq.GQA_ERR_ALIGN
     need = gq.gqa_attn_fwd_yarn_workspace_size(1, 4, 2, 128, 64)
-    # rotated keys (bf16), the (cos, sin) table and the key-norm record
-    assert need == 1 * 2 * 128 * 64 * 2 + 128 * 32 * 8 + 1 * 2 * 128
+    # rotated queries and keys (bf16), the (cos, sin) table and the key-norm record
+    assert need == 1 * 4 * 128 * 64 * 2 + 1 * 2 * 128 * 64 * 2 + 128 * 32 * 8 + 1 * 2 * 128
     assert _fwd_yarn(wsb=need - 1) == gq.GQA_ERR_WORKSPACE
     assert gq.gqa_attn_fwd_yarn_workspace_size(1, 3, 2, 128, 64) == 0
 

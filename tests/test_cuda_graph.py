@@ -63,7 +63,7 @@ def test_graph_replay_matches_eager(fwd_ws):
 
 @pytest.mark.parametrize("kind", ["yarn", "fp8"])
 def test_graph_replay_yarn_and_fp8(kind):
-    """The rotary forward (table, key rotation, forward) and the fp8 forward
+    """The rotary forward (table, q and k rotation, forward) and the fp8 forward
     captured and replayed with new inputs: bit-identical to eager calls."""
     B, H, G, S, d, scale = 1, 8, 2, 1000, 64, 0.125
     q, k, v = (t.cuda() for t in make_inputs(B, H, G, S, seed=31))

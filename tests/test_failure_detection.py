@@ -115,9 +115,9 @@ def test_production_kernels_leave_through_the_abort_path(window, n_sink):
 
 @pytest.mark.gpu
 def test_yarn_and_fp8_forwards_leave_through_the_abort_path():
-    """The same missing load in the rotary and fp8 instantiations of the
-    forward: the query-rotation barriers and the fp8 tiles' transaction counts
-    must not keep any role waiting."""
+    """The same missing load in the rotary forward (pre-pass, then the forward
+    kernel with the score bound) and in the fp8 instantiation, whose tiles'
+    transaction counts differ: no role may be kept waiting."""
     lib = _stall_lib()
     B, H, G, S, d, scale = 1, 6, 2, 700, 64, 0.125
     q, k, v = (t.cuda() for t in make_inputs(B, H, G, S, seed=19))

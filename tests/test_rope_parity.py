@@ -3,8 +3,8 @@ oracle, through the C ABI.
 
 The oracle rotates q and k exactly (YaRN frequencies and temperature, YaRN
 paper section 3), rounds the rotated tensors once to bf16 -- what a bf16 model
-hands to its attention -- and attends in float64.  The kernel rotates the keys
-in a pre-pass and each query tile in shared memory inside the forward."""
+hands to its attention -- and attends in float64.  The library rotates q and k
+in a pre-pass into its workspace and runs the forward kernel on them."""
 import numpy as np
 import pytest
 import torch
@@ -35,7 +35,7 @@ def _gpu(q, k, v, rope, score_bound=None, **mask):
     (1, 6, 2, 777, True, 129, 300),
     (1, 4, 2, 513, False, 0, 0),
     (1, 8, 1, 520, True, 0, 0),
-    (4, 6, 2, 2048, True, 0, 0),      # more units than SMs: rotations carried across units
+    (4, 6, 2, 2048, True, 0, 0),      # more units than SMs
 ])
 @pytest.mark.parametrize("score_bound", [False, True], ids=["plain", "bound"])
 def test_yarn_forward(B, H, G, S, causal, window, n_sink, score_bound):
@@ -60,22 +60,26 @@ def test_yarn_parameters(rope):
     check_close("LSE", to64(lse), rl, max_abs=LSE_ABS, mean_abs=None, bf16_out=False)
 
 
-def test_rotated_keys_in_workspace():
-    """The pre-pass leaves bf16(rot(k)) at the start of the workspace: equal to
-    the oracle's rounded rotation except for rare one-ulp ties decided by the
-    fp32 rounding of the rotation (at most 1e-3 of the elements)."""
+def test_rotated_rows_in_workspace():
+    """The pre-pass leaves bf16(rot(q)) and then bf16(rot(k)) at the start of the
+    workspace: equal to the oracle's rounded rotation except for rare one-ulp
+    ties decided by the fp32 rounding of the rotation (at most 1e-3 of the
+    elements)."""
     B, H, G, S = 1, 4, 2, 3000
     q, k, v = make_inputs(B, H, G, S, seed=9)
     ws = torch.zeros(gq.gqa_attn_fwd_yarn_workspace_size(B, H, G, S, 64), dtype=torch.uint8,
                      device="cuda")
     gq.fwd_yarn(q.cuda(), k.cuda(), v.cuda(), workspace=ws)
     torch.cuda.synchronize()
-    got = ws[:B * G * S * 64 * 2].view(torch.bfloat16).view(B, G, S, 64).to(torch.float64).cpu().numpy()
-    _, ref = oracle.yarn_rotated(to64(q), to64(k), **DEFAULT)
-    diff = np.abs(got - ref)
-    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - 7)
-    assert (diff <= ulp * 1.0001).all()
-    assert (diff > 0).mean() <= 1e-3
+    nq, nk = B * H * S * 64 * 2, B * G * S * 64 * 2
+    got_q = ws[:nq].view(torch.bfloat16).view(B, H, S, 64).to(torch.float64).cpu().numpy()
+    got_k = ws[nq:nq + nk].view(torch.bfloat16).view(B, G, S, 64).to(torch.float64).cpu().numpy()
+    ref_q, ref_k = oracle.yarn_rotated(to64(q), to64(k), **DEFAULT)
+    for got, ref in ((got_q, ref_q), (got_k, ref_k)):
+        diff = np.abs(got - ref)
+        ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - 7)
+        assert (diff <= ulp * 1.0001).all()
+        assert (diff > 0).mean() <= 1e-3
 
 
 @pytest.mark.parametrize("score_bound", [False, True], ids=["plain", "bound"])
