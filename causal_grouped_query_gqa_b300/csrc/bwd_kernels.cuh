@@ -55,6 +55,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "bwd_order.cuh"
 #include "device_checks.cuh"
 #include "error_detail.cuh"
 #include "sm100_ptx.cuh"
@@ -160,6 +161,8 @@ struct MainParams {
   float scale;
   float scale_log2;
   int n_ktiles;
+  int n_small;      // CTA order (bwd_order.cuh): the first n_small batches hold
+  int batch_pairs;  // batch_pairs kv heads, the others batch_pairs + 1
   const float *lse2;  // [B*H][S_pad]  LSE log2(e) + e_i - E_g
   const float *delta; // [B*H][S_pad]  D' = 2^e_i D
   const int *emin;    // [B*G]         E_g
@@ -169,6 +172,7 @@ struct MainParams {
 };
 
 enum : int { kTimeoutCode = -9 };
+
 
 __host__ __device__ inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
@@ -479,12 +483,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // work unit: key tiles with the most query tiles first
-  const int u = blockIdx.x;
-  const int per_kb = p.B * p.G;
-  const int kb = u / per_kb;
-  const int b = (u % per_kb) / p.G;
-  const int g = u % p.G;
+  // work unit (cta_unit): batches of kv heads, key tiles with the most query
+  // tiles first in each
+  int kb, pair;
+  cta_unit(static_cast<int>(blockIdx.x), p.n_ktiles, p.n_small, p.batch_pairs, kb, pair);
+  const int b = pair / p.G;
+  const int g = pair % p.G;
   int qlo, qhi;
   q_range(kb, p, qlo, qhi);
   const int nqt = qhi - qlo + 1;
@@ -942,6 +946,7 @@ inline int launch(const Problem &pr, const void *q, const void *k, const void *v
     p.scale = pr.scale;
     p.scale_log2 = pr.scale * 1.4426950408889634f;
     p.n_ktiles = (S + BK - 1) / BK;
+    cta_order(B, G, R, S, p.n_ktiles, sm_count, p.n_small, p.batch_pairs);
     p.lse2 = w.lse2;
     p.delta = w.delta;
     p.emin = w.emin;
