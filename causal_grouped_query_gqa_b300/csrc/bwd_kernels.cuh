@@ -33,7 +33,9 @@
 //          take the power of two back out exactly).  The fp16 P' and dO' give
 //          the dV product 11-bit operands where bf16 would give 8;
 //          S^T, dP^T of step n+1 are issued as soon as the P/dS warps have read
-//          step n into registers, so those warps overlap step n's dV, dK, dQ;
+//          all of step n into registers, so those warps overlap step n's dV, dK,
+//          dQ; three issuing threads (S^T and dP^T; dV and dK; dQ) keep a
+//          step's dQ, which waits for the drain, from holding back the rest;
 //          P^T and dS are handed over separately (dV starts while dS is still
 //          being written) and freed separately (after dV, after dK and dQ).
 //          dS alternates between two shared-memory tiles by step, so each half
@@ -71,11 +73,12 @@ constexpr int HD = 64;
 constexpr int TILE_BYTES = 128 * HD * 2;  // 16 KB bf16 tile, 128-byte rows
 constexpr int NSTAGE = 3;                 // Q/dO ring depth
 constexpr int NTHREADS = 512;
-// Registers per thread after the split: warps 0-3 (producer, two MMA issuers,
-// TMEM alloc), the two P/dS warpgroups, the dQ drain warpgroup.
-constexpr int kRegsControl = 72;
-constexpr int kRegsSoftmax = 168;
-constexpr int kRegsDrain = 96;
+// Registers per thread after the split: warps 0-3 (producer, three MMA
+// issuers, TMEM alloc), the two P/dS warpgroups (which hold a whole step's
+// S^T and dP^T rows), the dQ drain warpgroup.
+constexpr int kRegsControl = 56;
+constexpr int kRegsSoftmax = 184;
+constexpr int kRegsDrain = 80;
 // the launch allocation must cover the split (checked on the host)
 constexpr int kMinLaunchRegs =
     (128 * (kRegsControl + kRegsDrain) + 256 * kRegsSoftmax + NTHREADS - 1) / NTHREADS;
@@ -109,11 +112,12 @@ struct Bars {
   uint64_t pt_ready;  // P^T stored in TMEM (256 P/dS threads)
   uint64_t ds_ready;  // dS stored in shared memory (256 P/dS threads)
   uint64_t pt_free;   // dV of the step finished: P^T may be overwritten (issuer B commit)
-  uint64_t ds_free[2];  // dK, dQ finished with dS tile t (issuer B commit, steps t, t+2, ...)
-  uint64_t dq_full;   // dQ tile ready (issuer B commit)
+  uint64_t ds_free[2];  // dK and dQ finished with dS tile t (issuer B and C commits, steps t, t+2, ...)
+  uint64_t dq_full;   // dQ tile ready (issuer C commit)
   uint64_t dq_free;   // dQ tile read out (128 drain threads)
   uint64_t a_done;    // every product of issuer A finished
   uint64_t dkv_done;  // every product of issuer B finished
+  uint64_t q_done;    // every product of issuer C finished
   uint32_t tmem_base;
   AbortState abort;
 };
@@ -506,8 +510,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(&bars->pt_ready, 256);
     mbar_init(&bars->ds_ready, 256);
     mbar_init(&bars->pt_free, 1);
-    mbar_init(&bars->ds_free[0], 1);
-    mbar_init(&bars->ds_free[1], 1);
+    mbar_init(&bars->ds_free[0], 2);
+    mbar_init(&bars->ds_free[1], 2);
+    mbar_init(&bars->q_done, 1);
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_free, 128);
     mbar_init(&bars->a_done, 1);
@@ -581,7 +586,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       bool ok = mbar_wait(&bars->kv_full, 0, ab, p.status, kTimeoutCode);
       for (int n = 0; ok && n < nsteps; ++n) {
         const int st = n % NSTAGE;
+        GQA_TRACE_EVENT(1, 21, n);  // issuer A starts waiting for the step's Q and dO
         if (!mbar_wait(&bars->qdo_full[st], (n / NSTAGE) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        GQA_TRACE_EVENT(1, 22, n);
         // V' (fp16) must be in place before the first dP''^T
         if (n == 0 && !mbar_wait(&bars->v_ready, 0, ab, p.status, kTimeoutCode)) { ok = false; break; }
         // the P/dS warps must have read the previous step's S^T and dP^T
@@ -602,21 +609,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mma_commit(&bars->a_done);
       if (!ok) mbar_wait_drain(&bars->a_done, 0);
     } else if (warp == 3 && lane == 0) {
-      // ============================================ issuer B: dV, dK, dQ
+      // ============================================ issuer B: dV, dK
       const uint32_t id_dv = idesc_fp16_f32(128, 64, false, true);  // dV: P'^T, dO' fp16
       const uint32_t id_dk = idesc_bf16_f32(128, 64, false, true);  // dK: dS'^T, Q bf16
-      const uint32_t id_dq = idesc_bf16_f32(128, 64, true, true);   // dQ: dS', K bf16
       const uint32_t q_addr = smem_u32(smem + SM_Q);
       const uint32_t do_addr = smem_u32(smem + SM_DO);
       const uint32_t ds_addr = smem_u32(smem + SM_DS);
-      const uint64_t k_mn = sdesc_sw128(smem_u32(smem + SM_K), TILE_BYTES, 1024);
       bool ok = true;
       for (int n = 0; n < nsteps; ++n) {
         const int st = n % NSTAGE;
         const uint64_t q_mn = sdesc_sw128(q_addr + st * TILE_BYTES, TILE_BYTES, 1024);
         const uint32_t ds_t = ds_addr + (n & 1) * DS_BYTES;  // this step's dS tile
-        const uint64_t ds_mn = sdesc_sw128(ds_t, TILE_BYTES, 1024);  // LBO: next 64-query half
         const uint64_t do_mn = sdesc_sw128(do_addr + st * TILE_BYTES, TILE_BYTES, 1024);
+        GQA_TRACE_EVENT(1, 20, n);  // issuer B starts waiting for the step's P^T
         if (!mbar_wait(&bars->pt_ready, n & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
         GQA_TRACE_EVENT(1, 4, n);
         tc_fence_after_sync();
@@ -635,6 +640,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           mma_bf16_ss(tbase + C_DK, a, q_mn + ks * 128, id_dk, (n > 0 || ks > 0));
         }
         mma_commit(&bars->qdo_empty[st]);
+        mma_commit(&bars->ds_free[n & 1]);
+        GQA_TRACE_EVENT(1, 23, n);
+      }
+      mma_commit(&bars->dkv_done);
+      if (!ok) mbar_wait_drain(&bars->dkv_done, 0);
+    } else if (warp == 2 && lane == 0) {
+      // ============================================ issuer C: dQ
+      // On its own thread, so that a step's dQ, which waits for the drain to
+      // have read the previous tile, never holds back the next step's dV and dK
+      // (one issuer for all three left the tensor pipe idle between steps).
+      const uint32_t id_dq = idesc_bf16_f32(128, 64, true, true);  // dQ: dS', K bf16
+      const uint32_t ds_addr = smem_u32(smem + SM_DS);
+      const uint64_t k_mn = sdesc_sw128(smem_u32(smem + SM_K), TILE_BYTES, 1024);
+      bool ok = true;
+      for (int n = 0; n < nsteps; ++n) {
+        const uint64_t ds_mn = sdesc_sw128(ds_addr + (n & 1) * DS_BYTES, TILE_BYTES, 1024);  // LBO: next 64-query half
+        // dS of the step is written (which implies K has landed: S^T read it)
+        if (!mbar_wait(&bars->ds_ready, n & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        // the drain has read the previous dQ tile out of TMEM
         if (n > 0 && !mbar_wait(&bars->dq_free, (n - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
         GQA_TRACE_EVENT(1, 5, n);
         tc_fence_after_sync();
@@ -645,8 +669,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mma_commit(&bars->ds_free[n & 1]);
         GQA_TRACE_EVENT(1, 6, n);
       }
-      mma_commit(&bars->dkv_done);
-      if (!ok) mbar_wait_drain(&bars->dkv_done, 0);
+      mma_commit(&bars->q_done);
+      if (!ok) mbar_wait_drain(&bars->q_done, 0);
     }
   } else if (warp < 12) {
     setmaxnreg_inc<kRegsSoftmax>();
@@ -710,16 +734,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_after_sync();
       const bool masked = pair_needs_mask(qb, kb, p);
       uint32_t pp0[16], pd0[16], pp1[16], pd1[16];
-      {
-        uint32_t sr[32], dr[32];
-        tmem_ld_32x32b_x32(tbase + lane_off + C_S + 64 * wg, sr);
-        tmem_ld_32x32b_x32(tbase + lane_off + C_DP + 64 * wg, dr);
-        tmem_wait_ld();
-        reg_fence(sr);
-        reg_fence(dr);
-        p_ds_chunk(sr, dr, lse2, dlt, 64 * wg, masked ? visible_bits(64 * wg, i0, j, p) : 0u,
-                   masked, sl2, cv, pp0, pd0);
-      }
+      uint32_t sr0[32], dr0[32], sr1[32], dr1[32];
+      // the whole step's S^T and dP^T rows into registers first, so that the
+      // next step's two products may start while this step is computed
+      tmem_ld_32x32b_x32(tbase + lane_off + C_S + 64 * wg, sr0);
+      tmem_ld_32x32b_x32(tbase + lane_off + C_DP + 64 * wg, dr0);
+      tmem_ld_32x32b_x32(tbase + lane_off + C_S + 64 * wg + 32, sr1);
+      tmem_ld_32x32b_x32(tbase + lane_off + C_DP + 64 * wg + 32, dr1);
+      tmem_wait_ld();
+      reg_fence(sr0);
+      reg_fence(dr0);
+      reg_fence(sr1);
+      reg_fence(dr1);
+      tc_fence_before_sync();
+      mbar_arrive(&bars->st_free);
+      if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 9, n);
+      p_ds_chunk(sr0, dr0, lse2, dlt, 64 * wg, masked ? visible_bits(64 * wg, i0, j, p) : 0u,
+                 masked, sl2, cv, pp0, pd0);
+#ifdef GQA_TRACE
+      reg_fence(pd0);  // the chunk's results exist before the time is taken
+#endif
+      if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 17, n);
       // dS goes to the step's tile as soon as each half of the row is computed:
       // the tile was last read by the dK and dQ products of step n - 2
       uint8_t *ds_row = ds_row0 + (n & 1) * DS_BYTES;
@@ -731,20 +766,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int q8 = 0; q8 < 4; ++q8)
         *reinterpret_cast<uint4 *>(ds_row + ((q8 ^ (r & 7)) << 4)) =
             make_uint4(pd0[4 * q8], pd0[4 * q8 + 1], pd0[4 * q8 + 2], pd0[4 * q8 + 3]);
-      {
-        uint32_t sr[32], dr[32];
-        tmem_ld_32x32b_x32(tbase + lane_off + C_S + 64 * wg + 32, sr);
-        tmem_ld_32x32b_x32(tbase + lane_off + C_DP + 64 * wg + 32, dr);
-        tmem_wait_ld();
-        reg_fence(sr);
-        reg_fence(dr);
-        // S^T and dP^T of this step are in registers: the next step's may overwrite them
-        tc_fence_before_sync();
-        mbar_arrive(&bars->st_free);
-        if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 9, n);
-        p_ds_chunk(sr, dr, lse2, dlt, 64 * wg + 32,
-                   masked ? visible_bits(64 * wg + 32, i0, j, p) : 0u, masked, sl2, cv, pp1, pd1);
-      }
+      if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 18, n);
+      p_ds_chunk(sr1, dr1, lse2, dlt, 64 * wg + 32,
+                 masked ? visible_bits(64 * wg + 32, i0, j, p) : 0u, masked, sl2, cv, pp1, pd1);
+#ifdef GQA_TRACE
+      reg_fence(pd1);
+#endif
+      if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 19, n);
 #pragma unroll
       for (int q8 = 0; q8 < 4; ++q8)
         *reinterpret_cast<uint4 *>(ds_row + (((4 + q8) ^ (r & 7)) << 4)) =
@@ -764,6 +792,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // the dS stores above become visible to the tensor core's operand reads
       fence_proxy_async_smem();
       if (lane == 0 && (warp == 4 || warp == 8)) GQA_TRACE_EVENT(1, warp == 4 ? 11 : 7, n);
+      if (lane == 0) GQA_TRACE_EVENT(1, 20 + warp, n);  // every P/dS warp's hand-over (events 24-31)
       mbar_arrive(&bars->ds_ready);
     }
     // epilogue: group 0 writes dV, group 1 writes dK (x scale), one key row per thread
