@@ -180,7 +180,7 @@ class ClockSampler:
 class Problem:
     """Device tensors of one workload and the calls of one step (through the C ABI)."""
 
-    def __init__(self, w, dev, seed, with_bwd, yarn=False, fp8=False, outliers=False):
+    def __init__(self, w, dev, seed, with_bwd, yarn=False, fp8=False, outliers=False, yarn_mode=0):
         import torch
         import causal_grouped_query_gqa_b300 as gq
         from causal_grouped_query_gqa_b300.inputs import make_inputs
@@ -216,7 +216,8 @@ class Problem:
         # the YaRN forward (rotary embeddings on q and k) instead of the plain one
         self.yarn = yarn
         if yarn:
-            self.yws_bytes = gq.gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d)
+            self.yarn_mode = yarn_mode  # rotate q and k in a pre-pass (0) or q inside the forward (1)
+            self.yws_bytes = gq.gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d, yarn_mode)
             self.yws = torch.empty(max(self.yws_bytes, 16), dtype=torch.uint8, device=dev)
 
     def step_on(self, ins, outs, strm, score_bound=None):
@@ -235,7 +236,7 @@ class Problem:
             rc = gq.gqa_attn_fwd_yarn(q_, k_, v_, o_, lse_, B, H, G, S, d, w.causal, w.window,
                                       w.n_sink, w.scale, y["rope_base"], y["rope_factor"],
                                       y["rope_orig_ctx"], y["rope_alpha"], y["rope_beta"],
-                                      bound, self.yws, self.yws_bytes, strm)
+                                      bound, self.yarn_mode, self.yws, self.yws_bytes, strm)
         elif bound:
             rc = gq.gqa_attn_fwd_ws(q_, k_, v_, o_, lse_, B, H, G, S, d, w.causal, w.window,
                                     w.n_sink, w.scale, self.fws, self.fws_bytes, strm)
@@ -347,7 +348,7 @@ def summarize(w, pb, kernel_ms, total_ms, steps, world, peaks, workload):
                           "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": fb,
                           "kernel": "gqa_fwd_kernel"}
     for kid, nbytes in ((4, knorm_bytes(w)), (1, prep_bytes(w)), (3, convert_bytes(w)),
-                       (5, rope_bytes(w))):
+                       (5, rope_bytes(w, getattr(pb, "yarn_mode", 0)))):
         if avg[kid] > 0:
             gbs = nbytes / (avg[kid] * 1e-3) / 1e9
             out.setdefault("hbm_kernels", {})[KERNEL_NAMES[kid]] = {
@@ -423,8 +424,10 @@ def run_ours(args, w, rank, world, local_rank):
         extras = {}
         for name, step in EXTRA_WORKLOADS:
             ew = WORKLOADS[name]
-            epb = Problem(ew, dev, seed=0, with_bwd=(step == "fwd+bwd"), yarn=(step == "fwd_yarn"),
-                          fp8=(step == "fwd_fp8"), outliers=step.startswith("fwd_outliers"))
+            epb = Problem(ew, dev, seed=0, with_bwd=(step == "fwd+bwd"),
+                          yarn=step.startswith("fwd_yarn"), fp8=(step == "fwd_fp8"),
+                          outliers=step.startswith("fwd_outliers"),
+                          yarn_mode=1 if step == "fwd_yarn_fused" else 0)
             if step == "fwd_outliers_plain":
                 epb.score_bound = False
             e_steps = max(3, min(args.steps, 10))
@@ -433,7 +436,8 @@ def run_ours(args, w, rank, world, local_rank):
             res.update({"step": step, "steps": e_steps, "clocks": e_clk,
                         "config": {"B": ew.B, "H": ew.H, "G": ew.G, "S": ew.S,
                                    "window": ew.window, "n_sink": ew.n_sink}})
-            extras[name + {"fwd_yarn": "+yarn", "fwd_fp8": "+fp8", "fwd_outliers": "+outlier_rows",
+            extras[name + {"fwd_yarn": "+yarn", "fwd_yarn_fused": "+yarn_fused", "fwd_fp8": "+fp8",
+                           "fwd_outliers": "+outlier_rows",
                            "fwd_outliers_plain": "+outlier_rows_plain"}.get(step, "")] = res
             del epb
             torch.cuda.empty_cache()
@@ -448,6 +452,7 @@ EXTRA_WORKLOADS = [
     ("window_b1_h128_g16_s32768_w4096_sink128", "fwd"),
     ("bwd_b4_h32_g8_s4096", "fwd+bwd"),
     ("wide_b1_h128_g16_s8192", "fwd_yarn"),   # YaRN rotary forward (table, q and k rotation, forward)
+    ("wide_b1_h128_g16_s8192", "fwd_yarn_fused"),  # the same, query tiles rotated inside the forward
     ("wide_b1_h128_g16_s8192", "fwd_fp8"),    # E4M3 queries and keys (quantised before timing)
     ("wide_b1_h128_g16_s8192", "fwd_outliers"),  # score bound with a quarter of the warps exact
     ("wide_b1_h128_g16_s8192", "fwd_outliers_plain"),  # the same input through gqa_attn_fwd
@@ -459,10 +464,12 @@ def knorm_bytes(w):
     return 2 * w.d * w.S * w.B * w.G + 128 * w.B * w.G
 
 
-def rope_bytes(w):
-    """Rotary pre-pass: writes the (cos, sin) table ([S][32] float2), reads q and
-    k (bf16) and writes their rotations (bf16)."""
-    return 8 * 32 * w.S + 2 * 2 * w.d * w.S * w.B * (w.H + w.G)
+def rope_bytes(w, mode=0):
+    """Rotary pre-pass: writes the (cos, sin) table ([S][32] float2), reads k and,
+    in the pre-pass mode (0), q (bf16) and writes their rotations (bf16); the
+    fused mode (1) rotates q inside the forward."""
+    heads = w.H + w.G if mode == 0 else w.G
+    return 8 * 32 * w.S + 2 * 2 * w.d * w.S * w.B * heads
 
 
 def prep_bytes(w):

@@ -12,9 +12,11 @@ Low-level calls (same names and argument order as the C header):
                     workspace, workspace_bytes, stream)   (score-bound forward)
     gqa_attn_fwd_workspace_size(B, H, G, S, d)
     gqa_attn_fwd_yarn(q, k, v, o, lse, B, H, G, S, d, causal, window, n_sink, scale, rope_base,
-                      rope_factor, rope_orig_ctx, rope_alpha, rope_beta, workspace,
-                      workspace_bytes, stream)   (YaRN rotary embeddings on q and k)
-    gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d)
+                      rope_factor, rope_orig_ctx, rope_alpha, rope_beta, score_bound,
+                      rope_mode, workspace, workspace_bytes, stream)
+                      (YaRN rotary embeddings on q and k; rope_mode GQA_ROPE_PREPASS or
+                      GQA_ROPE_FUSED)
+    gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d, rope_mode)
     gqa_attn_fwd_fp8(q8, k8, v, o, lse, B, H, G, S, d, causal, window, n_sink, scale, q_scale,
                      k_scale, stream)   (E4M3 queries and keys, tcgen05 kind::f8f6f4 Q K^T)
     gqa_attn_quantize_e4m3(x, out, n, inv_scale, stream)   (bf16 -> E4M3 bytes)
@@ -34,7 +36,7 @@ from __future__ import annotations
 
 from ._lib import (GQA_ERR_ALIGN, GQA_ERR_CUDA, GQA_ERR_DEVICE_TIMEOUT, GQA_ERR_HEADDIM,
                    GQA_ERR_DEVICE_BOUNDS, GQA_ERR_MASK, GQA_ERR_NULL, GQA_ERR_SCALE,
-                   GQA_ERR_SHAPE, GQA_ERR_TOO_LARGE, GQA_ERR_ROPE, YARN_DEFAULTS,
+                   GQA_ERR_SHAPE, GQA_ERR_TOO_LARGE, GQA_ERR_ROPE, GQA_ROPE_PREPASS, GQA_ROPE_FUSED, YARN_DEFAULTS,
                    fwd_yarn, gqa_attn_fwd_yarn, gqa_attn_fwd_yarn_workspace_size,
                    fwd_fp8, gqa_attn_fwd_fp8, gqa_attn_quantize_e4m3, quantize_e4m3,
                    GQA_ERR_WORKSPACE, GQA_NOALLOC_SCRATCH_BYTES, GQA_OK, SCORE_BOUND_MIN_FLOPS,
@@ -48,7 +50,7 @@ from ._lib import (GQA_ERR_ALIGN, GQA_ERR_CUDA, GQA_ERR_DEVICE_TIMEOUT, GQA_ERR_
 __all__ = [
     "fwd", "bwd", "fwd_yarn", "fwd_fp8", "gqa_attn_fwd_fp8", "gqa_attn_quantize_e4m3",
     "quantize_e4m3", "gqa_attn_fwd_yarn", "gqa_attn_fwd_yarn_workspace_size",
-    "GQA_ERR_ROPE", "YARN_DEFAULTS", "visible_pairs", "SCORE_BOUND_MIN_FLOPS", "gqa_attn_fwd", "gqa_attn_fwd_ws", "gqa_attn_fwd_workspace_size",
+    "GQA_ERR_ROPE", "GQA_ROPE_PREPASS", "GQA_ROPE_FUSED", "YARN_DEFAULTS", "visible_pairs", "SCORE_BOUND_MIN_FLOPS", "gqa_attn_fwd", "gqa_attn_fwd_ws", "gqa_attn_fwd_workspace_size",
     "gqa_attn_bwd", "gqa_attn_bwd_noalloc",
     "gqa_attn_bwd_workspace_size", "GQA_ERR_TOO_LARGE", "GQA_ERR_DEVICE_BOUNDS", "GQA_NOALLOC_SCRATCH_BYTES",
     "gqa_attn_strerror", "gqa_attn_last_error_detail", "gqa_attn_last_device_status",

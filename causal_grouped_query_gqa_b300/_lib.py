@@ -23,6 +23,9 @@ GQA_ERR_DEVICE_TIMEOUT = -9
 GQA_ERR_TOO_LARGE = -10
 GQA_ERR_DEVICE_BOUNDS = -11
 GQA_ERR_ROPE = -12
+# gqa_attn_fwd_yarn rope_mode: rotate q and k before the forward / query tiles inside it
+GQA_ROPE_PREPASS = 0
+GQA_ROPE_FUSED = 1
 GQA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -60,9 +63,9 @@ def load_library():
         lib.gqa_attn_fwd_workspace_size.argtypes = [i, i, i, i, i]
         lib.gqa_attn_fwd_workspace_size.restype = sz
         lib.gqa_attn_fwd_yarn.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f,
-                                          f, f, i, f, f, i, vp, sz, vp]
+                                          f, f, i, f, f, i, i, vp, sz, vp]
         lib.gqa_attn_fwd_yarn.restype = i
-        lib.gqa_attn_fwd_yarn_workspace_size.argtypes = [i, i, i, i, i]
+        lib.gqa_attn_fwd_yarn_workspace_size.argtypes = [i, i, i, i, i, i]
         lib.gqa_attn_fwd_yarn_workspace_size.restype = sz
         lib.gqa_attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, f, f, vp]
         lib.gqa_attn_fwd_fp8.restype = i
@@ -132,14 +135,15 @@ def gqa_attn_fwd_workspace_size(B, H, G, S, d):
 
 
 def gqa_attn_fwd_yarn(q, k, v, o, lse, B, H, G, S, d, causal, window, n_sink, scale, rope_base,
-                      rope_factor, rope_orig_ctx, rope_alpha, rope_beta, score_bound, workspace,
-                      workspace_bytes, stream=None):
+                      rope_factor, rope_orig_ctx, rope_alpha, rope_beta, score_bound, rope_mode,
+                      workspace, workspace_bytes, stream=None):
     return load_library().gqa_attn_fwd_yarn(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, G, S, d,
                                             int(causal), int(window), int(n_sink), float(scale),
                                             float(rope_base), float(rope_factor),
                                             int(rope_orig_ctx), float(rope_alpha),
                                             float(rope_beta), int(bool(score_bound)),
-                                            _p(workspace), int(workspace_bytes), _stream(stream))
+                                            int(rope_mode), _p(workspace), int(workspace_bytes),
+                                            _stream(stream))
 
 
 def gqa_attn_fwd_fp8(q8, k8, v, o, lse, B, H, G, S, d, causal, window, n_sink, scale, q_scale,
@@ -154,8 +158,8 @@ def gqa_attn_quantize_e4m3(x, out, n, inv_scale, stream=None):
                                                  _stream(stream))
 
 
-def gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d):
-    return load_library().gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d)
+def gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d, rope_mode=0):
+    return load_library().gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d, int(rope_mode))
 
 
 def gqa_attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, G, S, d, causal, window, n_sink,
@@ -298,10 +302,14 @@ YARN_DEFAULTS = dict(rope_base=10000.0, rope_factor=32.0, rope_orig_ctx=6400, ro
 
 def fwd_yarn(q, k, v, *, causal=True, window=0, n_sink=0, scale=None, rope_base=10000.0,
              rope_factor=32.0, rope_orig_ctx=6400, rope_alpha=1.0, rope_beta=32.0,
-             out=None, lse=None, workspace=None, score_bound=None, stream=None):
+             out=None, lse=None, workspace=None, score_bound=None, rope_mode=GQA_ROPE_PREPASS,
+             stream=None):
     """o, lse = fwd_yarn(q, k, v) with YaRN rotary embeddings on q and k
     (gqa_attn_fwd_yarn; `workspace` is allocated when not given; score_bound as
-    in fwd(): None takes it for problems of at least SCORE_BOUND_MIN_FLOPS)."""
+    in fwd(): None takes it for problems of at least SCORE_BOUND_MIN_FLOPS;
+    rope_mode GQA_ROPE_PREPASS rotates q and k before the forward,
+    GQA_ROPE_FUSED turns the query tiles inside it, with no rotated-query
+    workspace)."""
     import torch
     B, H, S, d = q.shape
     G = k.shape[1]
@@ -311,14 +319,15 @@ def fwd_yarn(q, k, v, *, causal=True, window=0, n_sink=0, scale=None, rope_base=
     scale = 1.0 / d ** 0.5 if scale is None else scale
     o = torch.empty_like(q) if out is None else out
     l = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if lse is None else lse
-    need = gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d)
+    need = gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d, rope_mode)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     if score_bound is None:
         score_bound = 4 * d * B * H * visible_pairs(S, causal, window, n_sink) >= SCORE_BOUND_MIN_FLOPS
     rc = gqa_attn_fwd_yarn(q, k, v, o, l, B, H, G, S, d, causal, window, n_sink, scale, rope_base,
                            rope_factor, rope_orig_ctx, rope_alpha, rope_beta, score_bound,
-                           workspace, workspace.numel() * workspace.element_size(), stream)
+                           rope_mode, workspace, workspace.numel() * workspace.element_size(),
+                           stream)
     if rc != GQA_OK:
         raise GqaError(rc, "gqa_attn_fwd_yarn")
     return o, l

@@ -48,6 +48,7 @@
 #include <type_traits>
 
 #include "device_checks.cuh"
+#include "rope_kernels.cuh"
 #include "sm100_ptx.cuh"
 #include "trace.cuh"
 
@@ -115,6 +116,8 @@ struct Bars {
   uint64_t pv_done[2]; // every P.V product of head t finished (abort drain)
   uint64_t turn[2];    // ping-pong of the exp2 sections: turn[t] opens head t's
                        // section (arrived by the other head's 128 threads)
+  uint64_t q_ready[2]; // rotary embedding only: head t's Q tile rotated in place
+                       // (128 softmax threads of head t, once per unit)
   uint64_t vote_bar[2];  // score bound: head t's four warps have cast their vote
   int vote[2][2];        // score bound: AND of head t's warp votes, two alternating slots
   uint32_t tmem_base;
@@ -131,6 +134,7 @@ struct Params {
   int n_pairs;  // ceil(R / 2) head pairs per kv head
   int n_units;  // n_qblocks * B * G * n_pairs
   const float *kn2;  // [B*G][kKnParts] partial maxima of |k_j|^2, or null (no score bound)
+  const float2 *rope_tab;  // rotary embedding: [S][32] (cos, sin) per position and pair
   __nv_bfloat16 *o;
   float *lse;
   int *status;
@@ -253,11 +257,13 @@ __device__ __forceinline__ int unit_at(int k, const Params &p) {
   return base + c < p.n_units ? base + c : -1;
 }
 
+// kRope: the query tiles are turned by the rotary embedding (rope_kernels.cuh)
+// in shared memory before their first Q K^T; the keys arrive already rotated.
 // kFp8: queries and keys are OCP E4M3 bytes (64-byte rows, 64-byte swizzle,
 // 8 KB tiles in the 16 KB slots); S = Q K^T runs as tcgen05.mma
 // kind::f8f6f4 (K = 32 per instruction) and the two per-tensor scales are
 // folded into scale_log2 on the host.  P.V stays bf16.
-template <bool kFp8>
+template <bool kRope, bool kFp8>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gqa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
@@ -271,6 +277,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int lane = threadIdx.x & 31;
   // bytes of one Q or K tile as loaded (fp8 rows are half as long)
   constexpr uint32_t kQTileBytes = kFp8 ? TILE_BYTES / 2 : TILE_BYTES;
+  static_assert(!(kFp8 && kRope), "the fp8 forward takes no rotary embedding");
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full[0], 1);
@@ -289,6 +296,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&bars->o_empty[t], 128);
       mbar_init(&bars->turn[t], 128);
       mbar_init(&bars->pv_done[t], 1);
+      mbar_init(&bars->q_ready[t], 128);
       mbar_init(&bars->vote_bar[t], 128);
       bars->vote[t][0] = 1;
       bars->vote[t][1] = 1;
@@ -375,6 +383,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     int gt = 0;             // K/V tiles consumed (all units)
     int ts[2] = {0, 0};     // S products issued per head (all units)
     int qf[2] = {0, 0};     // Q tiles consumed per head (all units)
+    int qr[2] = {0, 0};     // rotated Q tiles consumed per head (rotary embedding)
     bool ok = true;
     for (int k = 0; ok; ++k) {
       const int u = unit_at(k, p);
@@ -396,6 +405,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               break;
             }
             ++qf[t];
+          }
+          if constexpr (kRope) {
+            // and, with the rotary embedding, that tile turned
+            if (it == 0) {
+              if (!mbar_wait(&bars->q_ready[t], qr[t] & 1, ab, p.status, kTimeoutCode)) {
+                ok = false;
+                break;
+              }
+              ++qr[t];
+            }
           }
           tc_fence_after_sync();
           if constexpr (kFp8) {
@@ -516,6 +535,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int lo = win ? i - p.window : -1;
       const int ns = win ? p.n_sink : 0;
 
+      if constexpr (kRope) {
+        // turn this row of head t's Q tile (position i) before any Q K^T reads it
+        if (!mbar_wait(&bars->q_full[t], qk & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        if (i < p.S)
+          rope::rope_rotate_smem_row(smem + SM_Q + t * TILE_BYTES + r * 128, r,
+                                     p.rope_tab + static_cast<size_t>(i) * rope::kPairs);
+        fence_proxy_async_smem();
+        mbar_arrive(&bars->q_ready[t]);
+      }
       float m_run = -CUDART_INF_F;  // running max of scaled scores, base-2 units
       float l_run = 0.f;            // running sum of 2^(s - m_run)
       // Score bound (kBoundMax): decided for the head's 128 rows together

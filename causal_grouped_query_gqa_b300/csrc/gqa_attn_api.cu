@@ -68,7 +68,8 @@ int device_state(DeviceState **out) {
             cudaGetSymbolAddress(reinterpret_cast<void **>(&st.status), g_device_status),
             "cudaGetSymbolAddress(device status word)"))
       return GQA_ERR_CUDA;
-    for (auto kern : {gqa::fwd::gqa_fwd_kernel<false>, gqa::fwd::gqa_fwd_kernel<true>}) {
+    for (auto kern : {gqa::fwd::gqa_fwd_kernel<false, false>, gqa::fwd::gqa_fwd_kernel<true, false>,
+                      gqa::fwd::gqa_fwd_kernel<false, true>}) {
       if (gqa::cuda_failed(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                 gqa::fwd::SMEM_BYTES),
                            "cudaFuncSetAttribute(forward shared memory)"))
@@ -183,11 +184,13 @@ const char *gqa_attn_strerror(int status) {
 namespace {
 
 // The forward launch shared by the entry points; kn2 (the score-bound record
-// that fwd_knorm_kernel writes first, on the same stream) may be null.  fp8: q and k
+// that fwd_knorm_kernel writes first, on the same stream) may be null, and so
+// may rope_tab (the rotary table: with it the kernel rotates each query tile;
+// k is then already rotated).  fp8: q and k
 // are E4M3 bytes and `scale` already carries their two dequantisation scales.
 int launch_forward(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
                    int G, int S, int causal, int window, int n_sink, float scale, float *kn2,
-                   cudaStream_t st, bool fp8 = false) {
+                   const float2 *rope_tab, cudaStream_t st, bool fp8 = false) {
   DeviceState *ds = nullptr;
   int rc = device_state(&ds);
   if (rc != GQA_OK) return rc;
@@ -217,6 +220,7 @@ int launch_forward(const void *q, const void *k, const void *v, void *o, float *
   p.n_qblocks = (S + BM - 1) / BM;
   p.n_pairs = (p.R + 1) / 2;
   p.kn2 = kn2;
+  p.rope_tab = rope_tab;
   p.o = static_cast<__nv_bfloat16 *>(o);
   p.lse = lse;
   p.status = ds->status;
@@ -238,9 +242,11 @@ int launch_forward(const void *q, const void *k, const void *v, void *o, float *
   }
   gqa::timing_begin(GQA_KERNEL_FWD, st);
   if (fp8)
-    gqa_fwd_kernel<true><<<static_cast<unsigned>(grid), NTHREADS, SMEM_BYTES, st>>>(tq, tk, tv, p);
+    gqa_fwd_kernel<false, true><<<static_cast<unsigned>(grid), NTHREADS, SMEM_BYTES, st>>>(tq, tk, tv, p);
+  else if (rope_tab)
+    gqa_fwd_kernel<true, false><<<static_cast<unsigned>(grid), NTHREADS, SMEM_BYTES, st>>>(tq, tk, tv, p);
   else
-    gqa_fwd_kernel<false><<<static_cast<unsigned>(grid), NTHREADS, SMEM_BYTES, st>>>(tq, tk, tv, p);
+    gqa_fwd_kernel<false, false><<<static_cast<unsigned>(grid), NTHREADS, SMEM_BYTES, st>>>(tq, tk, tv, p);
   gqa::timing_end(GQA_KERNEL_FWD, st);
   return gqa::cuda_failed(cudaGetLastError(), "launch of the forward kernel") ? GQA_ERR_CUDA
                                                                                : GQA_OK;
@@ -257,7 +263,7 @@ int gqa_attn_fwd(const void *q, const void *k, const void *v, void *o, float *ls
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return GQA_ERR_ALIGN;
   return launch_forward(q, k, v, o, lse, B, H, G, S, causal, window, n_sink, scale, nullptr,
-                        static_cast<cudaStream_t>(stream));
+                        nullptr, static_cast<cudaStream_t>(stream));
 }
 
 size_t gqa_attn_fwd_workspace_size(int B, int H, int G, int S, int d) {
@@ -276,7 +282,7 @@ int gqa_attn_fwd_ws(const void *q, const void *k, const void *v, void *o, float 
     return GQA_ERR_ALIGN;
   if (workspace_bytes < gqa_attn_fwd_workspace_size(B, H, G, S, d)) return GQA_ERR_WORKSPACE;
   return launch_forward(q, k, v, o, lse, B, H, G, S, causal, window, n_sink, scale,
-                        static_cast<float *>(workspace), static_cast<cudaStream_t>(stream));
+                        static_cast<float *>(workspace), nullptr, static_cast<cudaStream_t>(stream));
 }
 
 int gqa_attn_fwd_fp8(const void *q8, const void *k8, const void *v, void *o, float *lse, int B,
@@ -292,7 +298,7 @@ int gqa_attn_fwd_fp8(const void *q8, const void *k8, const void *v, void *o, flo
   if (!aligned16(q8) || !aligned16(k8) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return GQA_ERR_ALIGN;
   return launch_forward(q8, k8, v, o, lse, B, H, G, S, causal, window, n_sink,
-                        static_cast<float>(folded), nullptr,
+                        static_cast<float>(folded), nullptr, nullptr,
                         static_cast<cudaStream_t>(stream), true);
 }
 
@@ -315,43 +321,49 @@ int gqa_attn_quantize_e4m3(const void *x, void *out, long long n, float inv_scal
              : GQA_OK;
 }
 
-size_t gqa_attn_fwd_yarn_workspace_size(int B, int H, int G, int S, int d) {
+size_t gqa_attn_fwd_yarn_workspace_size(int B, int H, int G, int S, int d, int rope_mode) {
   if (check_common(B, H, G, S, d, 1, 0, 0, 1.f) != GQA_OK) return 0;
-  const size_t qrot = static_cast<size_t>(B) * H * S * 64 * 2;  // multiples of 16
+  if (rope_mode != GQA_ROPE_PREPASS && rope_mode != GQA_ROPE_FUSED) return 0;
+  // k_rot, the (cos, sin) table, the key-norm record, then (pre-pass) q_rot;
+  // every part a multiple of 16 bytes
   const size_t krot = static_cast<size_t>(B) * G * S * 64 * 2;
   const size_t tab = static_cast<size_t>(S) * gqa::rope::kPairs * sizeof(float2);
-  return qrot + krot + tab + static_cast<size_t>(B) * G * gqa::fwd::kKnParts * sizeof(float);
+  const size_t kn = static_cast<size_t>(B) * G * gqa::fwd::kKnParts * sizeof(float);
+  const size_t qrot = rope_mode == GQA_ROPE_PREPASS ? static_cast<size_t>(B) * H * S * 64 * 2 : 0;
+  return krot + tab + kn + qrot;
 }
 
 int gqa_attn_fwd_yarn(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                       int H, int G, int S, int d, int causal, int window, int n_sink, float scale,
                       float rope_base, float rope_factor, int rope_orig_ctx, float rope_alpha,
-                      float rope_beta, int score_bound, void *workspace, size_t workspace_bytes,
-                      void *stream) {
+                      float rope_beta, int score_bound, int rope_mode, void *workspace,
+                      size_t workspace_bytes, void *stream) {
   int rc = check_common(B, H, G, S, d, causal, window, n_sink, scale);
   if (rc != GQA_OK) return rc;
   gqa::rope::Freqs f;
-  if (!gqa::rope::yarn_freqs(rope_base, rope_factor, rope_orig_ctx, rope_alpha, rope_beta, &f))
+  if (!gqa::rope::yarn_freqs(rope_base, rope_factor, rope_orig_ctx, rope_alpha, rope_beta, &f) ||
+      (rope_mode != GQA_ROPE_PREPASS && rope_mode != GQA_ROPE_FUSED))
     return GQA_ERR_ROPE;
   if (!q || !k || !v || !o || !lse || !workspace) return GQA_ERR_NULL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
       !aligned16(workspace))
     return GQA_ERR_ALIGN;
-  if (workspace_bytes < gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d)) return GQA_ERR_WORKSPACE;
+  if (workspace_bytes < gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d, rope_mode))
+    return GQA_ERR_WORKSPACE;
   const double tempered = static_cast<double>(scale) * gqa::rope::yarn_score_factor(rope_factor);
   if (!(tempered < 3.0e38)) return GQA_ERR_SCALE;
   DeviceState *ds = nullptr;
   if ((rc = device_state(&ds)) != GQA_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // workspace: q_rot, k_rot, the (cos, sin) table, the key-norm record
+  const bool prepass = rope_mode == GQA_ROPE_PREPASS;
   char *wp = static_cast<char *>(workspace);
-  __nv_bfloat16 *q_rot = reinterpret_cast<__nv_bfloat16 *>(wp);
-  wp += static_cast<size_t>(B) * H * S * 64 * 2;
   __nv_bfloat16 *k_rot = reinterpret_cast<__nv_bfloat16 *>(wp);
   wp += static_cast<size_t>(B) * G * S * 64 * 2;
   float2 *tab = reinterpret_cast<float2 *>(wp);
   wp += static_cast<size_t>(S) * gqa::rope::kPairs * sizeof(float2);
   float *kn2 = score_bound ? reinterpret_cast<float *>(wp) : nullptr;
+  wp += static_cast<size_t>(B) * G * gqa::fwd::kKnParts * sizeof(float);
+  __nv_bfloat16 *q_rot = prepass ? reinterpret_cast<__nv_bfloat16 *>(wp) : nullptr;
   gqa::timing_begin(GQA_KERNEL_ROPE, st);
   {
     const long long n = static_cast<long long>(S) * gqa::rope::kPairs;
@@ -361,7 +373,8 @@ int gqa_attn_fwd_yarn(const void *q, const void *k, const void *v, void *o, floa
     if (gqa::cuda_failed(cudaGetLastError(), "launch of the rotary table kernel")) return GQA_ERR_CUDA;
   }
   {
-    const long long nq = static_cast<long long>(B) * H * S * 8, nk = static_cast<long long>(B) * G * S * 8;
+    const long long nq = prepass ? static_cast<long long>(B) * H * S * 8 : 0;
+    const long long nk = static_cast<long long>(B) * G * S * 8;
     long long blocks = (nq + nk + 255) / 256;
     blocks = blocks > 8LL * ds->sm_count ? 8LL * ds->sm_count : blocks;
     gqa::rope::rope_rotate_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
@@ -370,8 +383,11 @@ int gqa_attn_fwd_yarn(const void *q, const void *k, const void *v, void *o, floa
     gqa::timing_end(GQA_KERNEL_ROPE, st);
     if (gqa::cuda_failed(cudaGetLastError(), "launch of the rotation kernel")) return GQA_ERR_CUDA;
   }
-  return launch_forward(q_rot, k_rot, v, o, lse, B, H, G, S, causal, window, n_sink,
-                        static_cast<float>(tempered), kn2, st);
+  // pre-pass: the plain forward on rotated q and k; fused: the forward turns
+  // each query tile by the table itself
+  return launch_forward(prepass ? static_cast<const void *>(q_rot) : q, k_rot, v, o, lse, B, H, G,
+                        S, causal, window, n_sink, static_cast<float>(tempered), kn2,
+                        prepass ? nullptr : tab, st);
 }
 
 size_t gqa_attn_bwd_workspace_size(int B, int H, int G, int S, int d) {

@@ -18,9 +18,12 @@
 //                       2 pi in fp64 (m h_i / pi in fp64, minus the nearest
 //                       even integer) before an fp32 sincospif, so positions
 //                       up to 2^24 keep full fp32 accuracy;
-//   rope_rotate_kernel  the rotated queries [B*H][S][64] and keys [B*G][S][64]
-//                       in bf16 (one rounding), in one launch; the forward
-//                       kernel then runs on them as on unrotated inputs.
+//   rope_rotate_kernel  the rotated keys [B*G][S][64] in bf16 (one rounding)
+//                       and, in the pre-pass mode, the rotated queries
+//                       [B*H][S][64] as well, in one launch.
+// In the fused mode the forward kernel rotates each query tile in shared
+// memory as it lands (rope_rotate_smem_row, fwd_kernel.cuh kRope), which
+// needs no query-sized workspace; the pre-pass mode measured faster.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -118,6 +121,17 @@ __global__ void __launch_bounds__(256) rope_rotate_kernel(const __nv_bfloat16 *_
     const int m = static_cast<int>((c >> 3) % S);
     dst[c] = rope_rotate_chunk(__ldcs(src + c), tab + static_cast<size_t>(m) * kPairs,
                                static_cast<int>(c & 7));
+  }
+}
+
+// Rotates one 128-byte bf16 row (64 elements; 128-byte swizzle: 16-byte chunk c
+// at c ^ (r & 7)) in shared memory by the table row of its position.
+__device__ __forceinline__ void rope_rotate_smem_row(uint8_t *row, int r,
+                                                     const float2 *__restrict__ tab_m) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint4 *p = reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) << 4));
+    *p = rope_rotate_chunk(*p, tab_m, c);
   }
 }
 

@@ -129,25 +129,34 @@ GQA_API int gqa_attn_fwd_ws(const void *q, const void *k, const void *v, void *o
  * and o, lse are those of these scores (lse is their natural-log normaliser).
  * The rotated rows are rounded once to bf16 before the products.  Mask, layouts
  * and errors as gqa_attn_fwd, plus GQA_ERR_ROPE when rope_base <= 1,
- * rope_factor < 1, rope_orig_ctx <= 0 or not 0 <= rope_alpha < rope_beta, and
+ * rope_factor < 1, rope_orig_ctx <= 0, not 0 <= rope_alpha < rope_beta or
+ * rope_mode is neither GQA_ROPE_PREPASS nor GQA_ROPE_FUSED, and
  * GQA_ERR_NULL / GQA_ERR_WORKSPACE for a missing or short workspace.
  * score_bound: 0 takes the online maximum on every tile as gqa_attn_fwd does;
  * non-zero takes the score bound of gqa_attn_fwd_ws on the rotated queries and
  * keys (one more launch: the key-norm pre-pass on the rotated keys; same input
  * range note as gqa_attn_fwd_ws).
- * workspace: device memory of at least gqa_attn_fwd_yarn_workspace_size()
- * bytes, 16-byte aligned, owned by the caller and not used by any other call
- * running at the same time: the rotated queries [B][H][S][d] and keys
- * [B][G][S][d] in bf16, a [S][d/2] table of (cos, sin) fp32 pairs and the
- * key-norm record (B * G * 128 bytes), written by this call in that order of
- * launches (table, rotation of q and k, [key norms,] forward).
+ * rope_mode: GQA_ROPE_PREPASS rotates q and k in one launch before the forward,
+ * which then runs as gqa_attn_fwd on the rotated tensors (the faster mode);
+ * GQA_ROPE_FUSED rotates only k beforehand and turns each query tile in
+ * shared memory inside the forward kernel, right after it lands and before
+ * its first Q K^T, so the workspace holds no rotated queries.  The two modes
+ * compute the same bf16-rounded rotations.
+ * workspace: device memory of at least
+ * gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d, rope_mode) bytes, 16-byte
+ * aligned, owned by the caller and not used by any other call running at the
+ * same time: the rotated keys [B][G][S][d] bf16, a [S][d/2] table of
+ * (cos, sin) fp32 pairs, the key-norm record (B * G * 128 bytes) and, with
+ * GQA_ROPE_PREPASS, the rotated queries [B][H][S][d] bf16, in that order; the
+ * size function returns 0 for arguments the call rejects.
  */
-GQA_API size_t gqa_attn_fwd_yarn_workspace_size(int B, int H, int G, int S, int d);
+enum { GQA_ROPE_PREPASS = 0, GQA_ROPE_FUSED = 1 };
+GQA_API size_t gqa_attn_fwd_yarn_workspace_size(int B, int H, int G, int S, int d, int rope_mode);
 GQA_API int gqa_attn_fwd_yarn(const void *q, const void *k, const void *v, void *o, float *lse,
                       int B, int H, int G, int S, int d,
                       int causal, int window, int n_sink, float scale,
                       float rope_base, float rope_factor, int rope_orig_ctx,
-                      float rope_alpha, float rope_beta, int score_bound,
+                      float rope_alpha, float rope_beta, int score_bound, int rope_mode,
                       void *workspace, size_t workspace_bytes, void *stream);
 
 /*
@@ -298,7 +307,7 @@ typedef enum {
     GQA_KERNEL_BWD_MAIN = 2,  /* backward: dk, dv and the dq accumulation */
     GQA_KERNEL_BWD_DQ = 3,    /* backward: dq accumulator -> bf16 dq */
     GQA_KERNEL_FWD_KNORM = 4, /* gqa_attn_fwd_ws: key-norm maxima for the score bound */
-    GQA_KERNEL_ROPE = 5,      /* gqa_attn_fwd_yarn: rotary table and key rotation */
+    GQA_KERNEL_ROPE = 5,      /* gqa_attn_fwd_yarn: rotary table and the q / k rotation */
     GQA_KERNEL_COUNT = 6
 } gqa_kernel_id;
 

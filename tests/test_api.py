@@ -96,12 +96,12 @@ def _bwd(**kw):
 def _fwd_yarn(**kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=4, G=2, S=128, d=64,
              causal=1, window=0, n_sink=0, scale=0.125, base=10000.0, factor=32.0, L=6400,
-             alpha=1.0, beta=32.0, sb=1, ws=FAKE, wsb=1 << 24, stream=0)
+             alpha=1.0, beta=32.0, sb=1, mode=0, ws=FAKE, wsb=1 << 24, stream=0)
     a.update(kw)
     return gq.gqa_attn_fwd_yarn(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["G"],
                                 a["S"], a["d"], a["causal"], a["window"], a["n_sink"], a["scale"],
                                 a["base"], a["factor"], a["L"], a["alpha"], a["beta"], a["sb"],
-                                a["ws"], a["wsb"], a["stream"])
+                                a["mode"], a["ws"], a["wsb"], a["stream"])
 
 
 def _fwd_fp8(**kw):
@@ -154,11 +154,18 @@ def test_fwd_yarn_specific_errors(lib):
     assert _fwd_yarn(base=float("nan")) == gq.GQA_ERR_ROPE
     assert _fwd_yarn(ws=None) == gq.GQA_ERR_NULL
     assert _fwd_yarn(ws=FAKE + 4) == gq.GQA_ERR_ALIGN
-    need = gq.gqa_attn_fwd_yarn_workspace_size(1, 4, 2, 128, 64)
-    # rotated queries and keys (bf16), the (cos, sin) table and the key-norm record
-    assert need == 1 * 4 * 128 * 64 * 2 + 1 * 2 * 128 * 64 * 2 + 128 * 32 * 8 + 1 * 2 * 128
+    assert _fwd_yarn(mode=2) == gq.GQA_ERR_ROPE
+    assert _fwd_yarn(mode=-1) == gq.GQA_ERR_ROPE
+    # rotated keys (bf16), the (cos, sin) table, the key-norm record and, in the
+    # pre-pass mode, the rotated queries (bf16)
+    fused = gq.gqa_attn_fwd_yarn_workspace_size(1, 4, 2, 128, 64, gq.GQA_ROPE_FUSED)
+    assert fused == 1 * 2 * 128 * 64 * 2 + 128 * 32 * 8 + 1 * 2 * 128
+    need = gq.gqa_attn_fwd_yarn_workspace_size(1, 4, 2, 128, 64, gq.GQA_ROPE_PREPASS)
+    assert need == fused + 1 * 4 * 128 * 64 * 2
     assert _fwd_yarn(wsb=need - 1) == gq.GQA_ERR_WORKSPACE
-    assert gq.gqa_attn_fwd_yarn_workspace_size(1, 3, 2, 128, 64) == 0
+    assert _fwd_yarn(mode=1, wsb=fused - 1) == gq.GQA_ERR_WORKSPACE
+    assert gq.gqa_attn_fwd_yarn_workspace_size(1, 3, 2, 128, 64, 0) == 0
+    assert gq.gqa_attn_fwd_yarn_workspace_size(1, 4, 2, 128, 64, 2) == 0
 
 
 def test_fp8_specific_errors(lib):

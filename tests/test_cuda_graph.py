@@ -61,23 +61,24 @@ def test_graph_replay_matches_eager(fwd_ws):
         assert (got[2].float() - rq.float()).abs().max().item() <= 2e-2
 
 
-@pytest.mark.parametrize("kind", ["yarn", "fp8"])
+@pytest.mark.parametrize("kind", ["yarn", "yarn_fused", "fp8"])
 def test_graph_replay_yarn_and_fp8(kind):
-    """The rotary forward (table, q and k rotation, forward) and the fp8 forward
-    captured and replayed with new inputs: bit-identical to eager calls."""
+    """The rotary forward (both modes: table, rotation, forward) and the fp8
+    forward captured and replayed with new inputs: bit-identical to eager calls."""
     B, H, G, S, d, scale = 1, 8, 2, 1000, 64, 0.125
     q, k, v = (t.cuda() for t in make_inputs(B, H, G, S, seed=31))
     q8 = torch.empty(q.shape, dtype=torch.uint8, device="cuda")
     k8 = torch.empty(k.shape, dtype=torch.uint8, device="cuda")
     o = torch.empty_like(q)
     lse = torch.empty((B, H, S), dtype=torch.float32, device="cuda")
-    yws = torch.empty(gq.gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d), dtype=torch.uint8,
+    mode = gq.GQA_ROPE_FUSED if kind == "yarn_fused" else gq.GQA_ROPE_PREPASS
+    yws = torch.empty(gq.gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d, mode), dtype=torch.uint8,
                       device="cuda")
 
     def forward(o_, lse_, stream):
-        if kind == "yarn":
+        if kind.startswith("yarn"):
             return gq.gqa_attn_fwd_yarn(q, k, v, o_, lse_, B, H, G, S, d, 1, 0, 0, scale, 10000.0,
-                                        32.0, 6400, 1.0, 32.0, 1, yws, yws.numel(), stream)
+                                        32.0, 6400, 1.0, 32.0, 1, mode, yws, yws.numel(), stream)
         return gq.gqa_attn_fwd_fp8(q8, k8, v, o_, lse_, B, H, G, S, d, 1, 0, 0, scale, 1 / 64,
                                    1 / 64, stream)
 

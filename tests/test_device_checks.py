@@ -41,8 +41,8 @@ def checked():
     lib.gqa_attn_bwd_workspace_size.restype = sz
     lib.gqa_attn_last_device_status.argtypes = [vp]
     lib.gqa_attn_fwd_yarn.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f,
-                                      f, f, i, f, f, i, vp, sz, vp]
-    lib.gqa_attn_fwd_yarn_workspace_size.argtypes = [i, i, i, i, i]
+                                      f, f, i, f, f, i, i, vp, sz, vp]
+    lib.gqa_attn_fwd_yarn_workspace_size.argtypes = [i, i, i, i, i, i]
     lib.gqa_attn_fwd_yarn_workspace_size.restype = sz
     lib.gqa_attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, f, f, vp]
     return lib
@@ -83,17 +83,18 @@ def test_checked_build_yarn_and_fp8(checked, B, H, G, S, causal, window, n_sink)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     o = torch.empty_like(qd)
     lse = torch.empty((B, H, S), dtype=torch.float32, device="cuda")
-    ws = torch.empty(checked.gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d), dtype=torch.uint8,
-                     device="cuda")
     st = torch.cuda.current_stream().cuda_stream
     p = lambda t: t.data_ptr()
-    assert checked.gqa_attn_fwd_yarn(p(qd), p(kd), p(vd), p(o), p(lse), B, H, G, S, d, causal,
-                                     window, n_sink, scale, 10000.0, 32.0, 6400, 1.0, 32.0, 1,
-                                     p(ws), ws.numel(), st) == gq.GQA_OK
-    assert checked.gqa_attn_last_device_status(st) == gq.GQA_OK
     kw = dict(causal=bool(causal), window=window, n_sink=n_sink, scale=scale)
     ro, _ = oracle.attn_fwd_yarn(to64(q), to64(k), to64(v), **kw)
-    check_close("O (YaRN)", to64(o), ro)
+    for mode in (gq.GQA_ROPE_PREPASS, gq.GQA_ROPE_FUSED):
+        ws = torch.empty(checked.gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d, mode),
+                         dtype=torch.uint8, device="cuda")
+        assert checked.gqa_attn_fwd_yarn(p(qd), p(kd), p(vd), p(o), p(lse), B, H, G, S, d, causal,
+                                         window, n_sink, scale, 10000.0, 32.0, 6400, 1.0, 32.0, 1,
+                                         mode, p(ws), ws.numel(), st) == gq.GQA_OK
+        assert checked.gqa_attn_last_device_status(st) == gq.GQA_OK
+        check_close(f"O (YaRN, rope_mode {mode})", to64(o), ro)
     q8 = (q.float() * 64).to(torch.float8_e4m3fn).view(torch.uint8)
     k8 = (k.float() * 64).to(torch.float8_e4m3fn).view(torch.uint8)
     assert checked.gqa_attn_fwd_fp8(p(q8.cuda()), p(k8.cuda()), p(vd), p(o), p(lse), B, H, G, S, d,

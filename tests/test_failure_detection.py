@@ -65,8 +65,8 @@ def _stall_lib():
     lib.gqa_attn_bwd_workspace_size.restype = sz
     lib.gqa_attn_last_device_status.argtypes = [vp]
     lib.gqa_attn_fwd_yarn.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f,
-                                      f, f, i, f, f, i, vp, sz, vp]
-    lib.gqa_attn_fwd_yarn_workspace_size.argtypes = [i, i, i, i, i]
+                                      f, f, i, f, f, i, i, vp, sz, vp]
+    lib.gqa_attn_fwd_yarn_workspace_size.argtypes = [i, i, i, i, i, i]
     lib.gqa_attn_fwd_yarn_workspace_size.restype = sz
     lib.gqa_attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, f, f, vp]
     return lib
@@ -115,22 +115,25 @@ def test_production_kernels_leave_through_the_abort_path(window, n_sink):
 
 @pytest.mark.gpu
 def test_yarn_and_fp8_forwards_leave_through_the_abort_path():
-    """The same missing load in the rotary forward (pre-pass, then the forward
-    kernel with the score bound) and in the fp8 instantiation, whose tiles'
-    transaction counts differ: no role may be kept waiting."""
+    """The same missing load in the rotary forward (both modes: rotated inputs,
+    and the query-rotation barriers of the fused mode; with the score bound)
+    and in the fp8 instantiation, whose tiles' transaction counts differ: no
+    role may be kept waiting."""
     lib = _stall_lib()
     B, H, G, S, d, scale = 1, 6, 2, 700, 64, 0.125
     q, k, v = (t.cuda() for t in make_inputs(B, H, G, S, seed=19))
     o = torch.empty_like(q)
     lse = torch.empty((B, H, S), dtype=torch.float32, device="cuda")
-    ws = torch.empty(lib.gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d), dtype=torch.uint8,
-                     device="cuda")
     st = torch.cuda.current_stream().cuda_stream
     p = lambda t: t.data_ptr()
     assert lib.gqa_attn_last_device_status(st) == gq.GQA_OK
-    assert lib.gqa_attn_fwd_yarn(p(q), p(k), p(v), p(o), p(lse), B, H, G, S, d, 1, 0, 0, scale,
-                                 10000.0, 32.0, 6400, 1.0, 32.0, 1, p(ws), ws.numel(), st) == gq.GQA_OK
-    assert lib.gqa_attn_last_device_status(st) == gq.GQA_ERR_DEVICE_TIMEOUT
+    for mode in (gq.GQA_ROPE_PREPASS, gq.GQA_ROPE_FUSED):
+        ws = torch.empty(lib.gqa_attn_fwd_yarn_workspace_size(B, H, G, S, d, mode),
+                         dtype=torch.uint8, device="cuda")
+        assert lib.gqa_attn_fwd_yarn(p(q), p(k), p(v), p(o), p(lse), B, H, G, S, d, 1, 0, 0, scale,
+                                     10000.0, 32.0, 6400, 1.0, 32.0, 1, mode, p(ws), ws.numel(),
+                                     st) == gq.GQA_OK
+        assert lib.gqa_attn_last_device_status(st) == gq.GQA_ERR_DEVICE_TIMEOUT
     q8 = (q.float() * 64).to(torch.float8_e4m3fn).view(torch.uint8)
     k8 = (k.float() * 64).to(torch.float8_e4m3fn).view(torch.uint8)
     assert lib.gqa_attn_fwd_fp8(p(q8), p(k8), p(v), p(o), p(lse), B, H, G, S, d, 1, 0, 0, scale,
