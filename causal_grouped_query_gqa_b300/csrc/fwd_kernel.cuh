@@ -416,6 +416,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               ++qr[t];
             }
           }
+          GQA_TRACE_EVENT(0, t == 0 ? 22 : 23, k == 0 ? it : kTraceSteps);  // S_t issue starts
           tc_fence_after_sync();
           if constexpr (kFp8) {
             const uint64_t ad = sdesc_sw64(q_addr0 + t * TILE_BYTES, 16, 512);

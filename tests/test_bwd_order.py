@@ -63,6 +63,7 @@ def _order(exe, B, G, R, S, sms=148):
     (3, 5, 2, 1000),     # uneven batch sizes
     (7, 3, 16, 20000),
     (1, 16, 8, 204800),  # the longest stated sequence
+    (4, 4, 16, 4096),    # batches of 5, 5 and 6
 ])
 def test_order_is_a_bijection_in_key_tile_major_batches(order_exe, B, G, R, S):
     n_small, bp, units = _order(order_exe, B, G, R, S)
@@ -90,6 +91,9 @@ def test_batch_sizes_follow_the_row_budget(order_exe):
     assert _order(order_exe, 4, 8, 4, 4096)[:2] == (2, 16)      # 8.4 MB a head
     assert _order(order_exe, 1, 16, 8, 32768)[:2] == (16, 1)    # 134 MB a head
     assert _order(order_exe, 2, 8, 4, 2048)[:2] == (1, 16)      # all in one batch
+    # 16 kv heads of 33.5 MB: the budget allows 4, 32 key tiles ask for
+    # ceil(222 / 33) = 7, so 3 batches: 5, 5, 6 (the GPU parity test's shape)
+    assert _order(order_exe, 4, 4, 16, 4096)[:2] == (2, 5)
     # the floor: 8 kv heads of 268 MB each at S = 65536 would be one a batch by
     # the budget; 512 key tiles ask for ceil(1.5 * 148 / 513) = 1 -- unchanged
     assert _order(order_exe, 1, 8, 8, 65536)[:2] == (8, 1)

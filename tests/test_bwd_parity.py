@@ -186,6 +186,32 @@ def test_model_workload_bwd_tail():
     check_close("dV(last keys)", to64(dv[0, g, i0:]), rv[i0:])
 
 
+def test_uneven_cta_batches():
+    """B4 H64 G4 S4096: 16 kv heads run in CTA batches of 5, 5 and 6 (the order of
+    bwd_order.cuh).  Checked on a kv head of the first batch and one of the last:
+    dQ of 256 middle rows (every key tile before them contributes, from many
+    CTAs) and of the last 256 rows, dK and dV of the last 256 keys (all of their
+    visible queries are among those rows)."""
+    B, H, G, S = 4, 64, 4, 4096
+    q, k, v, do = make_inputs(B, H, G, S, seed=5, with_grad=True)
+    dq, dk, dv = _gpu_fwd_bwd(q, k, v, do)
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t).all()
+    R, n = H // G, 256
+    for b, g in [(0, 1), (B - 1, G - 1)]:
+        heads = slice(g * R, (g + 1) * R)
+        args = (to64(q[b:b + 1, heads]), to64(k[b:b + 1, g:g + 1]), to64(v[b:b + 1, g:g + 1]),
+                to64(do[b:b + 1, heads]), 0, 0)
+        i0 = S // 2
+        rq, _, _ = oracle.attn_bwd_group_rows(*args, i0, i0 + n)
+        check_close(f"dQ(middle rows)[b{b},g{g}]", to64(dq[b, heads, i0:i0 + n]), rq[:, i0:i0 + n])
+        i0 = S - n
+        rq, rk, rv = oracle.attn_bwd_group_rows(*args, i0, S)
+        check_close(f"dQ(last rows)[b{b},g{g}]", to64(dq[b, heads, i0:]), rq[:, i0:])
+        check_close(f"dK(last keys)[b{b},g{g}]", to64(dk[b, g, i0:]), rk[i0:])
+        check_close(f"dV(last keys)[b{b},g{g}]", to64(dv[b, g, i0:]), rv[i0:])
+
+
 def test_repeat_dk_dv_deterministic():
     q, k, v, do = [t.cuda() for t in make_inputs(1, 8, 2, 700, seed=4, with_grad=True)]
     o, lse = gq.fwd(q, k, v, window=200, n_sink=50)
