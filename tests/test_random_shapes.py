@@ -1,0 +1,126 @@
+"""Seeded random shapes and masks, forward and backward, against the float64
+oracle through the C ABI.
+
+The other parity tests pick their shapes by hand; here a fixed generator draws
+B, kv heads G, group size R (query heads H = R * G), S, causal or not, a window
+and sinks, and the scale, so that combinations nobody chose (S of one row,
+odd group sizes, a window longer than S, sinks past the window, full
+attention) are covered too.  Both forward entry points are checked (online
+maximum and score bound), then the backward.
+
+Scales are drawn up to the stated 1/8 (larger logit spreads are the rounding
+model's cases, tests/test_grad_precision.py).  The mean-abs bound of a bf16
+output adds that output's own mean half-ulp to 2e-3: degenerate shapes (S of
+one or two rows) make outputs sums of a few O(1) terms, where rounding the
+exact result to bf16 alone already averages about 2e-3.
+
+The gradients of these shapes can be larger than on the stated workloads (eight
+heads over 255 queries put |dK| at 4.5), and the backward's operand roundings
+(bf16 dS, D on the bf16 O it is handed) are relative: the float64 model of
+those roundings itself lands 1.8e-2 from the exact dK there before the GPU's
+own O is fed in.  So the backward is held, per kv group, to that model fed the
+GPU's O (half a bf16 ulp + 4e-3: the kernel computes its stated arithmetic),
+and to the oracle within 2e-2 + 2^-8 |ref| (the stated bound plus the
+design's relative operand error).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import causal_grouped_query_gqa_b300 as gq
+from causal_grouped_query_gqa_b300.inputs import make_inputs
+from parity_util import LSE_ABS, MEAN_ABS, _bf16_half_ulp, check_close, to64
+
+pytestmark = pytest.mark.gpu
+
+
+def _draw(n, seed=2024):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n):
+        B = int(rng.integers(1, 4))
+        G = int(rng.integers(1, 5))
+        R = int(rng.choice([1, 2, 3, 5, 8]))
+        S = int(rng.choice([1, 2, 63, 127, 128, 129, 255, 300, 511, 700]))
+        causal = bool(rng.random() < 0.8)
+        window = int(rng.integers(1, S + 200)) if causal and rng.random() < 0.5 else 0
+        n_sink = int(rng.integers(0, S + 2)) if window else 0
+        scale = float(rng.choice([0.125, 0.05, 0.1]))
+        cases.append((B, G * R, G, S, causal, window, n_sink, scale))
+    return cases
+
+
+CASES = _draw(24)
+
+
+def _mask(mask):
+    return {k: mask[k] for k in ("causal", "window", "n_sink")}
+
+
+def _check_bf16(name, got, ref):
+    """Max error as check_close states it; mean error within 2e-3 plus the mean
+    half-ulp of the bf16 result (the rounding any bf16 answer carries)."""
+    check_close(name, got, ref, mean_abs=None)
+    got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
+    mean_err = float(np.abs(got - ref).mean())
+    bound = MEAN_ABS + float(_bf16_half_ulp(np.abs(ref)).mean())
+    assert mean_err <= bound, f"{name}: mean_err={mean_err:.3e} > {bound:.3e}"
+
+
+@pytest.mark.parametrize("B,H,G,S,causal,window,n_sink,scale", CASES,
+                         ids=[f"B{c[0]}H{c[1]}G{c[2]}S{c[3]}{'c' if c[4] else 'f'}w{c[5]}s{c[6]}"
+                              for c in CASES])
+def test_random_shape(B, H, G, S, causal, window, n_sink, scale):
+    q, k, v, do = make_inputs(B, H, G, S, seed=S + 7 * H + 13 * G + B, with_grad=True)
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    mask = dict(causal=causal, window=window, n_sink=n_sink, scale=scale)
+    o, lse = gq.fwd(qd, kd, vd, score_bound=False, **mask)
+    ob, lseb = gq.fwd(qd, kd, vd, score_bound=True, **mask)
+    dq, dk, dv = gq.bwd(qd, kd, vd, o, dod, lse, **mask)
+    torch.cuda.synchronize()
+    assert gq.gqa_attn_last_device_status() == gq.GQA_OK
+    ro, rl = oracle.attn_fwd(to64(q), to64(k), to64(v), **mask)
+    rq, rk, rv = oracle.attn_bwd(to64(q), to64(k), to64(v), to64(do), **mask)
+    for name, got, lg in (("O", o, lse), ("O (score bound)", ob, lseb)):
+        _check_bf16(name, to64(got), ro)
+        check_close("LSE" + name[1:], to64(lg), rl, max_abs=LSE_ABS, mean_abs=None, bf16_out=False)
+    from bwd_rounding_model import model_bwd_group
+    R = H // G
+    for b in range(B):
+        for g in range(G):
+            hs = slice(g * R, (g + 1) * R)
+            m = model_bwd_group(to64(q[b, hs]), to64(k[b, g]), to64(v[b, g]), to64(do[b, hs]),
+                                scale, o=to64(o[b, hs]), p_round="f16_rowscaled", **_mask(mask))
+            got3 = (dq[b, hs], dk[b, g], dv[b, g])
+            ref3 = (rq[b, hs], rk[b, g], rv[b, g])
+            for name, got, mod, ref in zip(("dQ", "dK", "dV"), got3, m, ref3):
+                got = to64(got)
+                e = np.floor(np.log2(np.maximum(np.abs(mod), 1e-30)))
+                err_m = np.abs(got - mod)
+                assert (err_m <= 0.5 * np.exp2(e - 7) + 4e-3).all(), (name, b, g, float(err_m.max()))
+                err = np.abs(got - ref)
+                assert (err <= 2e-2 + np.abs(ref) * 2.0 ** -8).all(), (name, b, g, float(err.max()))
+                assert err.mean() <= MEAN_ABS + float(_bf16_half_ulp(np.abs(ref)).mean()), (name, b, g)
+    # the two forward entry points give the same softmax
+    assert (o.float() - ob.float()).abs().max().item() <= 2e-2
+
+
+@pytest.mark.parametrize("mode", [0, 1], ids=["prepass", "fused"])
+@pytest.mark.parametrize("B,H,G,S,causal,window,n_sink,scale", CASES[:12],
+                         ids=[f"B{c[0]}H{c[1]}G{c[2]}S{c[3]}{'c' if c[4] else 'f'}w{c[5]}s{c[6]}"
+                              for c in CASES[:12]])
+def test_random_shape_yarn(B, H, G, S, causal, window, n_sink, scale, mode):
+    """The same draws through the YaRN forward, both rotation modes, with and
+    without the score bound (default rotary parameters)."""
+    q, k, v = make_inputs(B, H, G, S, seed=S + 5 * H + G)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    mask = dict(causal=causal, window=window, n_sink=n_sink, scale=scale)
+    ro, rl = oracle.attn_fwd_yarn(to64(q), to64(k), to64(v), **mask)
+    for bound in (False, True):
+        o, lse = gq.fwd_yarn(qd, kd, vd, score_bound=bound, rope_mode=mode, **mask)
+        torch.cuda.synchronize()
+        assert gq.gqa_attn_last_device_status() == gq.GQA_OK
+        _check_bf16(f"O (YaRN, bound={bound})", to64(o), ro)
+        check_close(f"LSE (YaRN, bound={bound})", to64(lse), rl, max_abs=LSE_ABS, mean_abs=None,
+                    bf16_out=False)
