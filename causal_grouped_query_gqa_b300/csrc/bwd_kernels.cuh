@@ -551,7 +551,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int h = g * p.R + n / nqt;
         const int qb = qlo + n % nqt;
         const int bh = b * p.H + h;
-        if (!mbar_wait(&bars->qdo_empty[st], ph ^ 1, ab, p.status, kTimeoutCode)) break;
+        if (!mbar_wait<true>(&bars->qdo_empty[st], ph ^ 1, ab, p.status, kTimeoutCode)) break;
         GQA_TRACE_EVENT(1, 0, n);
 #ifdef GQA_INJECT_STALL
         // failure-detection test build only: CTA 0 never loads one step's Q/dO
@@ -583,16 +583,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint64_t v_kmaj = sdesc_sw128(smem_u32(smem + SM_V), 16, 1024);
       const uint32_t q_addr = smem_u32(smem + SM_Q);
       const uint32_t do_addr = smem_u32(smem + SM_DO);
-      bool ok = mbar_wait(&bars->kv_full, 0, ab, p.status, kTimeoutCode);
+      bool ok = mbar_wait<true>(&bars->kv_full, 0, ab, p.status, kTimeoutCode);
       for (int n = 0; ok && n < nsteps; ++n) {
         const int st = n % NSTAGE;
         GQA_TRACE_EVENT(1, 21, n);  // issuer A starts waiting for the step's Q and dO
-        if (!mbar_wait(&bars->qdo_full[st], (n / NSTAGE) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        if (!mbar_wait<true>(&bars->qdo_full[st], (n / NSTAGE) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
         GQA_TRACE_EVENT(1, 22, n);
         // V' (fp16) must be in place before the first dP''^T
-        if (n == 0 && !mbar_wait(&bars->v_ready, 0, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        if (n == 0 && !mbar_wait<true>(&bars->v_ready, 0, ab, p.status, kTimeoutCode)) { ok = false; break; }
         // the P/dS warps must have read the previous step's S^T and dP^T
-        if (n > 0 && !mbar_wait(&bars->st_free, (n - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        if (n > 0 && !mbar_wait<true>(&bars->st_free, (n - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
         GQA_TRACE_EVENT(1, 2, n);
         tc_fence_after_sync();
         const uint64_t q_kmaj = sdesc_sw128(q_addr + st * TILE_BYTES, 16, 1024);
@@ -622,7 +622,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t ds_t = ds_addr + (n & 1) * DS_BYTES;  // this step's dS tile
         const uint64_t do_mn = sdesc_sw128(do_addr + st * TILE_BYTES, TILE_BYTES, 1024);
         GQA_TRACE_EVENT(1, 20, n);  // issuer B starts waiting for the step's P^T
-        if (!mbar_wait(&bars->pt_ready, n & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        if (!mbar_wait<true>(&bars->pt_ready, n & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
         GQA_TRACE_EVENT(1, 4, n);
         tc_fence_after_sync();
         // dV += P^T dO: P^T from TMEM (16 queries = 8 packed columns per step)
@@ -630,7 +630,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int ks = 0; ks < BQ / 16; ++ks)
           mma_bf16_ts(tbase + C_DV, tbase + C_PT + ks * 8, do_mn + ks * 128, id_dv, (n > 0 || ks > 0));
         mma_commit(&bars->pt_free);
-        if (!mbar_wait(&bars->ds_ready, n & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        if (!mbar_wait<true>(&bars->ds_ready, n & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
         tc_fence_after_sync();
         // dK += dS^T Q: dS^T is the shared dS tile read K-major (queries 0-63 in
         // the first 16 KB half, 64-127 in the second; 32 B per 16 queries)
@@ -657,9 +657,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int n = 0; n < nsteps; ++n) {
         const uint64_t ds_mn = sdesc_sw128(ds_addr + (n & 1) * DS_BYTES, TILE_BYTES, 1024);  // LBO: next 64-query half
         // dS of the step is written (which implies K has landed: S^T read it)
-        if (!mbar_wait(&bars->ds_ready, n & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        if (!mbar_wait<true>(&bars->ds_ready, n & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
         // the drain has read the previous dQ tile out of TMEM
-        if (n > 0 && !mbar_wait(&bars->dq_free, (n - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        if (n > 0 && !mbar_wait<true>(&bars->dq_free, (n - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
         GQA_TRACE_EVENT(1, 5, n);
         tc_fence_after_sync();
 #pragma unroll
@@ -688,7 +688,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // row and take cv = 2^-ev, group 0 writes it back once every P/dS thread
     // has read (a barrier every one of the 256 threads reaches, also on abort).
     float cv = 1.f;
-    bool ok = mbar_wait_warp(&bars->kv_full, 0, ab, p.status, kTimeoutCode);
+    bool ok = mbar_wait_warp<true>(&bars->kv_full, 0, ab, p.status, kTimeoutCode);
     {
       uint8_t *vrow = smem + SM_V + r * 128;  // 16-byte chunk c at (c ^ (r & 7))
       uint4 vv[8];
@@ -729,7 +729,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int i0 = qb * BQ;
       const float *lse2 = vec + st * 2 * BQ;
       const float *dlt = lse2 + BQ;
-      if (!mbar_wait_warp(&bars->st_full, n & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+      if (!mbar_wait_warp<true>(&bars->st_full, n & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
       if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 8, n);
       tc_fence_after_sync();
       const bool masked = pair_needs_mask(qb, kb, p);
@@ -758,7 +758,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // dS goes to the step's tile as soon as each half of the row is computed:
       // the tile was last read by the dK and dQ products of step n - 2
       uint8_t *ds_row = ds_row0 + (n & 1) * DS_BYTES;
-      if (n >= 2 && !mbar_wait_warp(&bars->ds_free[n & 1], ((n >> 1) - 1) & 1, ab, p.status, kTimeoutCode)) {
+      if (n >= 2 && !mbar_wait_warp<true>(&bars->ds_free[n & 1], ((n >> 1) - 1) & 1, ab, p.status, kTimeoutCode)) {
         ok = false;
         break;
       }
@@ -779,7 +779,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             make_uint4(pd1[4 * q8], pd1[4 * q8 + 1], pd1[4 * q8 + 2], pd1[4 * q8 + 3]);
       // the previous step's dV must be done with P^T
       if (n > 0) {
-        if (!mbar_wait_warp(&bars->pt_free, (n - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
+        if (!mbar_wait_warp<true>(&bars->pt_free, (n - 1) & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
         tc_fence_after_sync();
       }
       if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 10, n);
@@ -796,7 +796,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_arrive(&bars->ds_ready);
     }
     // epilogue: group 0 writes dV, group 1 writes dK (x scale), one key row per thread
-    if (ok && mbar_wait_warp(&bars->dkv_done, 0, ab, p.status, kTimeoutCode)) {
+    if (ok && mbar_wait_warp<true>(&bars->dkv_done, 0, ab, p.status, kTimeoutCode)) {
       tc_fence_after_sync();
       uint32_t a0[32], a1[32];
       const uint32_t col = wg == 0 ? C_DV : C_DK;
@@ -830,7 +830,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // The four drain warps meet at named barriers below, so they decide
       // together whether to go on: one warp must never leave while the others
       // wait there for it.
-      if (!named_bar_and(1, 128, mbar_wait(&bars->dq_full, n & 1, ab, p.status, kTimeoutCode)))
+      if (!named_bar_and(1, 128, mbar_wait<true>(&bars->dq_full, n & 1, ab, p.status, kTimeoutCode)))
         break;
       if (leader) GQA_TRACE_EVENT(1, 12, n);
       tc_fence_after_sync();
@@ -851,7 +851,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t *a = half == 0 ? a0 : a1;
         // the staging box was last read by the previous pass's reduce
         if (leader) bulk_wait_group_read<0>();
-        if (leader && half == 0) GQA_TRACE_EVENT(1, 13, n);
+        if (leader) GQA_TRACE_EVENT(1, half == 0 ? 13 : 16, n);
         named_bar_sync(1, 128);
 #pragma unroll
         for (int c = 0; c < 8; ++c)

@@ -82,6 +82,19 @@ constexpr uint64_t kWaitBudgetNs = GQA_WAIT_BUDGET_NS;  // 2 s
 // when the phase completes); the budget above is checked between suspensions.
 constexpr uint32_t kSuspendNs = 1000000u;  // 1 ms
 
+// Non-blocking probe of the phase (the thread is never suspended).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Shared abort state of one CTA: once any role gives up, the others stop
 // waiting too and everyone reaches the common exit (where TMEM is freed).
 struct AbortState {
@@ -90,7 +103,11 @@ struct AbortState {
 
 // Waits until the phase with the given parity of `bar` has completed.
 // Returns false (and raises the CTA abort flag and the global status) on timeout
-// or when another role of the CTA has already aborted.
+// or when another role of the CTA has already aborted.  kPoll: probe with
+// test_wait instead of letting the hardware suspend the thread in try_wait;
+// the backward's hand-offs are observed about 2 % sooner that way (the forward
+// is indifferent and keeps the suspending form).
+template <bool kPoll = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, AbortState *ab,
                                           int *status, int code,
                                           uint64_t budget_ns = kWaitBudgetNs) {
@@ -98,7 +115,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, AbortS
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
-    if (mbar_try_wait_sleep(a, parity, kSuspendNs)) return true;
+    if (kPoll ? mbar_test_wait(a, parity) : mbar_try_wait_sleep(a, parity, kSuspendNs)) return true;
     if (ab->flag) return false;
     if (globaltimer_ns() - t0 > budget_ns) {
       ab->flag = 1;
@@ -112,9 +129,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, AbortS
 // acquire semantics, then they vote), for warps whose next instructions are
 // warp-collective (tcgen05.ld/st): on the abort path a lane that saw the phase
 // complete and one that saw the abort flag must not split the warp.
+template <bool kPoll = false>
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, AbortState *ab,
                                                int *status, int code) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, ab, status, code));
+  return __all_sync(0xffffffffu, mbar_wait<kPoll>(bar, parity, ab, status, code));
 }
 
 // Same, without abort bookkeeping: for drains at the exit (bounded, silent).
