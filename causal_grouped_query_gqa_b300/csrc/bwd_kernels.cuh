@@ -605,6 +605,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           mma_bf16_ss(tbase + C_DP, v_kmaj + 2 * ks, do_kmaj + 2 * ks, id_nn16, ks > 0);
         mma_commit(&bars->st_full);
         GQA_TRACE_EVENT(1, 3, n);
+#ifdef GQA_TRACE
+        // trace builds: the time this step's S^T and dP^T are complete, seen by
+        // the issuing thread itself (its next wait comes after that anyway)
+        if (mbar_wait<true>(&bars->st_full, n & 1, ab, p.status, kTimeoutCode)) GQA_TRACE_EVENT(1, 32, n);
+#endif
       }
       mma_commit(&bars->a_done);
       if (!ok) mbar_wait_drain(&bars->a_done, 0);
@@ -729,6 +734,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int i0 = qb * BQ;
       const float *lse2 = vec + st * 2 * BQ;
       const float *dlt = lse2 + BQ;
+      if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 34, n);
       if (!mbar_wait_warp<true>(&bars->st_full, n & 1, ab, p.status, kTimeoutCode)) { ok = false; break; }
       if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 8, n);
       tc_fence_after_sync();
@@ -794,6 +800,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (lane == 0 && (warp == 4 || warp == 8)) GQA_TRACE_EVENT(1, warp == 4 ? 11 : 7, n);
       if (lane == 0) GQA_TRACE_EVENT(1, 20 + warp, n);  // every P/dS warp's hand-over (events 24-31)
       mbar_arrive(&bars->ds_ready);
+      if (warp == 4 && lane == 0) GQA_TRACE_EVENT(1, 33, n);
     }
     // epilogue: group 0 writes dV, group 1 writes dK (x scale), one key row per thread
     if (ok && mbar_wait_warp<true>(&bars->dkv_done, 0, ab, p.status, kTimeoutCode)) {

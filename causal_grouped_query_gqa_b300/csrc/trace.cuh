@@ -10,7 +10,7 @@
 namespace gqa {
 constexpr int kTraceKernels = 2;  // 0 forward, 1 backward main
 constexpr int kTraceCtas = 4;
-constexpr int kTraceEvents = 32;
+constexpr int kTraceEvents = 40;
 constexpr int kTraceSteps = 128;
 }  // namespace gqa
 
