@@ -436,9 +436,12 @@ def run_ours(args, w, rank, world, local_rank):
             res.update({"step": step, "steps": e_steps, "clocks": e_clk,
                         "config": {"B": ew.B, "H": ew.H, "G": ew.G, "S": ew.S,
                                    "window": ew.window, "n_sink": ew.n_sink}})
-            extras[name + {"fwd_yarn": "+yarn", "fwd_yarn_fused": "+yarn_fused", "fwd_fp8": "+fp8",
-                           "fwd_outliers": "+outlier_rows",
-                           "fwd_outliers_plain": "+outlier_rows_plain"}.get(step, "")] = res
+            key = name + {"fwd_yarn": "+yarn", "fwd_yarn_fused": "+yarn_fused", "fwd_fp8": "+fp8",
+                          "fwd_outliers": "+outlier_rows",
+                          "fwd_outliers_plain": "+outlier_rows_plain"}.get(step, "")
+            if key in extras:  # the same workload measured with another step
+                key = name + "+" + step.replace("+", "_")
+            extras[key] = res
             del epb
             torch.cuda.empty_cache()
         out["extra_workloads"] = extras
@@ -451,6 +454,8 @@ EXTRA_WORKLOADS = [
     ("gqa_b2_h32_g8_s2048", "fwd"),
     ("window_b1_h128_g16_s32768_w4096_sink128", "fwd"),
     ("bwd_b4_h32_g8_s4096", "fwd+bwd"),
+    ("window_b1_h128_g16_s32768_w4096_sink128", "fwd+bwd"),  # the window + sink backward at S = 32768
+    ("model_b1_h128_g16_s204800_w65536_sink2048", "fwd+bwd"),  # the model's mask at S = 204800
     ("wide_b1_h128_g16_s8192", "fwd_yarn"),   # YaRN rotary forward (table, q and k rotation, forward)
     ("wide_b1_h128_g16_s8192", "fwd_yarn_fused"),  # the same, query tiles rotated inside the forward
     ("wide_b1_h128_g16_s8192", "fwd_fp8"),    # E4M3 queries and keys (quantised before timing)

@@ -165,7 +165,8 @@ struct MainParams {
   float scale;
   float scale_log2;
   int n_ktiles;
-  int n_small;      // CTA order (bwd_order.cuh): the first n_small batches hold
+  int n_front;      // CTA order (bwd_order.cuh): the first n_front key tiles of every kv head first,
+  int n_small;      // then batches of the others: the first n_small batches hold
   int batch_pairs;  // batch_pairs kv heads, the others batch_pairs + 1
   const float *lse2;  // [B*H][S_pad]  LSE log2(e) + e_i - E_g
   const float *delta; // [B*H][S_pad]  D' = 2^e_i D
@@ -490,7 +491,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // work unit (cta_unit): batches of kv heads, key tiles with the most query
   // tiles first in each
   int kb, pair;
-  cta_unit(static_cast<int>(blockIdx.x), p.n_ktiles, p.n_small, p.batch_pairs, kb, pair);
+  cta_unit(static_cast<int>(blockIdx.x), p.n_ktiles, p.n_front, p.B * p.G, p.n_small, p.batch_pairs,
+           kb, pair);
   const int b = pair / p.G;
   const int g = pair % p.G;
   int qlo, qhi;
@@ -982,7 +984,8 @@ inline int launch(const Problem &pr, const void *q, const void *k, const void *v
     p.scale = pr.scale;
     p.scale_log2 = pr.scale * 1.4426950408889634f;
     p.n_ktiles = (S + BK - 1) / BK;
-    cta_order(B, G, R, S, p.n_ktiles, sm_count, p.n_small, p.batch_pairs);
+    p.n_front = p.causal ? front_tiles(p.n_ktiles, p.window, p.n_sink, BK) : 0;
+    cta_order(B, G, R, S, p.n_ktiles, p.n_front, sm_count, p.n_small, p.batch_pairs);
     p.lse2 = w.lse2;
     p.delta = w.delta;
     p.emin = w.emin;

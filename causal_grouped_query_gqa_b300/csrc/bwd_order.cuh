@@ -17,6 +17,15 @@
 // asks for at least about 1.5 * SMs / (key tiles + 1) pairs in it (the share
 // of one pair's work that falls on an SM, against one key tile's work).
 //
+// With a window, the key tiles that hold sinks are seen by every later query,
+// not by a window's worth: at S = 32768, window 4096, 128 sinks, key tile 0
+// has 256 query tiles against 33 for the others.  Left at the head of their
+// pair's batch, the last pair's sink tiles would start near the end of the
+// launch and run on alone (a batch of one pair there lasts about a fifth of
+// such a tile).  They stream through all of their pair's rows whatever the
+// order, so they gain nothing from the batches: the sink key tiles of every
+// pair run first, key-tile-major, and the batches cover the other key tiles.
+//
 // Host and device code, with no other dependency, so that a host program can
 // check the order on its own.
 #pragma once
@@ -26,11 +35,20 @@ namespace bwd {
 
 constexpr double kOrderBudget = 136.0 * 1024 * 1024;
 
-// Batches of the B * G pairs: n_small batches of batch_pairs pairs, then the
-// rest of batch_pairs + 1.
-__host__ __device__ inline void cta_order(int B, int G, int R, int S, int n_ktiles, int sm_count,
-                                          int &n_small, int &batch_pairs) {
+// Key tiles that run ahead of the batches: those holding sinks when the mask
+// has a window (window > 0 only with causal masking), else none.
+__host__ __device__ inline int front_tiles(int n_ktiles, int window, int n_sink, int tile_keys) {
+  if (window <= 0 || n_sink <= 0) return 0;
+  const long long t = (static_cast<long long>(n_sink) + tile_keys - 1) / tile_keys;
+  return t < n_ktiles ? static_cast<int>(t) : n_ktiles;
+}
+
+// Batches of the B * G pairs over the key tiles after the n_front first ones:
+// n_small batches of batch_pairs pairs, then the rest of batch_pairs + 1.
+__host__ __device__ inline void cta_order(int B, int G, int R, int S, int n_ktiles, int n_front,
+                                          int sm_count, int &n_small, int &batch_pairs) {
   const int pairs = B * G;
+  n_ktiles -= n_front;
   long long m = static_cast<long long>(kOrderBudget / (static_cast<double>(R) * S * 512.0));
   const long long m_tail = (3LL * sm_count + 2LL * (n_ktiles + 1) - 1) / (2LL * (n_ktiles + 1));
   m = m < m_tail ? m_tail : m;
@@ -40,9 +58,17 @@ __host__ __device__ inline void cta_order(int B, int G, int R, int S, int n_ktil
   n_small = nb - pairs % nb;
 }
 
-// CTA u (0 <= u < n_ktiles * B * G) -> key tile kb and pair.
-__host__ __device__ inline void cta_unit(int u, int n_ktiles, int n_small, int batch_pairs, int &kb,
-                                         int &pair) {
+// CTA u (0 <= u < n_ktiles * pairs) -> key tile kb and pair: first the
+// n_front key tiles of every pair, key-tile-major, then the batches.
+__host__ __device__ inline void cta_unit(int u, int n_ktiles, int n_front, int pairs, int n_small,
+                                         int batch_pairs, int &kb, int &pair) {
+  if (u < n_front * pairs) {
+    kb = u / pairs;
+    pair = u % pairs;
+    return;
+  }
+  u -= n_front * pairs;
+  n_ktiles -= n_front;
   const int q = batch_pairs;
   const int small = n_small * q * n_ktiles;  // CTAs of the small batches
   int v, sz, base;
@@ -58,7 +84,7 @@ __host__ __device__ inline void cta_unit(int u, int n_ktiles, int n_small, int b
     sz = q + 1;
     base = n_small * q + bi * (q + 1);
   }
-  kb = v / sz;
+  kb = n_front + v / sz;
   pair = base + v % sz;
 }
 

@@ -2,7 +2,9 @@
 
 A host program built from the header alone enumerates every CTA of a launch
 and prints its (key tile, kv head) unit; the order must visit every unit once,
-keep each batch of kv heads contiguous, and run each batch key-tile-major.
+run the sink key tiles of a windowed mask first (key-tile-major over every kv
+head), keep each batch of kv heads contiguous, and run each batch
+key-tile-major.
 """
 import os
 import shutil
@@ -19,14 +21,15 @@ PROGRAM = r"""
 #include "bwd_order.cuh"
 int main(int argc, char **argv) {
   const int B = atoi(argv[1]), G = atoi(argv[2]), R = atoi(argv[3]), S = atoi(argv[4]);
-  const int sms = atoi(argv[5]);
+  const int sms = atoi(argv[5]), window = atoi(argv[6]), n_sink = atoi(argv[7]);
   const int nk = (S + 127) / 128;
+  const int nf = gqa::bwd::front_tiles(nk, window, n_sink, 128);
   int n_small, bp;
-  gqa::bwd::cta_order(B, G, R, S, nk, sms, n_small, bp);
-  printf("%d %d\n", n_small, bp);
+  gqa::bwd::cta_order(B, G, R, S, nk, nf, sms, n_small, bp);
+  printf("%d %d %d\n", n_small, bp, nf);
   for (int u = 0; u < nk * B * G; ++u) {
     int kb, pair;
-    gqa::bwd::cta_unit(u, nk, n_small, bp, kb, pair);
+    gqa::bwd::cta_unit(u, nk, nf, B * G, n_small, bp, kb, pair);
     printf("%d %d\n", kb, pair);
   }
   return 0;
@@ -46,12 +49,12 @@ def order_exe(tmp_path_factory):
     return str(exe)
 
 
-def _order(exe, B, G, R, S, sms=148):
-    out = subprocess.run([exe, str(B), str(G), str(R), str(S), str(sms)], check=True,
-                         capture_output=True, text=True).stdout.split("\n")
-    n_small, bp = map(int, out[0].split())
+def _order(exe, B, G, R, S, sms=148, window=0, n_sink=0, front=False):
+    out = subprocess.run([exe, str(B), str(G), str(R), str(S), str(sms), str(window), str(n_sink)],
+                         check=True, capture_output=True, text=True).stdout.split("\n")
+    n_small, bp, nf = map(int, out[0].split())
     units = [tuple(map(int, line.split())) for line in out[1:] if line]
-    return n_small, bp, units
+    return (n_small, bp, units, nf) if front else (n_small, bp, units)
 
 
 @pytest.mark.parametrize("B,G,R,S", [
@@ -104,3 +107,36 @@ def test_batch_sizes_follow_the_row_budget(order_exe):
     # the floor on uneven sizes: 268 MB a kv head, 8 key tiles -> at least
     # ceil(222 / 9) = 25 of the 64, so 3 batches: 21, 21, 22
     assert _order(order_exe, 1, 64, 512, 1024)[:2] == (2, 21)
+
+
+@pytest.mark.parametrize("B,G,R,S,window,n_sink,nf", [
+    (1, 16, 8, 32768, 4096, 128, 1),       # the window workload: key tile 0 holds the 128 sinks
+    (1, 16, 8, 204800, 65536, 2048, 16),   # the model's mask: 16 sink key tiles a kv head
+    (2, 3, 4, 1000, 300, 200, 2),          # sinks ending inside the second key tile
+    (1, 2, 4, 300, 100, 1000, 3),          # sinks past the sequence: every key tile in front
+    (1, 16, 8, 8192, 4096, 0, 0),          # a window without sinks: no front
+    (1, 16, 8, 8192, 0, 64, 0),            # sinks without a window are plain causal keys
+])
+def test_sink_key_tiles_run_first(order_exe, B, G, R, S, window, n_sink, nf):
+    n_small, bp, units, got_nf = _order(order_exe, B, G, R, S, window=window, n_sink=n_sink,
+                                        front=True)
+    nk, pairs = -(-S // 128), B * G
+    assert got_nf == nf
+    assert len(units) == nk * pairs
+    assert sorted(units) == [(kb, p) for kb in range(nk) for p in range(pairs)]
+    # the front: key tiles 0 .. nf-1 of every kv head, key tile by key tile
+    assert units[:nf * pairs] == [(kb, p) for kb in range(nf) for p in range(pairs)]
+    rest, nk2 = units[nf * pairs:], nk - nf
+    if nk2 == 0:
+        assert not rest
+        return
+    sizes = [bp] * n_small + [bp + 1] * ((pairs - n_small * bp) // (bp + 1))
+    assert sum(sizes) == pairs
+    pos = first = 0
+    for sz in sizes:
+        batch = rest[pos:pos + sz * nk2]
+        assert [kb for kb, _ in batch] == [kb for kb in range(nf, nk) for _ in range(sz)]
+        assert [p for _, p in batch] == list(range(first, first + sz)) * nk2
+        pos += sz * nk2
+        first += sz
+    assert pos == len(rest)
