@@ -163,6 +163,25 @@ def test_window_bwd_long_context_sampled():
     check_close("dQ", to64(dq[0, 2:4]), rq)
 
 
+def test_window_workload_bwd_group():
+    """B1 H128 G16 S32768, window 4096 + 128 sinks: the backward as the
+    benchmark launches it (the 16 sink key tiles ahead of the one-kv-head
+    batches), checked on the last kv group whole (dQ of its 8 heads, dK, dV)."""
+    w = WORKLOADS["window_b1_h128_g16_s32768_w4096_sink128"]
+    q, k, v, do = make_inputs(w.B, w.H, w.G, w.S, seed=0, with_grad=True)
+    kw = dict(window=w.window, n_sink=w.n_sink)
+    dq, dk, dv = _gpu_fwd_bwd(q, k, v, do, **kw)
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t).all()
+    R, g = w.H // w.G, w.G - 1
+    heads = slice(g * R, (g + 1) * R)
+    rq, rk, rv = oracle.attn_bwd_group(to64(q[:, heads]), to64(k[:, g:g + 1]), to64(v[:, g:g + 1]),
+                                       to64(do[:, heads]), 0, 0, **kw)
+    check_close("dK", to64(dk[0, g]), rk)
+    check_close("dV", to64(dv[0, g]), rv)
+    check_close("dQ", to64(dq[0, heads]), rq)
+
+
 def test_model_workload_bwd_tail():
     """The model-spec mask (window 65536, 2048 sinks) at S = 204800: full
     forward and backward on the GPU, checked on the last kv group: dQ of the
