@@ -436,16 +436,27 @@ def run_ours(args, w, rank, world, local_rank):
             res.update({"step": step, "steps": e_steps, "clocks": e_clk,
                         "config": {"B": ew.B, "H": ew.H, "G": ew.G, "S": ew.S,
                                    "window": ew.window, "n_sink": ew.n_sink}})
-            key = name + {"fwd_yarn": "+yarn", "fwd_yarn_fused": "+yarn_fused", "fwd_fp8": "+fp8",
-                          "fwd_outliers": "+outlier_rows",
-                          "fwd_outliers_plain": "+outlier_rows_plain"}.get(step, "")
-            if key in extras:  # the same workload measured with another step
-                key = name + "+" + step.replace("+", "_")
-            extras[key] = res
+            extras[extra_key(name, step, extras)] = res
             del epb
             torch.cuda.empty_cache()
         out["extra_workloads"] = extras
     return out
+
+
+EXTRA_STEPS = ("fwd", "fwd+bwd", "fwd_yarn", "fwd_yarn_fused", "fwd_fp8", "fwd_outliers",
+               "fwd_outliers_plain")
+
+
+def extra_key(name, step, taken):
+    """Key of an extra workload's entry in the JSON line: the workload's name,
+    a suffix for the variant steps, and the step itself when the plain key is
+    already taken by the same workload measured with another step."""
+    key = name + {"fwd_yarn": "+yarn", "fwd_yarn_fused": "+yarn_fused", "fwd_fp8": "+fp8",
+                  "fwd_outliers": "+outlier_rows",
+                  "fwd_outliers_plain": "+outlier_rows_plain"}.get(step, "")
+    if key in taken:
+        key = name + "+" + step.replace("+", "_")
+    return key
 
 
 # The stated workloads besides the default one, measured in the same run

@@ -30,6 +30,18 @@ def test_workload_flops():
     assert abs(bench.step_flops(w4, False)[0] / 4.2432e12 - 1) < 1e-4
 
 
+def test_extra_workloads_are_known_and_keyed_apart():
+    """Every extra workload of the bench line names a stated workload and a
+    step the bench knows, and no two share a key in the JSON line."""
+    keys = {}
+    for name, step in bench.EXTRA_WORKLOADS:
+        assert name in WORKLOADS and step in bench.EXTRA_STEPS
+        keys[bench.extra_key(name, step, keys)] = (name, step)
+    assert len(keys) == len(bench.EXTRA_WORKLOADS)
+    assert keys["window_b1_h128_g16_s32768_w4096_sink128"][1] == "fwd"
+    assert keys["window_b1_h128_g16_s32768_w4096_sink128+fwd_bwd"][1] == "fwd+bwd"
+
+
 def _free_port():
     with socket.socket() as s:
         s.bind(("127.0.0.1", 0))
