@@ -6,7 +6,8 @@ B, kv heads G, group size R (query heads H = R * G), S, causal or not, a window
 and sinks, and the scale, so that combinations nobody chose (S of one row,
 odd group sizes, a window longer than S, sinks past the window, full
 attention) are covered too.  Both forward entry points are checked (online
-maximum and score bound), then the backward.
+maximum and score bound), then the backward; the YaRN forward (both rotation
+modes) and the FP8 forward run on the first twelve draws.
 
 Scales are drawn up to the stated 1/8 (larger logit spreads are the rounding
 model's cases, tests/test_grad_precision.py).  The mean-abs bound of a bf16
@@ -124,3 +125,27 @@ def test_random_shape_yarn(B, H, G, S, causal, window, n_sink, scale, mode):
         _check_bf16(f"O (YaRN, bound={bound})", to64(o), ro)
         check_close(f"LSE (YaRN, bound={bound})", to64(lse), rl, max_abs=LSE_ABS, mean_abs=None,
                     bf16_out=False)
+
+
+@pytest.mark.parametrize("B,H,G,S,causal,window,n_sink,scale", CASES[:12],
+                         ids=[f"B{c[0]}H{c[1]}G{c[2]}S{c[3]}{'c' if c[4] else 'f'}w{c[5]}s{c[6]}"
+                              for c in CASES[:12]])
+def test_random_shape_fp8(B, H, G, S, causal, window, n_sink, scale):
+    """The same draws through the FP8 forward: q and k quantised to E4M3 on the
+    host (torch's float32 -> float8_e4m3fn cast at a per-tensor scale that
+    keeps every product below 448), so the GPU and the oracle's own decoder
+    see the same bytes; the stated tolerances apply unchanged."""
+    q, k, v = make_inputs(B, H, G, S, seed=S + 3 * H + G)
+    mask = dict(causal=causal, window=window, n_sink=n_sink, scale=scale)
+    enc = []
+    for x in (q, k):
+        inv = torch.tensor(440.0 / float(x.float().abs().max()), dtype=torch.float32)
+        enc.append(((x.float() * inv).to(torch.float8_e4m3fn).view(torch.uint8),
+                    float(np.float32(1.0 / inv.double()))))
+    (q8, qs), (k8, ks) = enc
+    o, lse = gq.fwd_fp8(q8.cuda(), k8.cuda(), v.cuda(), qs, ks, **mask)
+    torch.cuda.synchronize()
+    assert gq.gqa_attn_last_device_status() == gq.GQA_OK
+    ro, rl = oracle.attn_fwd_fp8(q8.numpy(), k8.numpy(), to64(v), qs, ks, **mask)
+    _check_bf16("O (FP8)", to64(o), ro)
+    check_close("LSE (FP8)", to64(lse), rl, max_abs=LSE_ABS, mean_abs=None, bf16_out=False)
